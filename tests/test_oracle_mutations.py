@@ -1,0 +1,121 @@
+"""Planted mistakes in the oracle (on the CPU) must be caught by its pins.
+
+Each test patches one oracle function with a plausible slip and reruns the
+check of the pin that should catch it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from oracle import formats as F
+from oracle import moe as M
+from tests import test_oracle_pins as P
+
+
+def test_swapped_nibbles_break_the_quantiser_bound(monkeypatch):
+    good = F.q4_k_fields
+
+    def swapped(blocks):
+        d, dmin, sc, m, q = good(blocks)
+        q2 = q.copy()
+        q2[..., 0::2, :], q2[..., 1::2, :] = q[..., 1::2, :], q[..., 0::2, :]
+        return d, dmin, sc, m, q2
+
+    monkeypatch.setattr(F, "q4_k_fields", swapped)
+    with pytest.raises(AssertionError):
+        P.test_q4_k_dequant_within_quantiser_error_bound()
+
+
+def test_swapped_scale_high_bits_break_the_bijection(monkeypatch):
+    good = F.q4_k_fields
+
+    def wrong(blocks):
+        d, dmin, sc, m, q = good(blocks)
+        s = np.asarray(blocks, dtype=np.uint8)[..., 4:16].astype(np.int64)
+        sc = sc.copy()
+        for j in range(4, 8):
+            sc[..., j] = (s[..., j + 4] & 0x0F) | ((s[..., j] >> 6) << 4)   # min's top bits
+        return d, dmin, sc, m, q
+
+    monkeypatch.setattr(F, "q4_k_fields", wrong)
+    with pytest.raises(AssertionError):
+        P.test_q4_k_scale_fields_are_a_bijection()
+
+
+def test_round_half_even_breaks_the_q8_1_worked_example(monkeypatch):
+    monkeypatch.setattr(F, "_round_half_away", lambda v32: np.rint(v32.astype(np.float64)))
+    with pytest.raises(AssertionError):
+        P.test_q8_1_worked_example()
+
+
+def test_s_from_sum_of_x_breaks_the_q8_1_worked_example(monkeypatch):
+    good = F.q8_1_quantize
+
+    def wrong(x):
+        a = good(x)
+        xb = np.asarray(x, np.float32).reshape(-1, 32).astype(np.float64)
+        a["s"] = F.fp16(xb.sum(1))
+        return a
+
+    monkeypatch.setattr(F, "q8_1_quantize", wrong)
+    with pytest.raises(AssertionError):
+        P.test_q8_1_worked_example()
+
+
+def test_ties_to_higher_index_break_the_hand_example(monkeypatch):
+    monkeypatch.setattr(M, "topk_sort", lambda l, k=8: sorted(
+        range(len(l)), key=lambda e: (-float(l[e]), -e))[:k])
+    with pytest.raises(AssertionError):
+        P.test_topk_hand_example()
+
+
+def test_gate_up_swapped_breaks_the_tiny_literal(monkeypatch):
+    good = M.matvec_bf16
+
+    def ffn(fmt, gate, up, down, x, x_q8_1=None):
+        g = good(up, x)
+        u = good(gate, x)
+        h = M.silu(g) * u
+        return {"g": g, "u": u, "h": h, "y": good(down, h)}
+
+    monkeypatch.setattr(M, "expert_ffn", ffn)
+    with pytest.raises(AssertionError):
+        P.test_expert_ffn_tiny_literal()
+
+
+def test_unnormalised_weights_break_the_convex_combination(monkeypatch):
+    monkeypatch.setattr(M, "softmax_selected",
+                        lambda l, ids: np.exp(np.asarray(l, np.float64)[list(ids)]))
+    with pytest.raises(AssertionError):
+        P.test_routed_combination_is_convex_over_identical_experts()
+
+
+def test_min_term_sign_flip_breaks_the_dequantised_product(monkeypatch):
+    good = F.q4_k_fields
+
+    def neg_min(blocks):
+        d, dmin, sc, m, q = good(blocks)
+        return d, -dmin, sc, m, q
+
+    def wrong_matvec(w_rows, a):
+        d, dmin, sc, m, _ = neg_min(F.q4_k_rows(w_rows))
+        rows, nsb = d.shape
+        isum = M.q4_k_block_dots(w_rows, a).reshape(rows, nsb, 8).astype(np.float64)
+        da, sa = a["d"].reshape(nsb, 8), a["s"].reshape(nsb, 8)
+        return (d[..., None] * sc * da[None] * isum - dmin[..., None] * m * sa[None]).reshape(rows, -1).sum(1)
+
+    monkeypatch.setattr(M, "matvec_q4_k", wrong_matvec)
+    with pytest.raises(AssertionError):
+        P.test_q4_k_matvec_equals_dequantised_product_when_s_is_exact()
+
+
+def test_missing_first_rounding_breaks_fused_equals_unfused(monkeypatch):
+    def fused_no_t_round(a, b, c, w, eps):
+        s = F.bf16(np.asarray(a) + np.asarray(b) + np.asarray(c))
+        r = 1.0 / np.sqrt(np.mean(s * s) + eps)
+        return s, F.bf16(s * r * np.asarray(w))
+
+    monkeypatch.setattr(M, "add_rmsnorm3", fused_no_t_round)
+    with pytest.raises(AssertionError):
+        P.test_add_rmsnorm3_equals_unfused_chain_bit_exact()

@@ -1,0 +1,247 @@
+/*
+ * si_moe.h - decode-time Mixture-of-Experts FFN stage for GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels. Plain pointers and sizes only.
+ *
+ * The calls follow the statement of the problem on three sparkinfer
+ * pull-request pages:
+ *   [R] "perf(qwen3.6): fused router GEMV+top-k + folded residual-norm (decode)"
+ *       (PR #273), Summary items 1 and 2;
+ *   [S] "perf(qwen3.6): fuse decode kernel launches - shared-expert + GDN
+ *       conv/L2-norm" (PR #239), Summary item 1;
+ *   [Q] "Q4_K shared-expert FFN kernels + Q8_0/Q5_K->Q4_K requant of the MoE FFN
+ *       stage" (PR #359), Summary.
+ *
+ * Conventions for every call below.
+ *  - Pointers named x, w_*, *_out, workspace are DEVICE pointers owned by the
+ *    caller; layer descriptors and handles are host memory. Matrices are
+ *    row-major with the reduction dimension contiguous. Quantised matrices are
+ *    rows of standard blocks: Q4_K 144 bytes per 256 weights, Q8_0 34 bytes per
+ *    32, Q8_1 36 bytes per 32; every row must start on a 16-byte boundary
+ *    (true for the sizes accepted below) and every base pointer must be
+ *    16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls only enqueue work: they never allocate device memory, never
+ *    synchronise (except si_workspace_status) and are valid inside CUDA
+ *    stream capture.
+ *  - Arguments are checked on the host first; on failure the call returns
+ *    SI_ERR_INVALID_ARG, SI_ERR_UNSUPPORTED or SI_ERR_WORKSPACE and enqueues
+ *    nothing. A failed launch returns SI_ERR_CUDA. Errors found on the device
+ *    (corrupted completion handshake, a bounded wait that ran out) are written
+ *    to the status word at the start of the workspace; read it with
+ *    si_workspace_status. No call throws.
+ *  - Workspaces: size them with the matching *_workspace_bytes query, align to
+ *    256 bytes and fill with zeros once before first use (cudaMemset). Their
+ *    completion counters return to zero at the end of every run, so a
+ *    workspace can be replayed from a CUDA graph with no reset node. Two calls
+ *    that may run at the same time must not share a workspace.
+ *  - Consecutive kernels of this library use programmatic dependent launch:
+ *    each kernel may start while its predecessor in the stream is still
+ *    running, and reads, before waiting for that predecessor, only inputs
+ *    produced by work that precedes the predecessor. A caller's kernel placed
+ *    between two calls behaves as an ordinary stream dependency.
+ */
+#ifndef SI_MOE_H
+#define SI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SI_OK = 0,
+  SI_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  SI_ERR_UNSUPPORTED = 2,   /* valid but not implemented (shape / dtype combination) */
+  SI_ERR_WORKSPACE = 3,     /* workspace null, too small or misaligned */
+  SI_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  SI_ERR_HANDSHAKE = 5,     /* device: completion counter inconsistent (workspace not zeroed?) */
+  SI_ERR_TIMEOUT = 6        /* device: a bounded wait ran out */
+} si_status;
+
+/* Element / block types; numbering follows GGML's type ids ([Q] names Q4_K as
+ * type 12 in its routed-down dispatch). */
+typedef enum {
+  SI_F32 = 0,
+  SI_F16 = 1,
+  SI_Q8_0 = 8,
+  SI_Q8_1 = 9,
+  SI_Q4_K = 12,
+  SI_BF16 = 30
+} si_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *si_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+int si_version(void);
+
+/* Bytes of one row of `k` elements of `type` (0 if k is not a multiple of the
+ * type's block size). */
+size_t si_row_bytes(si_dtype type, int64_t k);
+
+/*
+ * si_quantize_q8_1 - activation quantisation ("FNQ Q8_1", "quant_h Q8_1", [Q]).
+ *
+ * For each block of 32 values: amax = max|x|, d = amax / 127 (fp32, IEEE
+ * division), q_i = round-half-away-from-zero(x_i / d) clamped to [-127, 127]
+ * (all 0 when amax = 0), stored d16 = fp16(d), s16 = fp16(d * sum_i q_i).
+ * Output block: {fp16 d16, fp16 s16, int8 q[32]} = 36 bytes.
+ *   x       device, n values of x_type (SI_F32 or SI_BF16)
+ *   n       number of values, > 0 and a multiple of 32
+ *   y_q8_1  device, n/32 * 36 bytes
+ */
+si_status si_quantize_q8_1(const void *x, si_dtype x_type, int64_t n, void *y_q8_1,
+                           void *stream);
+
+/*
+ * si_moe_router_topk - fused router GEMV + top-k + softmax ([R] item 1).
+ *
+ * logits[t][e] = sum_h w_router[e][h] * x[t][h] (fp32 accumulate, split along h
+ * over thread blocks, partial sums reduced in a fixed order: deterministic);
+ * the last block to finish (a wrapping completion counter in the workspace)
+ * selects, per token, the top_k experts ordered by logit descending with ties
+ * to the lower expert index, and writes w[t][r] = exp(l_r - l_0) /
+ * sum_j exp(l_j - l_0) over the selected logits, in rank order.
+ *   x          device [n_tokens][hidden], x_type SI_BF16 or SI_F32
+ *   w_router   device [n_experts][hidden], w_type SI_BF16 or SI_F32
+ *   hidden     multiple of 256, <= 16384
+ *   n_experts  8..256; top_k 1..8 (top_k <= n_experts); n_tokens >= 1
+ *   topk_ids   device int32 [n_tokens][top_k]; topk_w device fp32 [n_tokens][top_k]
+ *   logits_out device fp32 [n_tokens][n_experts], or NULL
+ *   workspace  si_moe_router_workspace_bytes(n_experts, hidden, n_tokens) bytes
+ * NaN logits are outside the contract (selection among NaNs is unspecified).
+ */
+size_t si_moe_router_workspace_bytes(int n_experts, int hidden, int n_tokens);
+si_status si_moe_router_topk(const void *x, si_dtype x_type, const void *w_router,
+                             si_dtype w_type, int hidden, int n_experts, int top_k,
+                             int n_tokens, int32_t *topk_ids, float *topk_w,
+                             float *logits_out, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* One MoE FFN layer: shapes, formats and device weight pointers. */
+typedef struct si_moe_layer {
+  int hidden;                 /* H, multiple of 256 (2048 in the studied models) */
+  int n_experts;              /* E, 8..256 */
+  int top_k;                  /* k, 1..8 */
+  int inter;                  /* I, routed expert width, multiple of 256 */
+  si_dtype expert_type;       /* SI_Q4_K or SI_BF16 */
+  const void *w_gate;         /* [E][I] rows of H */
+  const void *w_up;           /* [E][I] rows of H */
+  const void *w_down;         /* [E][H] rows of I */
+  int shared_inter;           /* I_s, multiple of 256, or 0 for no shared expert */
+  si_dtype shared_type;       /* SI_Q8_0, SI_Q4_K or SI_BF16 (SI_BF16 iff expert_type is) */
+  const void *ws_gate;        /* [I_s] rows of H */
+  const void *ws_up;          /* [I_s] rows of H */
+  const void *ws_down;        /* [H] rows of I_s */
+  const void *w_shared_sigmoid; /* bf16 [H]: shared output is scaled by sigmoid(w . x) */
+  /* used by si_moe_layer_decode and the stack only: */
+  const void *w_router;       /* [E][H] of router_type */
+  si_dtype router_type;       /* SI_BF16 or SI_F32 */
+  const void *w_norm;         /* bf16 [H], RMSNorm weight */
+  float eps;                  /* RMSNorm epsilon */
+} si_moe_layer;
+
+/*
+ * si_moe_ffn_decode - routed experts and shared expert for one token
+ * ([S] item 1, [Q] Summary).
+ *
+ * For rank r = 0..k-1 with expert e = topk_ids[r]: g = G_e x, u = U_e x,
+ * h = silu(g) * u (silu(z) = z / (1 + exp(-z))), y_r = D_e h;
+ * routed = sum_r topk_w[r] * y_r (fp32, rank order) stored as bf16.
+ * Shared: shared = sigmoid(w_shared_sigmoid . x) * D_s(silu(G_s x) * (U_s x)),
+ * stored as bf16. With quantised weights the activations x and h enter the
+ * GEMVs as Q8_1 blocks and every 32-block dot is an exact int32 sum of int8
+ * products, scaled in fp32; with bf16 weights the GEMVs are fp32 dot products
+ * of bf16 weights and fp32 activations.
+ *   x          device bf16 [H]
+ *   x_q8_1     device Q8_1 [H/32] blocks of x, or NULL (then quantised inside)
+ *   topk_ids   device int32 [k]; topk_w device fp32 [k]
+ *   routed_out device bf16 [H]; shared_out device bf16 [H] (ignored if no shared)
+ *   n_tokens   must be 1 (batched tokens: si_moe_ffn_batched)
+ */
+size_t si_moe_ffn_workspace_bytes(const si_moe_layer *L, int n_tokens);
+si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, const void *x,
+                            const void *x_q8_1, const int32_t *topk_ids, const float *topk_w,
+                            void *routed_out, void *shared_out, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * si_add_rmsnorm3 - residual fold into the post-MoE RMSNorm ([R] item 2).
+ *
+ * Per row: t = bf16(a + b); sum = bf16(t + c) (c == NULL: sum = t);
+ * y = bf16(sum * rsqrt(mean(sum^2) + eps) * w_norm), fp32 arithmetic.
+ * Bit-identical to a separate residual add followed by the 2-input norm.
+ *   a, b, c       device bf16 [n_rows][n]
+ *   w_norm        device bf16 [n]
+ *   n             multiple of 256, <= 16384; n_rows >= 1
+ *   sum_out       device bf16 [n_rows][n] (the new residual stream)
+ *   norm_out      device bf16 [n_rows][n]
+ *   norm_q8_1_out device Q8_1 [n_rows][n/32] blocks of norm_out, or NULL
+ * Outputs may not alias inputs.
+ */
+si_status si_add_rmsnorm3(const void *a, const void *b, const void *c, const void *w_norm,
+                          int n, int n_rows, float eps, void *sum_out, void *norm_out,
+                          void *norm_q8_1_out, void *stream);
+
+/*
+ * si_moe_layer_decode - one whole layer for one token: router + top-k,
+ * routed and shared experts, residual fold (the calls above, enqueued back to
+ * back with programmatic dependent launch).
+ *   x          device bf16 [H]: FFN input (the previous norm's output)
+ *   residual   device bf16 [H]: residual stream (may equal x)
+ *   sum_out    device bf16 [H]: new residual; norm_out device bf16 [H]
+ *   topk_ids, topk_w, routed_out, shared_out: optional device outputs (NULL to skip)
+ */
+size_t si_moe_layer_workspace_bytes(const si_moe_layer *L);
+si_status si_moe_layer_decode(const si_moe_layer *L, const void *x, const void *residual,
+                              void *sum_out, void *norm_out, int32_t *topk_ids,
+                              float *topk_w, void *routed_out, void *shared_out,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Layer stack captured as one CUDA graph: n_tokens tokens, each through
+ * n_layers layers in order; layer l takes (norm_out, sum_out) of layer l-1 as
+ * (x, residual); layer 0 takes (x_in[t], x_in[t]). Tokens run one after the
+ * other.
+ *   x_in     device bf16 [n_tokens][H]; y_out device bf16 [n_tokens][H] (last norm)
+ *   sum_out  device bf16 [n_tokens][H] (last residual) or NULL
+ *   ids_out  device int32 [n_tokens][n_layers][k] or NULL
+ *   workspace si_moe_stack_workspace_bytes(layers, n_layers) bytes, zeroed once
+ * The graph captures the pointers: buffers must outlive it. `stream` is used
+ * for capture only (it must not be capturing already); launch on any stream.
+ */
+typedef struct si_graph si_graph;
+size_t si_moe_stack_workspace_bytes(const si_moe_layer *layers, int n_layers);
+si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n_layers, int n_tokens,
+                                    const void *x_in, void *y_out, void *sum_out,
+                                    int32_t *ids_out, void *workspace, size_t workspace_bytes,
+                                    void *stream, si_graph **graph_out);
+si_status si_graph_launch(si_graph *graph, void *stream);
+void si_graph_destroy(si_graph *graph);
+
+/* Synchronises `stream`, then reads the device status word of a workspace
+ * used by any call above (SI_OK if no device-side error was recorded) and
+ * clears it. */
+si_status si_workspace_status(const void *workspace, void *stream, int *status_out);
+
+/* ---- test-only exports (not on the hot path) ---------------------------- */
+
+/* Exact int32 sum_i q_w,i * q_a,i for every (row, 32-block) of a Q4_K matrix
+ * [rows][k] against Q8_1 activations [k/32]; out int32 [rows][k/32]. */
+si_status si_test_q4k_block_dots(const void *w, int rows, int k, const void *a_q8_1,
+                                 int32_t *out, void *stream);
+
+/* The unfused chain the fold replaced: t = bf16(a + b) by one kernel, then the
+ * 2-input norm of (t, c) by a second. Same outputs as si_add_rmsnorm3. */
+si_status si_test_unfused_add_rmsnorm(const void *a, const void *b, const void *c,
+                                      const void *w_norm, int n, int n_rows, float eps,
+                                      void *t_scratch, void *sum_out, void *norm_out,
+                                      void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SI_MOE_H */

@@ -1,0 +1,328 @@
+// Shared device helpers for the decode MoE FFN kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/si_moe.h"
+
+#define SI_DEV __device__ __forceinline__
+
+namespace si {
+
+constexpr int kQK = 32;          // values per Q8_0 / Q8_1 block
+constexpr int kQKK = 256;        // weights per Q4_K super-block
+constexpr int kQ4KBytes = 144;
+constexpr int kQ80Bytes = 34;
+constexpr int kQ81Bytes = 36;
+
+// Bounded waits: polls of an mbarrier before a kernel gives up and records
+// SI_ERR_TIMEOUT. Each try_wait blocks for a short hardware-defined interval,
+// so this bound is well above a second of waiting.
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+// Device status word: first 4 bytes of every workspace.
+struct WsHeader {
+  uint32_t status;
+  uint32_t pad[63];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+SI_DEV void record_status(uint32_t *status, uint32_t code) {
+  if (status) atomicCAS(status, 0u, code);
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+SI_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SI_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk async copy (TMA, 1-D)
+// ---------------------------------------------------------------------------
+SI_DEV uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+SI_DEV void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+SI_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+SI_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+SI_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` with an iteration bound. Returns false on
+// timeout (after recording SI_ERR_TIMEOUT).
+SI_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t *status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  record_status(status, SI_ERR_TIMEOUT);
+  return false;
+}
+
+// Global -> shared bulk copy completing on `bar` (bytes and both addresses
+// must be multiples of 16).
+SI_DEV void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Same, with an L2 eviction hint: weights streamed once per token.
+SI_DEV void bulk_g2s_evict_first(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                 uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+SI_DEV uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// Number formats
+// ---------------------------------------------------------------------------
+SI_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+SI_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+SI_DEV float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+SI_DEV uint16_t bf16_bits(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t *>(&b);
+}
+SI_DEV float half_bits_to_float(uint16_t h) {
+  __half_raw r;
+  r.x = h;
+  return __half2float(__half(r));
+}
+SI_DEV uint16_t float_to_half_bits(float v) {
+  __half h = __float2half_rn(v);
+  return reinterpret_cast<__half_raw &>(h).x;
+}
+
+// Load 8 consecutive values of type T as fp32 (16-byte aligned for bf16).
+template <typename T> struct Load8;
+template <> struct Load8<__nv_bfloat16> {
+  static SI_DEV void run(const void *p, float v[8]) {
+    uint4 u = *reinterpret_cast<const uint4 *>(p);
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+    v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+  }
+};
+template <> struct Load8<float> {
+  static SI_DEV void run(const void *p, float v[8]) {
+    float4 a = reinterpret_cast<const float4 *>(p)[0];
+    float4 b = reinterpret_cast<const float4 *>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Q8_1 block encoder, cooperative over 4 lanes of one warp (lanes 4g..4g+3
+// hold values 8*(lane&3) .. +7 of one 32-value block).
+//   d32 = amax / 127 (IEEE), q = round-half-away(x / d32) clamped to +-127,
+//   d16 = fp16(d32), s16 = fp16(d32 * sum q).
+// Outputs: this lane's 8 codes packed in two words (little-endian bytes) and,
+// identical on the 4 lanes, d16 and s16 bits.
+// ---------------------------------------------------------------------------
+SI_DEV void q8_1_encode_4lanes(const float v[8], uint32_t &q_lo, uint32_t &q_hi, uint16_t &d16,
+                               uint16_t &s16) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const float d = __fdiv_rn(amax, 127.0f);
+  int qi[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int q = 0;
+    if (d > 0.f) {
+      float r = roundf(__fdiv_rn(v[i], d));
+      r = fminf(fmaxf(r, -127.f), 127.f);
+      q = static_cast<int>(r);
+    }
+    qi[i] = q;
+    sum += q;
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  q_lo = (qi[0] & 0xFF) | ((qi[1] & 0xFF) << 8) | ((qi[2] & 0xFF) << 16) |
+         (static_cast<uint32_t>(qi[3] & 0xFF) << 24);
+  q_hi = (qi[4] & 0xFF) | ((qi[5] & 0xFF) << 8) | ((qi[6] & 0xFF) << 16) |
+         (static_cast<uint32_t>(qi[7] & 0xFF) << 24);
+  d16 = float_to_half_bits(d);
+  s16 = float_to_half_bits(__fmul_rn(d, static_cast<float>(sum)));
+}
+
+// ---------------------------------------------------------------------------
+// Activation tile in shared memory, the form every quantised GEMV reads.
+// Codes of 256-value super-block b live at qs + b * kActSbStride (256 bytes of
+// codes + 16 bytes of padding, which keeps the 8 lanes that read 8
+// consecutive super-blocks on distinct banks). d and s are the fp16 block
+// scale and sum widened to fp32, per 32-block.
+// ---------------------------------------------------------------------------
+constexpr int kActSbStride = 272;
+
+struct ActTile {
+  uint8_t *qs;  // [nsb][272]
+  float *d;     // [nsb * 8]
+  float *s;     // [nsb * 8]
+};
+
+// Quantise n (multiple of 256) values of `x` (row of T) into an ActTile, all
+// threads of the block cooperating (blockDim multiple of 32). Ends with
+// __syncthreads().
+template <typename T>
+SI_DEV void quantize_to_tile(const T *x, int n, ActTile t) {
+  const int groups = n / 8;  // 8 values per lane, 4 lanes per 32-block
+  for (int g0 = 0; g0 < groups; g0 += blockDim.x) {
+    const int g = g0 + threadIdx.x;
+    const bool live = g < groups;   // warp-uniform when groups % 32 == 0
+    float v[8];
+    if (live) {
+      Load8<T>::run(x + 8 * g, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    uint32_t lo, hi;
+    uint16_t d16, s16;
+    q8_1_encode_4lanes(v, lo, hi, d16, s16);
+    if (live) {
+      const int blk = g >> 2, part = g & 3;
+      uint8_t *dst = t.qs + (blk >> 3) * kActSbStride + (blk & 7) * 32 + part * 8;
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
+      if (part == 0) {
+        t.d[blk] = half_bits_to_float(d16);
+        t.s[blk] = half_bits_to_float(s16);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Q4_K super-block x Q8_1 activations.
+// w: the 144-byte super-block (16-byte aligned, shared memory);
+// a: the 256 activation codes of the matching super-block (16-byte aligned);
+// isum[j] = exact sum over sub-block j of q_w * q_a.
+// ---------------------------------------------------------------------------
+SI_DEV void q4k_unpack_scales(const uint32_t sw[3], int sc[8], int mn[8]) {
+  // sw = the 12 scale bytes as 3 little-endian words.
+  const uint8_t *b = reinterpret_cast<const uint8_t *>(sw);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    sc[j] = b[j] & 63;
+    mn[j] = b[j + 4] & 63;
+    sc[j + 4] = (b[j + 8] & 0x0F) | ((b[j] >> 6) << 4);
+    mn[j + 4] = (b[j + 8] >> 4) | ((b[j + 4] >> 6) << 4);
+  }
+}
+
+SI_DEV void q4k_isums(const uint4 *w, const uint4 *a, int isum[8], uint32_t &dd,
+                      uint32_t sw[3]) {
+  uint4 h = w[0];  // d, dmin, scale bytes 0..11
+  dd = h.x;
+  sw[0] = h.y; sw[1] = h.z; sw[2] = h.w;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint4 q0 = w[1 + 2 * p], q1 = w[2 + 2 * p];     // 32 code bytes of pair p
+    const uint4 al0 = a[4 * p + 0], al1 = a[4 * p + 1];   // sub-block 2p
+    const uint4 ah0 = a[4 * p + 2], ah1 = a[4 * p + 3];   // sub-block 2p+1
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+    const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+    int lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lo = __dp4a(static_cast<int>(qw[i] & 0x0F0F0F0Fu), static_cast<int>(aw_lo[i]), lo);
+      hi = __dp4a(static_cast<int>((qw[i] >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[i]), hi);
+    }
+    isum[2 * p] = lo;
+    isum[2 * p + 1] = hi;
+  }
+}
+
+// d*sum_j sc_j*d_a(j)*isum_j - dmin*sum_j m_j*s_a(j), fp32.
+SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa) {
+  int isum[8], sc[8], mn[8];
+  uint32_t dd, sw[3];
+  q4k_isums(w, a, isum, dd, sw);
+  q4k_unpack_scales(sw, sc, mn);
+  float acc_d = 0.f, acc_m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    acc_d = fmaf(static_cast<float>(sc[j] * isum[j]), da[j], acc_d);
+    acc_m = fmaf(static_cast<float>(mn[j]), sa[j], acc_m);
+  }
+  const float d = half_bits_to_float(static_cast<uint16_t>(dd & 0xFFFF));
+  const float dmin = half_bits_to_float(static_cast<uint16_t>(dd >> 16));
+  return d * acc_d - dmin * acc_m;
+}
+
+// Q8_0 x Q8_1 over 256 weights = 8 Q8_0 blocks (272 bytes, 16-byte aligned).
+SI_DEV float q80_sb_dot(const uint4 *w, const uint4 *a, const float *da) {
+  uint32_t ww[68];
+#pragma unroll
+  for (int i = 0; i < 17; ++i) {
+    const uint4 u = w[i];
+    ww[4 * i] = u.x; ww[4 * i + 1] = u.y; ww[4 * i + 2] = u.z; ww[4 * i + 3] = u.w;
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    // block b starts at byte 34*b: fp16 d, then 32 code bytes.
+    const int off = 34 * b;
+    const int wi = off >> 2;
+    uint32_t dword = ww[wi];
+    const uint16_t dbits = (off & 2) ? static_cast<uint16_t>(dword >> 16)
+                                     : static_cast<uint16_t>(dword & 0xFFFF);
+    const int cstart = off + 2;  // byte offset of codes, 4-aligned when (off & 2)
+    int s = 0;
+    const uint4 a0 = a[2 * b], a1 = a[2 * b + 1];
+    const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t q;
+      if (cstart & 2)
+        q = __byte_perm(ww[(cstart >> 2) + i], ww[(cstart >> 2) + i + 1], 0x5432);
+      else
+        q = ww[(cstart >> 2) + i];
+      s = __dp4a(static_cast<int>(q), static_cast<int>(aw[i]), s);
+    }
+    acc = fmaf(half_bits_to_float(dbits) * da[b], static_cast<float>(s), acc);
+  }
+  return acc;
+}
+
+}  // namespace si

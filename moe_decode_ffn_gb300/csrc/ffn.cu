@@ -1,0 +1,699 @@
+// Routed experts + shared expert for one decode token.
+//
+// "perf(qwen3.6): fuse decode kernel launches - shared-expert + GDN
+// conv/L2-norm" (sparkinfer PR #239), Summary item 1: gate and up GEMVs and
+// the SwiGLU h = silu(g) * u in one pass over a staged input, the down GEMV
+// separate. "Q4_K shared-expert FFN kernels + Q8_0/Q5_K->Q4_K requant of the
+// MoE FFN stage" (sparkinfer PR #359), Summary: activations as Q8_1, Q4_K and
+// Q8_0 weights dotted with int8 dp4a, h re-quantised to Q8_1 before down.
+// "perf(qwen3.6): fused router GEMV+top-k + folded residual-norm (decode)"
+// (sparkinfer PR #273), "Relation to open PRs": the shared expert's output is
+// gated by sigmoid of a GEMV.
+//
+// GB300 design. The shared expert is treated as one more "slot" next to the k
+// routed experts, so one gate/up launch and one down launch cover all of them.
+//  * gate/up: one thread block per 32-row unit of h (one Q8_1 block of h):
+//    the unit's 32 gate rows and 32 up rows arrive by 1-D TMA bulk copies
+//    (cp.async.bulk) into shared memory in four mbarrier groups, so all of a
+//    block's bytes are requested at once and compute on the first group
+//    overlaps the arrival of the rest. One thread per (row, 256-weight
+//    super-block); 8 lanes reduce a row; the block quantises its 32 h values
+//    to Q8_1 itself. Shared-expert units depend only on x, so their copies
+//    are issued before the kernel waits on the router.
+//  * down: one thread block per tile of output rows, all slots; the weight
+//    rows depend only on the expert ids (written by the router, two kernels
+//    back), so they are requested before waiting on gate/up; only the h tile
+//    (a few KB) is read after the wait. The rank-order combination and the
+//    sigmoid gate are applied in the same block.
+#include "common.cuh"
+#include "host.hpp"
+
+namespace si {
+
+enum SharedFmt { kNoShared = 0, kSharedQ4K = SI_Q4_K, kSharedQ80 = SI_Q8_0 };
+
+constexpr int kGuThreads = 512;   // 32 row pairs x (2 matrices x 8 lanes)
+constexpr int kDownThreads = 256;
+
+struct GateUpParams {
+  const __nv_bfloat16 *x;
+  const uint8_t *x_q8;      // nullable: Q8_1 blocks of x
+  const int32_t *ids;
+  int H, E, k, I, Is;
+  const uint8_t *wg, *wu;   // routed [E][I] rows
+  const uint8_t *wsg, *wsu; // shared [Is] rows
+  int rb_r, rb_s;           // gate/up row bytes, routed / shared
+  int units_routed;         // k * I / 32
+  int8_t *hq;               // [k*I + Is] codes
+  float *hd, *hs;           // [(k*I + Is)/32] block scale / sum (fp16 values)
+  float *hf;                // [k*I + Is] h in fp32
+  uint32_t *status;
+};
+
+struct DownParams {
+  const __nv_bfloat16 *x;
+  const __nv_bfloat16 *w_sg;  // nullable when no shared expert
+  const int32_t *ids;
+  const float *wts;
+  int H, E, k, I, Is, J;
+  const uint8_t *wd, *wsd;    // routed [E][H] rows of I, shared [H] rows of Is
+  int rbd_r, rbd_s;
+  const int8_t *hq;
+  const float *hd, *hs, *hf;
+  __nv_bfloat16 *routed, *shared;
+  uint32_t *status;
+};
+
+// Expert id of routed slot r, validated (an out-of-range id is recorded and
+// replaced by 0 so that no access leaves the weight arrays).
+SI_DEV int load_expert(const int32_t *ids, int r, int E, uint32_t *status) {
+  int e = __ldcg(ids + r);
+  if (e < 0 || e >= E) {
+    record_status(status, SI_ERR_INVALID_ARG);
+    e = 0;
+  }
+  return e;
+}
+
+// Fill an ActTile from Q8_1 blocks in global memory (36-byte blocks).
+SI_DEV void tile_from_q8_1(const uint8_t *src, int n, ActTile t) {
+  const int words = n / 32 * 9;
+  for (int i = threadIdx.x; i < words; i += blockDim.x) {
+    const int blk = i / 9, w = i % 9;
+    const uint32_t v = __ldcg(reinterpret_cast<const uint32_t *>(src + blk * kQ81Bytes) + w);
+    if (w == 0) {
+      t.d[blk] = half_bits_to_float(static_cast<uint16_t>(v & 0xFFFF));
+      t.s[blk] = half_bits_to_float(static_cast<uint16_t>(v >> 16));
+    } else {
+      *reinterpret_cast<uint32_t *>(t.qs + (blk >> 3) * kActSbStride + (blk & 7) * 32 + 4 * (w - 1)) = v;
+    }
+  }
+  __syncthreads();
+}
+
+template <int SFMT>
+SI_DEV float row_dot_q(const uint8_t *row, bool shared, int nsb, int lane8, const ActTile &a) {
+  float acc = 0.f;
+  for (int sb = lane8; sb < nsb; sb += 8) {
+    const uint4 *av = reinterpret_cast<const uint4 *>(a.qs + sb * kActSbStride);
+    if (SFMT == kSharedQ80 && shared)
+      acc += q80_sb_dot(reinterpret_cast<const uint4 *>(row + sb * 272), av, a.d + 8 * sb);
+    else
+      acc += q4k_sb_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes), av, a.d + 8 * sb,
+                        a.s + 8 * sb);
+  }
+  return acc;
+}
+
+// ---------------------------------------------------------------------------
+// gate/up + SiLU gating + Q8_1 of h, quantised weights.
+// ---------------------------------------------------------------------------
+template <int SFMT>
+__global__ void __launch_bounds__(kGuThreads, 1) gateup_q_kernel(GateUpParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nsb = p.H / kQKK;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                 // 4 groups
+  ActTile act;
+  act.qs = smem + 64;
+  act.d = reinterpret_cast<float *>(act.qs + nsb * kActSbStride);
+  act.s = act.d + nsb * 8;
+  float *h_s = act.s + nsb * 8;                                        // [32]
+  const int rb_max = (SFMT == kNoShared) ? p.rb_r : max(p.rb_r, p.rb_s);
+  uint8_t *wbuf = reinterpret_cast<uint8_t *>(h_s + 32);               // [2][32][rb_max]
+  wbuf = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(wbuf) + 127) & ~uintptr_t(127));
+
+  const int unit = blockIdx.x;
+  const bool shared = (SFMT != kNoShared) && unit >= p.units_routed;
+  const int nhb_r = p.I / 32;
+  const int slot = shared ? p.k : unit / nhb_r;
+  const int hb = shared ? unit - p.units_routed : unit % nhb_r;
+  const int rb = shared ? p.rb_s : p.rb_r;
+
+  if (threadIdx.x == 0) {
+    for (int g = 0; g < 4; ++g) mbar_init(&bars[g], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Gate rows of the unit go to wbuf, up rows to wbuf + 32 * rb_max, each at
+  // the unit's own row stride rb; group g (rows 8g..8g+7 of both) completes
+  // on bars[g].
+  uint8_t *gate_buf = wbuf, *up_buf = wbuf + 32 * rb_max;
+  auto issue = [&](const uint8_t *g_rows, const uint8_t *u_rows) {
+    const uint64_t pol = policy_evict_first();
+    const uint32_t bytes = 8u * rb;
+    for (int g = 0; g < 4; ++g) {
+      mbar_arrive_expect_tx(&bars[g], 2 * bytes);
+      bulk_g2s_evict_first(gate_buf + 8 * g * rb, g_rows + static_cast<size_t>(8 * g) * rb, bytes,
+                           &bars[g], pol);
+      bulk_g2s_evict_first(up_buf + 8 * g * rb, u_rows + static_cast<size_t>(8 * g) * rb, bytes,
+                           &bars[g], pol);
+    }
+  };
+  if (shared && threadIdx.x == 0)
+    issue(p.wsg + static_cast<size_t>(hb) * 32 * rb, p.wsu + static_cast<size_t>(hb) * 32 * rb);
+
+  // x -> Q8_1 tile (x comes from work before the predecessor kernel).
+  if (p.x_q8) tile_from_q8_1(p.x_q8, p.H, act);
+  else quantize_to_tile<__nv_bfloat16>(p.x, p.H, act);
+
+  grid_dep_wait();
+  grid_dep_launch();
+
+  if (!shared && threadIdx.x == 0) {
+    const int e = load_expert(p.ids, slot, p.E, p.status);
+    const size_t row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(hb) * 32;
+    issue(p.wg + row0 * rb, p.wu + row0 * rb);
+  }
+
+  const int pr = threadIdx.x >> 4, m = (threadIdx.x >> 3) & 1, lane8 = threadIdx.x & 7;
+  const int grp = pr >> 3;
+  float acc = 0.f;
+  if (mbar_wait_bounded(&bars[grp], 0, p.status))
+    acc = row_dot_q<SFMT>((m ? up_buf : gate_buf) + pr * rb, shared, nsb, lane8, act);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  const float other = __shfl_xor_sync(0xffffffffu, acc, 8);
+  const int slot_off = slot * p.I;   // shared slot: k * I
+  if ((threadIdx.x & 15) == 0) {
+    const float g = acc, u = other;
+    const float h = __fdiv_rn(g, 1.f + expf(-g)) * u;
+    h_s[pr] = h;
+    p.hf[slot_off + hb * 32 + pr] = h;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v[8];
+    const int part = threadIdx.x & 3;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = h_s[8 * part + i];
+    uint32_t lo, hi;
+    uint16_t d16, s16;
+    q8_1_encode_4lanes(v, lo, hi, d16, s16);
+    if (threadIdx.x < 4) {
+      *reinterpret_cast<uint2 *>(p.hq + slot_off + hb * 32 + 8 * part) = make_uint2(lo, hi);
+      if (part == 0) {
+        const int bidx = (slot_off + hb * 32) / 32;
+        p.hd[bidx] = half_bits_to_float(d16);
+        p.hs[bidx] = half_bits_to_float(s16);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// down + rank-order combination + sigmoid-gated shared output, quantised.
+// ---------------------------------------------------------------------------
+SI_DEV float block_dot_bf16(const __nv_bfloat16 *a, const __nv_bfloat16 *b, int n, float *red) {
+  float acc = 0.f;
+  for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+    float va[8], vb[8];
+    Load8<__nv_bfloat16>::run(a + i0, va);
+    Load8<__nv_bfloat16>::run(b + i0, vb);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(va[i], vb[i], acc);
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  float tot = 0.f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) tot += red[i];
+  return tot;
+}
+
+template <int SFMT>
+__global__ void __launch_bounds__(kDownThreads) down_q_kernel(DownParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr bool kShared = SFMT != kNoShared;
+  const int n_slots = p.k + (kShared ? 1 : 0);
+  const int nsb_r = p.I / kQKK, nsb_s = kShared ? p.Is / kQKK : 0;
+  const int nq = p.k * p.I + (kShared ? p.Is : 0);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+  float *wts = reinterpret_cast<float *>(smem + 16);           // [8]
+  float *red = wts + 8;                                        // [8]
+  float *y = red + 8;                                          // [n_slots][J]
+  ActTile act;
+  act.qs = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(y + n_slots * p.J) + 15) & ~uintptr_t(15));
+  act.d = reinterpret_cast<float *>(act.qs + (p.k * nsb_r + nsb_s) * kActSbStride);
+  act.s = act.d + nq / 32;
+  uint8_t *wbuf = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(act.s + nq / 32) + 127) & ~uintptr_t(127));
+
+  const int j0 = blockIdx.x * p.J;
+  const int nrows = min(p.J, p.H - j0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Expert ids and weights come from the router (two kernels back): read
+  // before waiting, and request the weight rows at once.
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_first();
+    const uint32_t br = static_cast<uint32_t>(nrows) * p.rbd_r;
+    const uint32_t bs = kShared ? static_cast<uint32_t>(nrows) * p.rbd_s : 0u;
+    mbar_arrive_expect_tx(bar, p.k * br + bs);
+    for (int r = 0; r < p.k; ++r) {
+      const int e = load_expert(p.ids, r, p.E, p.status);
+      wts[r] = __ldcg(p.wts + r);
+      bulk_g2s_evict_first(wbuf + static_cast<size_t>(r) * p.J * p.rbd_r,
+                           p.wd + (static_cast<size_t>(e) * p.H + j0) * p.rbd_r, br, bar, pol);
+    }
+    if (kShared)
+      bulk_g2s_evict_first(wbuf + static_cast<size_t>(p.k) * p.J * p.rbd_r,
+                           p.wsd + static_cast<size_t>(j0) * p.rbd_s, bs, bar, pol);
+  }
+  float sigma = 0.f;
+  if (kShared) {
+    const float z = block_dot_bf16(p.w_sg, p.x, p.H, red);
+    sigma = __fdiv_rn(1.f, 1.f + expf(-z));
+  }
+
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // h codes of every slot -> tile (super-blocks at the padded stride).
+  for (int c = threadIdx.x; c < nq / 16; c += blockDim.x) {
+    const int o = 16 * c;
+    int base_sb, w;
+    if (o < p.k * p.I) {
+      base_sb = (o / p.I) * nsb_r;
+      w = o % p.I;
+    } else {
+      base_sb = p.k * nsb_r;
+      w = o - p.k * p.I;
+    }
+    *reinterpret_cast<uint4 *>(act.qs + (base_sb + w / kQKK) * kActSbStride + w % kQKK) =
+        __ldcg(reinterpret_cast<const uint4 *>(p.hq + o));
+  }
+  for (int b = threadIdx.x; b < nq / 32; b += blockDim.x) {
+    act.d[b] = __ldcg(p.hd + b);
+    act.s[b] = __ldcg(p.hs + b);
+  }
+  __syncthreads();
+  mbar_wait_bounded(bar, 0, p.status);
+
+  for (int task = threadIdx.x; task < n_slots * p.J; task += blockDim.x) {
+    const int r = task / p.J, jl = task % p.J;
+    if (jl >= nrows) continue;
+    const bool sh = kShared && r == p.k;
+    const int rbd = sh ? p.rbd_s : p.rbd_r;
+    const uint8_t *row = wbuf + static_cast<size_t>(r) * p.J * p.rbd_r + static_cast<size_t>(jl) * rbd;
+    const int nsb = sh ? nsb_s : nsb_r;
+    const int sb0 = r * nsb_r;           // shared slot: k * nsb_r
+    const int blk0 = (r * p.I) / 32;     // shared slot: k * I / 32
+    float acc = 0.f;
+    for (int sb = 0; sb < nsb; ++sb) {
+      const uint4 *av = reinterpret_cast<const uint4 *>(act.qs + (sb0 + sb) * kActSbStride);
+      if (SFMT == kSharedQ80 && sh)
+        acc += q80_sb_dot(reinterpret_cast<const uint4 *>(row + sb * 272), av, act.d + blk0 + 8 * sb);
+      else
+        acc += q4k_sb_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes), av,
+                          act.d + blk0 + 8 * sb, act.s + blk0 + 8 * sb);
+    }
+    y[r * p.J + jl] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < nrows) {
+    const int jl = threadIdx.x;
+    float acc = 0.f;
+    for (int r = 0; r < p.k; ++r) acc = fmaf(wts[r], y[r * p.J + jl], acc);
+    p.routed[j0 + jl] = __float2bfloat16_rn(acc);
+    if (kShared) p.shared[j0 + jl] = __float2bfloat16_rn(sigma * y[p.k * p.J + jl]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 weights: fp32 activations, warp-level dot products.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kGuThreads, 1) gateup_bf16_kernel(GateUpParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  float *xs = reinterpret_cast<float *>(smem);   // [H]
+  const int unit = blockIdx.x;
+  const bool shared = p.Is > 0 && unit >= p.units_routed;
+  const int nhb_r = p.I / 32;
+  const int slot = shared ? p.k : unit / nhb_r;
+  const int hb = shared ? unit - p.units_routed : unit % nhb_r;
+  for (int i0 = 8 * threadIdx.x; i0 < p.H; i0 += 8 * blockDim.x) {
+    float v[8];
+    Load8<__nv_bfloat16>::run(p.x + i0, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xs[i0 + i] = v[i];
+  }
+  __syncthreads();
+  grid_dep_wait();
+  grid_dep_launch();
+  const __nv_bfloat16 *g_rows, *u_rows;
+  if (shared) {
+    g_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wsg) + static_cast<size_t>(hb) * 32 * p.H;
+    u_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wsu) + static_cast<size_t>(hb) * 32 * p.H;
+  } else {
+    const int e = load_expert(p.ids, slot, p.E, p.status);
+    const size_t row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(hb) * 32;
+    g_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wg) + row0 * p.H;
+    u_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wu) + row0 * p.H;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot_off = slot * p.I;
+  for (int pr = 2 * warp; pr < 2 * warp + 2; ++pr) {
+    const __nv_bfloat16 *gr = g_rows + static_cast<size_t>(pr) * p.H;
+    const __nv_bfloat16 *ur = u_rows + static_cast<size_t>(pr) * p.H;
+    float ag = 0.f, au = 0.f;
+    for (int c0 = 0; c0 < p.H; c0 += 256 * 8) {
+      uint4 gw[8], uw[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k0 = c0 + (c * 32 + lane) * 8;
+        if (k0 < p.H) {
+          gw[c] = __ldcs(reinterpret_cast<const uint4 *>(gr + k0));
+          uw[c] = __ldcs(reinterpret_cast<const uint4 *>(ur + k0));
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k0 = c0 + (c * 32 + lane) * 8;
+        if (k0 < p.H) {
+          float gv[8], uv[8];
+          Load8<__nv_bfloat16>::run(&gw[c], gv);
+          Load8<__nv_bfloat16>::run(&uw[c], uv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            ag = fmaf(gv[i], xs[k0 + i], ag);
+            au = fmaf(uv[i], xs[k0 + i], au);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+      ag += __shfl_xor_sync(0xffffffffu, ag, m);
+      au += __shfl_xor_sync(0xffffffffu, au, m);
+    }
+    if (lane == 0) p.hf[slot_off + hb * 32 + pr] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
+  }
+}
+
+__global__ void __launch_bounds__(kDownThreads) down_bf16_kernel(DownParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const bool has_shared = p.Is > 0;
+  const int n_slots = p.k + (has_shared ? 1 : 0);
+  const int nq = p.k * p.I + p.Is;
+  float *wts = reinterpret_cast<float *>(smem);   // [8]
+  float *red = wts + 8;                           // [8]
+  int *eid = reinterpret_cast<int *>(red + 8);    // [8]
+  float *y = reinterpret_cast<float *>(eid + 8);  // [n_slots][J]
+  float *hs = reinterpret_cast<float *>(            // [nq], 16-byte aligned
+      (reinterpret_cast<uintptr_t>(y + n_slots * p.J) + 15) & ~uintptr_t(15));
+  const int j0 = blockIdx.x * p.J;
+  const int nrows = min(p.J, p.H - j0);
+  if (threadIdx.x < p.k) {
+    eid[threadIdx.x] = load_expert(p.ids, threadIdx.x, p.E, p.status);
+    wts[threadIdx.x] = __ldcg(p.wts + threadIdx.x);
+  }
+  float sigma = 0.f;
+  if (has_shared) {
+    const float z = block_dot_bf16(p.w_sg, p.x, p.H, red);
+    sigma = __fdiv_rn(1.f, 1.f + expf(-z));
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int i = threadIdx.x; i < nq / 4; i += blockDim.x)
+    reinterpret_cast<float4 *>(hs)[i] = __ldcg(reinterpret_cast<const float4 *>(p.hf) + i);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane >> 3, l8 = lane & 7;   // 4 tasks per warp, 8 lanes each
+  for (int t0 = 4 * warp; t0 < n_slots * p.J; t0 += 4 * (kDownThreads / 32)) {
+    const int task = t0 + sub;
+    float acc = 0.f;
+    const int r = task / p.J, jl = task % p.J;
+    const bool live = task < n_slots * p.J && jl < nrows;
+    if (live) {
+      const bool sh = has_shared && r == p.k;
+      const int width = sh ? p.Is : p.I;
+      const __nv_bfloat16 *row =
+          sh ? reinterpret_cast<const __nv_bfloat16 *>(p.wsd) + static_cast<size_t>(j0 + jl) * p.Is
+             : reinterpret_cast<const __nv_bfloat16 *>(p.wd) +
+                   (static_cast<size_t>(eid[r]) * p.H + j0 + jl) * p.I;
+      const float *hv = hs + r * p.I;
+      for (int c = l8 * 8; c < width; c += 64) {
+        float wv[8];
+        const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(row + c));
+        Load8<__nv_bfloat16>::run(&u, wv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], hv[c + i], acc);
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (live && l8 == 0) y[r * p.J + jl] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < nrows) {
+    const int jl = threadIdx.x;
+    float acc = 0.f;
+    for (int r = 0; r < p.k; ++r) acc = fmaf(wts[r], y[r * p.J + jl], acc);
+    p.routed[j0 + jl] = __float2bfloat16_rn(acc);
+    if (has_shared) p.shared[j0 + jl] = __float2bfloat16_rn(sigma * y[p.k * p.J + jl]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Test export: exact per-(row, 32-block) integer dots of Q4_K x Q8_1.
+// ---------------------------------------------------------------------------
+__global__ void q4k_block_dots_kernel(const uint8_t *w, int rows, int k, const uint8_t *a,
+                                      int32_t *out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nsb = k / kQKK;
+  ActTile t;
+  t.qs = smem;
+  t.d = reinterpret_cast<float *>(smem + nsb * kActSbStride);
+  t.s = t.d + nsb * 8;
+  tile_from_q8_1(a, k, t);
+  const int r = blockIdx.x;
+  for (int sb = threadIdx.x; sb < nsb; sb += blockDim.x) {
+    int isum[8];
+    uint32_t dd, sw[3];
+    q4k_isums(reinterpret_cast<const uint4 *>(w + (static_cast<size_t>(r) * nsb + sb) * kQ4KBytes),
+              reinterpret_cast<const uint4 *>(t.qs + sb * kActSbStride), isum, dd, sw);
+    for (int j = 0; j < 8; ++j) out[static_cast<size_t>(r) * (k / 32) + 8 * sb + j] = isum[j];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static int row_bytes_of(si_dtype t, int k) {
+  switch (t) {
+    case SI_Q4_K: return k / 256 * kQ4KBytes;
+    case SI_Q8_0: return k / 32 * kQ80Bytes;
+    case SI_BF16: return 2 * k;
+    default: return 0;
+  }
+}
+
+FfnGeom ffn_geom(const si_moe_layer &L) {
+  FfnGeom g{};
+  const bool sh = L.shared_inter > 0;
+  g.n_slots = L.top_k + (sh ? 1 : 0);
+  g.n_units = L.top_k * L.inter / 32 + (sh ? L.shared_inter / 32 : 0);
+  const size_t nq = static_cast<size_t>(L.top_k) * L.inter + (sh ? L.shared_inter : 0);
+  size_t off = sizeof(WsHeader);
+  g.off_hq = off;
+  off = round_up(off + nq, 256);
+  g.off_hd = off;
+  off = round_up(off + nq / 32 * sizeof(float), 256);
+  g.off_hs = off;
+  off = round_up(off + nq / 32 * sizeof(float), 256);
+  g.off_hf = off;
+  off = round_up(off + nq * sizeof(float), 256);
+  g.bytes = off;
+  return g;
+}
+
+si_status ffn_check(const si_moe_layer &L) {
+  const bool sh = L.shared_inter > 0;
+  if (L.hidden < 256 || L.hidden % 256 || L.hidden > 16384) return SI_ERR_INVALID_ARG;
+  if (L.n_experts < 1 || L.n_experts > 256 || L.top_k < 1 || L.top_k > 8 || L.top_k > L.n_experts)
+    return SI_ERR_INVALID_ARG;
+  if (L.inter < 256 || L.inter % 256 || L.inter > 4096) return SI_ERR_INVALID_ARG;
+  if (L.shared_inter < 0 || (sh && (L.shared_inter % 256 || L.shared_inter > 4096)))
+    return SI_ERR_INVALID_ARG;
+  if (!L.w_gate || !L.w_up || !L.w_down) return SI_ERR_INVALID_ARG;
+  if (!aligned16(L.w_gate) || !aligned16(L.w_up) || !aligned16(L.w_down)) return SI_ERR_INVALID_ARG;
+  if (sh) {
+    if (!L.ws_gate || !L.ws_up || !L.ws_down || !L.w_shared_sigmoid) return SI_ERR_INVALID_ARG;
+    if (!aligned16(L.ws_gate) || !aligned16(L.ws_up) || !aligned16(L.ws_down) ||
+        !aligned16(L.w_shared_sigmoid))
+      return SI_ERR_INVALID_ARG;
+  }
+  if (L.expert_type == SI_Q4_K) {
+    if (sh && L.shared_type != SI_Q4_K && L.shared_type != SI_Q8_0) return SI_ERR_UNSUPPORTED;
+    // the gate/up shared-memory buffer holds 64 rows of the widest format
+    const int rb = sh ? max(row_bytes_of(SI_Q4_K, L.hidden), row_bytes_of(L.shared_type, L.hidden))
+                      : row_bytes_of(SI_Q4_K, L.hidden);
+    if (64u * rb + 4096u + L.hidden / 256 * 400u > 227u * 1024u) return SI_ERR_UNSUPPORTED;
+  } else if (L.expert_type == SI_BF16) {
+    if (sh && L.shared_type != SI_BF16) return SI_ERR_UNSUPPORTED;
+  } else {
+    return SI_ERR_UNSUPPORTED;
+  }
+  return SI_OK;
+}
+
+static size_t gateup_q_smem(const si_moe_layer &L, int rb_max) {
+  const int nsb = L.hidden / 256;
+  size_t off = 64 + nsb * kActSbStride + 2 * nsb * 8 * sizeof(float) + 32 * sizeof(float);
+  off = round_up(off, 128);
+  return off + 64u * rb_max + 128;
+}
+
+static size_t down_q_smem(const si_moe_layer &L, int J, int rbd_r, int rbd_s) {
+  const bool sh = L.shared_inter > 0;
+  const int n_slots = L.top_k + (sh ? 1 : 0);
+  const int nq = L.top_k * L.inter + (sh ? L.shared_inter : 0);
+  size_t off = 16 + 16 * sizeof(float) + n_slots * J * sizeof(float);
+  off = round_up(off, 16) + (nq / 256) * kActSbStride + 2 * (nq / 32) * sizeof(float);
+  off = round_up(off, 128);
+  return off + static_cast<size_t>(J) * (L.top_k * rbd_r + (sh ? rbd_s : 0)) + 128;
+}
+
+template <int SFMT>
+static cudaError_t launch_q(const GateUpParams &gp, const DownParams &dp, size_t gsm, size_t dsm,
+                            int down_ctas, int units, cudaStream_t s) {
+  cudaError_t e = allow_smem(gateup_q_kernel<SFMT>, gsm);
+  if (e != cudaSuccess) return e;
+  e = allow_smem(down_q_kernel<SFMT>, dsm);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(gateup_q_kernel<SFMT>, dim3(units), dim3(kGuThreads), gsm, s, gp);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(down_q_kernel<SFMT>, dim3(down_ctas), dim3(kDownThreads), dsm, s, dp);
+}
+
+cudaError_t preload_ffn() {
+  cudaFuncAttributes a;
+  const void *ks[] = {
+      reinterpret_cast<const void *>(gateup_q_kernel<kNoShared>),
+      reinterpret_cast<const void *>(gateup_q_kernel<kSharedQ4K>),
+      reinterpret_cast<const void *>(gateup_q_kernel<kSharedQ80>),
+      reinterpret_cast<const void *>(down_q_kernel<kNoShared>),
+      reinterpret_cast<const void *>(down_q_kernel<kSharedQ4K>),
+      reinterpret_cast<const void *>(down_q_kernel<kSharedQ80>),
+      reinterpret_cast<const void *>(gateup_bf16_kernel),
+      reinterpret_cast<const void *>(down_bf16_kernel),
+      reinterpret_cast<const void *>(q4k_block_dots_kernel)};
+  for (const void *k : ks) {
+    const cudaError_t e = cudaFuncGetAttributes(&a, k);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, const int32_t *ids,
+                     const float *wts, void *routed, void *shared, void *ws, uint32_t *status,
+                     cudaStream_t s) {
+  const FfnGeom g = ffn_geom(L);
+  const bool sh = L.shared_inter > 0;
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  GateUpParams gp{};
+  gp.x = static_cast<const __nv_bfloat16 *>(x);
+  gp.x_q8 = static_cast<const uint8_t *>(x_q8_1);
+  gp.ids = ids;
+  gp.H = L.hidden; gp.E = L.n_experts; gp.k = L.top_k; gp.I = L.inter;
+  gp.Is = sh ? L.shared_inter : 0;
+  gp.wg = static_cast<const uint8_t *>(L.w_gate);
+  gp.wu = static_cast<const uint8_t *>(L.w_up);
+  gp.wsg = static_cast<const uint8_t *>(L.ws_gate);
+  gp.wsu = static_cast<const uint8_t *>(L.ws_up);
+  gp.rb_r = row_bytes_of(L.expert_type, L.hidden);
+  gp.rb_s = sh ? row_bytes_of(L.shared_type, L.hidden) : 0;
+  gp.units_routed = L.top_k * L.inter / 32;
+  gp.hq = reinterpret_cast<int8_t *>(base + g.off_hq);
+  gp.hd = reinterpret_cast<float *>(base + g.off_hd);
+  gp.hs = reinterpret_cast<float *>(base + g.off_hs);
+  gp.hf = reinterpret_cast<float *>(base + g.off_hf);
+  gp.status = status;
+
+  const int sms = sm_count();
+  DownParams dp{};
+  dp.x = gp.x;
+  dp.w_sg = static_cast<const __nv_bfloat16 *>(L.w_shared_sigmoid);
+  dp.ids = ids; dp.wts = wts;
+  dp.H = L.hidden; dp.E = L.n_experts; dp.k = L.top_k; dp.I = L.inter; dp.Is = gp.Is;
+  dp.J = (L.hidden + sms - 1) / sms;
+  dp.wd = static_cast<const uint8_t *>(L.w_down);
+  dp.wsd = static_cast<const uint8_t *>(L.ws_down);
+  dp.rbd_r = row_bytes_of(L.expert_type, L.inter);
+  dp.rbd_s = sh ? row_bytes_of(L.shared_type, L.shared_inter) : 0;
+  dp.hq = gp.hq; dp.hd = gp.hd; dp.hs = gp.hs; dp.hf = gp.hf;
+  dp.routed = static_cast<__nv_bfloat16 *>(routed);
+  dp.shared = static_cast<__nv_bfloat16 *>(shared);
+  dp.status = gp.status;
+  const int down_ctas = (L.hidden + dp.J - 1) / dp.J;
+
+  cudaError_t e;
+  if (L.expert_type == SI_Q4_K) {
+    const int rb_max = sh ? max(gp.rb_r, gp.rb_s) : gp.rb_r;
+    const size_t gsm = gateup_q_smem(L, rb_max);
+    const size_t dsm = down_q_smem(L, dp.J, dp.rbd_r, dp.rbd_s);
+    if (!sh) e = launch_q<kNoShared>(gp, dp, gsm, dsm, down_ctas, g.n_units, s);
+    else if (L.shared_type == SI_Q4_K) e = launch_q<kSharedQ4K>(gp, dp, gsm, dsm, down_ctas, g.n_units, s);
+    else e = launch_q<kSharedQ80>(gp, dp, gsm, dsm, down_ctas, g.n_units, s);
+  } else {
+    const size_t gsm = static_cast<size_t>(L.hidden) * sizeof(float);
+    const int nq = L.top_k * L.inter + gp.Is;
+    const size_t dsm = 24 * sizeof(float) + (g.n_slots * dp.J + nq) * sizeof(float) + 16;
+    e = allow_smem(gateup_bf16_kernel, gsm);
+    if (e == cudaSuccess) e = allow_smem(down_bf16_kernel, dsm);
+    if (e == cudaSuccess)
+      e = launch_pdl(gateup_bf16_kernel, dim3(g.n_units), dim3(kGuThreads), gsm, s, gp);
+    if (e == cudaSuccess)
+      e = launch_pdl(down_bf16_kernel, dim3(down_ctas), dim3(kDownThreads), dsm, s, dp);
+  }
+  return cuda_status(e);
+}
+
+}  // namespace si
+
+using namespace si;
+
+extern "C" size_t si_moe_ffn_workspace_bytes(const si_moe_layer *L, int n_tokens) {
+  if (!L || n_tokens != 1) return 0;
+  return ffn_geom(*L).bytes;
+}
+
+extern "C" si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, const void *x,
+                                       const void *x_q8_1, const int32_t *topk_ids,
+                                       const float *topk_w, void *routed_out, void *shared_out,
+                                       void *workspace, size_t workspace_bytes, void *stream) {
+  if (!L || !x || !topk_ids || !topk_w || !routed_out) return SI_ERR_INVALID_ARG;
+  if (n_tokens != 1) return SI_ERR_UNSUPPORTED;
+  const si_status st = ffn_check(*L);
+  if (st != SI_OK) return st;
+  if (L->shared_inter > 0 && !shared_out) return SI_ERR_INVALID_ARG;
+  if (!aligned16(x) || (x_q8_1 && (reinterpret_cast<uintptr_t>(x_q8_1) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) ||
+      (reinterpret_cast<uintptr_t>(routed_out) & 1u) ||
+      (shared_out && (reinterpret_cast<uintptr_t>(shared_out) & 1u)))
+    return SI_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < ffn_geom(*L).bytes)
+    return SI_ERR_WORKSPACE;
+  return ffn_launch(*L, x, x_q8_1, topk_ids, topk_w, routed_out, shared_out, workspace,
+                    static_cast<uint32_t *>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+extern "C" si_status si_test_q4k_block_dots(const void *w, int rows, int k, const void *a_q8_1,
+                                            int32_t *out, void *stream) {
+  if (!w || !a_q8_1 || !out || rows < 1 || k < 256 || k % 256 || k > 16384) return SI_ERR_INVALID_ARG;
+  if (!aligned16(w) || (reinterpret_cast<uintptr_t>(a_q8_1) & 3u)) return SI_ERR_INVALID_ARG;
+  const size_t smem = (k / 256) * (kActSbStride + 64);
+  cudaError_t e = allow_smem(q4k_block_dots_kernel, smem);
+  if (e == cudaSuccess)
+    e = launch_pdl(q4k_block_dots_kernel, dim3(rows), dim3(128), smem,
+                   static_cast<cudaStream_t>(stream), static_cast<const uint8_t *>(w), rows, k,
+                   static_cast<const uint8_t *>(a_q8_1), out);
+  return cuda_status(e);
+}

@@ -1,0 +1,215 @@
+// Q8_1 activation quantisation and the 3-input residual RMSNorm.
+//
+// "Q4_K shared-expert FFN kernels + Q8_0/Q5_K->Q4_K requant of the MoE FFN
+// stage" (sparkinfer PR #359), Summary: activations enter the expert GEMVs as
+// Q8_1 blocks ("FNQ Q8_1", "quant_h Q8_1").
+// "perf(qwen3.6): fused router GEMV+top-k + folded residual-norm (decode)"
+// (sparkinfer PR #273), Summary item 2: routed + shared + residual folded into
+// one add+RMSNorm, bit-identical to the residual add followed by the 2-input
+// norm.
+#include "common.cuh"
+#include "host.hpp"
+
+namespace si {
+
+// One thread per 8 values; 4 consecutive lanes form one 32-value block.
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const T *__restrict__ x, int64_t n,
+                                                            uint8_t *__restrict__ y) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t groups = n / 8;
+  const bool live = g < groups;
+  float v[8];
+  if (live) {
+    Load8<T>::run(x + 8 * g, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  }
+  uint32_t lo, hi;
+  uint16_t d16, s16;
+  q8_1_encode_4lanes(v, lo, hi, d16, s16);
+  if (!live) return;
+  uint8_t *blk = y + (g >> 2) * kQ81Bytes;
+  const int part = static_cast<int>(g & 3);
+  uint32_t *q = reinterpret_cast<uint32_t *>(blk + 4 + 8 * part);  // 4-byte aligned
+  q[0] = lo;
+  q[1] = hi;
+  if (part == 0) *reinterpret_cast<uint32_t *>(blk) = d16 | (static_cast<uint32_t>(s16) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// add_rmsnorm: one block per row, 256 threads, each owning 8 consecutive
+// values per 2048-value slice.
+//   t = bf16(a + b); s = c ? bf16(t + c) : t; r = rsqrt(mean(s^2) + eps);
+//   y = bf16((s * r) * w); optional Q8_1 of y.
+// With b == nullptr: s = bf16(a + c) (the 2-input norm of the unfused chain).
+// ---------------------------------------------------------------------------
+constexpr int kNormThreads = 256;
+
+__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *p, float v[8]) {
+  Load8<__nv_bfloat16>::run(p, v);
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+    add_rmsnorm_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
+                       const __nv_bfloat16 *__restrict__ c, const __nv_bfloat16 *__restrict__ w,
+                       int n, float eps, __nv_bfloat16 *__restrict__ sum_out,
+                       __nv_bfloat16 *__restrict__ norm_out, uint8_t *__restrict__ q8_out) {
+  extern __shared__ float s_sum[];  // [n]
+  __shared__ float s_red[kNormThreads / 32];
+  const int row = blockIdx.x;
+  const size_t base = static_cast<size_t>(row) * n;
+  grid_dep_wait();
+  grid_dep_launch();
+  float ss = 0.f;
+  for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * kNormThreads) {
+    float va[8], vb[8], vc[8], s[8];
+    load_bf16x8(a + base + i0, va);
+    if (b) load_bf16x8(b + base + i0, vb);
+    if (c) load_bf16x8(c + base + i0, vc);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float t = b ? bf16_round(va[i] + vb[i]) : va[i];
+      s[i] = c ? bf16_round(t + vc[i]) : t;
+      ss = fmaf(s[i], s[i], ss);
+      s_sum[i0 + i] = s[i];
+    }
+    uint4 o;
+    o.x = bf16_bits(s[0]) | (static_cast<uint32_t>(bf16_bits(s[1])) << 16);
+    o.y = bf16_bits(s[2]) | (static_cast<uint32_t>(bf16_bits(s[3])) << 16);
+    o.z = bf16_bits(s[4]) | (static_cast<uint32_t>(bf16_bits(s[5])) << 16);
+    o.w = bf16_bits(s[6]) | (static_cast<uint32_t>(bf16_bits(s[7])) << 16);
+    *reinterpret_cast<uint4 *>(sum_out + base + i0) = o;
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += s_red[i];
+  const float r = rsqrtf(__fdiv_rn(tot, static_cast<float>(n)) + eps);
+  for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * kNormThreads) {
+    float vw[8], y[8];
+    load_bf16x8(w + i0, vw);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = bf16_round(__fmul_rn(__fmul_rn(s_sum[i0 + i], r), vw[i]));
+    uint4 o;
+    o.x = bf16_bits(y[0]) | (static_cast<uint32_t>(bf16_bits(y[1])) << 16);
+    o.y = bf16_bits(y[2]) | (static_cast<uint32_t>(bf16_bits(y[3])) << 16);
+    o.z = bf16_bits(y[4]) | (static_cast<uint32_t>(bf16_bits(y[5])) << 16);
+    o.w = bf16_bits(y[6]) | (static_cast<uint32_t>(bf16_bits(y[7])) << 16);
+    *reinterpret_cast<uint4 *>(norm_out + base + i0) = o;
+    if (q8_out) {  // n % 256 == 0, so whole warps take this branch together
+      uint32_t lo, hi;
+      uint16_t d16, s16;
+      q8_1_encode_4lanes(y, lo, hi, d16, s16);
+      const int g = i0 / 8;
+      uint8_t *blk = q8_out + (static_cast<size_t>(row) * (n / 32) + (g >> 2)) * kQ81Bytes;
+      uint32_t *q = reinterpret_cast<uint32_t *>(blk + 4 + 8 * (g & 3));
+      q[0] = lo;
+      q[1] = hi;
+      if ((g & 3) == 0) *reinterpret_cast<uint32_t *>(blk) = d16 | (static_cast<uint32_t>(s16) << 16);
+    }
+  }
+}
+
+// t = bf16(a + b), the separate residual-add kernel of the unfused chain.
+__global__ void __launch_bounds__(256) residual_add_kernel(const __nv_bfloat16 *__restrict__ a,
+                                                           const __nv_bfloat16 *__restrict__ b,
+                                                           int64_t n, __nv_bfloat16 *__restrict__ t) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (8 * g >= n) return;
+  float va[8], vb[8];
+  load_bf16x8(a + 8 * g, va);
+  load_bf16x8(b + 8 * g, vb);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = bf16_bits(va[2 * i] + vb[2 * i]) |
+           (static_cast<uint32_t>(bf16_bits(va[2 * i + 1] + vb[2 * i + 1])) << 16);
+  *reinterpret_cast<uint4 *>(t + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+cudaError_t preload_norm() {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, add_rmsnorm_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, residual_add_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<float>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<__nv_bfloat16>);
+  return e;
+}
+
+si_status norm_launch(const void *a, const void *b, const void *c, const void *w, int n, int rows,
+                      float eps, void *sum_out, void *norm_out, void *q8_out, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(n) * sizeof(float);
+  cudaError_t e = allow_smem(add_rmsnorm_kernel, smem);
+  if (e != cudaSuccess) return SI_ERR_CUDA;
+  e = launch_pdl(add_rmsnorm_kernel, dim3(rows), dim3(kNormThreads), smem, s,
+                 static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b),
+                 static_cast<const __nv_bfloat16 *>(c), static_cast<const __nv_bfloat16 *>(w), n,
+                 eps, static_cast<__nv_bfloat16 *>(sum_out), static_cast<__nv_bfloat16 *>(norm_out),
+                 static_cast<uint8_t *>(q8_out));
+  return cuda_status(e);
+}
+
+}  // namespace si
+
+using namespace si;
+
+extern "C" si_status si_quantize_q8_1(const void *x, si_dtype x_type, int64_t n, void *y_q8_1,
+                                      void *stream) {
+  if (!x || !y_q8_1 || n <= 0 || n % 32 != 0) return SI_ERR_INVALID_ARG;
+  if (x_type != SI_F32 && x_type != SI_BF16) return SI_ERR_UNSUPPORTED;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y_q8_1) & 3u)) return SI_ERR_INVALID_ARG;
+  const int64_t groups = n / 8;
+  const dim3 grid(static_cast<unsigned>((groups + 255) / 256));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (x_type == SI_F32)
+    e = launch_pdl(quantize_q8_1_kernel<float>, grid, dim3(256), 0, s,
+                   static_cast<const float *>(x), n, static_cast<uint8_t *>(y_q8_1));
+  else
+    e = launch_pdl(quantize_q8_1_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
+                   static_cast<const __nv_bfloat16 *>(x), n, static_cast<uint8_t *>(y_q8_1));
+  return cuda_status(e);
+}
+
+extern "C" si_status si_add_rmsnorm3(const void *a, const void *b, const void *c,
+                                     const void *w_norm, int n, int n_rows, float eps,
+                                     void *sum_out, void *norm_out, void *norm_q8_1_out,
+                                     void *stream) {
+  if (!a || !b || !w_norm || !sum_out || !norm_out) return SI_ERR_INVALID_ARG;
+  if (n <= 0 || n % 256 != 0 || n > 16384 || n_rows <= 0 || !(eps >= 0.f)) return SI_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || (c && !aligned16(c)) || !aligned16(w_norm) ||
+      !aligned16(sum_out) || !aligned16(norm_out) ||
+      (norm_q8_1_out && (reinterpret_cast<uintptr_t>(norm_q8_1_out) & 3u)))
+    return SI_ERR_INVALID_ARG;
+  return norm_launch(a, b, c, w_norm, n, n_rows, eps, sum_out, norm_out, norm_q8_1_out,
+                     static_cast<cudaStream_t>(stream));
+}
+
+extern "C" si_status si_test_unfused_add_rmsnorm(const void *a, const void *b, const void *c,
+                                                 const void *w_norm, int n, int n_rows, float eps,
+                                                 void *t_scratch, void *sum_out, void *norm_out,
+                                                 void *stream) {
+  if (!a || !b || !c || !w_norm || !t_scratch || !sum_out || !norm_out) return SI_ERR_INVALID_ARG;
+  if (n <= 0 || n % 256 != 0 || n > 16384 || n_rows <= 0) return SI_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(w_norm) ||
+      !aligned16(t_scratch) || !aligned16(sum_out) || !aligned16(norm_out))
+    return SI_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t total = static_cast<int64_t>(n) * n_rows;
+  cudaError_t e = launch_pdl(residual_add_kernel, dim3(static_cast<unsigned>((total / 8 + 255) / 256)),
+                             dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(a),
+                             static_cast<const __nv_bfloat16 *>(b), total,
+                             static_cast<__nv_bfloat16 *>(t_scratch));
+  if (e != cudaSuccess) return SI_ERR_CUDA;
+  // 2-input norm of (t, c): b == nullptr in the kernel means s = bf16(t + c).
+  return norm_launch(t_scratch, nullptr, c, w_norm, n, n_rows, eps, sum_out, norm_out, nullptr, s);
+}

@@ -1,0 +1,120 @@
+"""Expert FFNs (routed + shared) on the GPU against the oracle, full-size
+256-expert layers generated on the device."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import moe_decode_ffn_gb300 as m
+from oracle import formats as F
+from oracle import moe as M
+from oracle import parity as P
+from tests.gpu_common import bf16_np, device_layer, host_layer_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    m.build()
+    m.library()
+
+
+@pytest.mark.parametrize("rows,k", [(64, 2048), (48, 512), (5, 768)])
+def test_q4k_block_dots_bit_exact(rows, k):
+    w = gen.encode_q4_k(gen.float_weights(7, 0, gen.ROLE_GATE, rows, rows, k))
+    x = gen.normal([gen.stream_key(8, k)], k, 0.0, 1.0)[0]
+    a = F.q8_1_quantize(x.numpy())
+    a_bytes = torch.from_numpy(F.q8_1_to_bytes(a).reshape(-1))
+    got = m.si_test_q4k_block_dots(w.cuda(), rows, k, a_bytes.cuda()).cpu().numpy()
+    assert np.array_equal(got, M.q4_k_block_dots(w.numpy(), a))
+
+
+def _routing(seed, spec):
+    """Seeded distinct expert ids and softmax weights (inputs of the FFN call)."""
+    keys = gen.raw64([gen.stream_key(seed, 999)], spec.n_experts)[0]
+    ids = torch.argsort(keys)[: spec.top_k].to(torch.int32)
+    z = gen.normal([gen.stream_key(seed, 998)], spec.top_k, 0.0, 1.0)[0].double()
+    w = torch.softmax(torch.sort(z, descending=True).values, 0).to(torch.float32)
+    return ids, w
+
+
+SPECS = {
+    "q4k_shared_q8_0": gen.Q4K_LAYER_SHARED_Q8_0,
+    "q4k_shared_q4k": gen.Q4K_LAYER_SHARED_Q4_K,
+    "bf16": gen.BF16_LAYER,
+    "q4k_128e_i768": gen.Q4K_LAYER_128E,
+}
+
+
+@pytest.mark.parametrize("name", list(SPECS))
+@pytest.mark.parametrize("seed", [0, 1])
+def test_ffn_decode_against_oracle(name, seed):
+    spec = SPECS[name]
+    dev = device_layer(spec, 100, 0)
+    ids, w = _routing(seed, spec)
+    x = gen.make_tokens(500 + seed, 1)[0]
+    ws = m.workspace(m.ffn_workspace_bytes(dev))
+    routed, shared = m.si_moe_ffn_decode(dev, x.cuda(), ids.cuda(), w.cuda(), ws=ws)
+    assert m.si_workspace_status(ws) == m.SI_OK
+    host = host_layer_for(spec, 100, 0, ids.tolist())
+    f = M.moe_ffn(host, M.as_f64(x), ids.tolist(), w.double().numpy())
+    ok, rep = P.float_parity(bf16_np(routed), F.bf16(f["routed"]))
+    assert ok, "routed " + rep
+    if spec.shared_inter:
+        ok, rep = P.float_parity(bf16_np(shared), F.bf16(f["shared"]))
+        assert ok, "shared " + rep
+
+
+def test_ffn_given_q8_1_input_matches_internal_quantisation():
+    spec = gen.Q4K_LAYER_SHARED_Q8_0
+    dev = device_layer(spec, 100, 0)
+    ids, w = _routing(3, spec)
+    x = gen.make_tokens(503, 1)[0].cuda()
+    xq = m.si_quantize_q8_1(x)
+    r1, s1 = m.si_moe_ffn_decode(dev, x, ids.cuda(), w.cuda())
+    r2, s2 = m.si_moe_ffn_decode(dev, x, ids.cuda(), w.cuda(), x_q8_1=xq)
+    assert torch.equal(r1, r2) and torch.equal(s1, s2)
+
+
+def test_ffn_h_codes_follow_the_oracle():
+    """The gate/up kernel's Q8_1 codes of h: almost all equal to the oracle's
+    (h is fp32 on both sides; rounding-order differences may move a value
+    across a code boundary by one)."""
+    spec = gen.Q4K_LAYER_SHARED_Q4_K
+    dev = device_layer(spec, 100, 0)
+    ids, w = _routing(4, spec)
+    x = gen.make_tokens(504, 1)[0]
+    ws = m.workspace(m.ffn_workspace_bytes(dev))
+    m.si_moe_ffn_decode(dev, x.cuda(), ids.cuda(), w.cuda(), ws=ws)
+    torch.cuda.synchronize()
+    nq = spec.top_k * spec.inter + spec.shared_inter
+    hq = ws[256:256 + nq].cpu().view(torch.int8).numpy().astype(np.int64)
+    host = host_layer_for(spec, 100, 0, ids.tolist())
+    f = M.moe_ffn(host, M.as_f64(x), ids.tolist(), w.double().numpy())
+    ref = np.concatenate([e["h_q8_1"]["q"].reshape(-1) for e in f["experts"]] +
+                         [f["shared_expert"]["h_q8_1"]["q"].reshape(-1)])
+    diff = np.abs(hq - ref)
+    assert diff.max() <= 1 and (diff != 0).mean() < 2e-3
+
+
+def test_ffn_rejects_bad_arguments():
+    spec = gen.Q4K_LAYER_SHARED_Q8_0
+    dev = device_layer(spec, 100, 0)
+    ids, w = _routing(0, spec)
+    x = gen.make_tokens(1, 1)[0].cuda()
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.SiError) as e:
+        m.si_moe_ffn_decode(dev, x, ids.cuda(), w.cuda(), ws=small)
+    assert e.value.status == m.SI_ERR_WORKSPACE
+
+
+def test_ffn_out_of_range_expert_is_reported_not_faulted():
+    spec = gen.Q4K_LAYER_SHARED_Q8_0
+    dev = device_layer(spec, 100, 0)
+    _, w = _routing(0, spec)
+    ids = torch.tensor([0, 1, 2, 3, 4, 5, 6, 100000], dtype=torch.int32)
+    x = gen.make_tokens(1, 1)[0].cuda()
+    ws = m.workspace(m.ffn_workspace_bytes(dev))
+    m.si_moe_ffn_decode(dev, x, ids.cuda(), w.cuda(), ws=ws)
+    assert m.si_workspace_status(ws) == m.SI_ERR_INVALID_ARG

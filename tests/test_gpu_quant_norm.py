@@ -1,0 +1,91 @@
+"""Q8_1 quantiser and residual norm on the GPU against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import moe_decode_ffn_gb300 as m
+from oracle import formats as F
+from oracle import moe as M
+from oracle import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    m.build()
+    m.library()
+
+
+def _activation_vector(n, seed):
+    x = gen.normal([gen.stream_key(seed, n, 77)], n, 0.0, 1.0)[0]
+    scale = gen.uniform_int([gen.stream_key(seed, n, 78)], n // 32, -8, 6)[0].to(torch.float32)
+    x = x * torch.pow(torch.tensor(10.0), scale).repeat_interleave(32) / 10
+    nb = n // 32
+    if nb > 3:
+        x[0:32] = 0.0                                           # all-zero block
+        x[32:64] = torch.arange(-16, 16, dtype=torch.float32) / 64 + 0.0078125   # exact halves
+        x[64:96] = torch.tensor([127.0] + [-62.5, 0.5, 2.5, -0.25] * 7 + [1, 2, 3]) / 64
+    return x
+
+
+@pytest.mark.parametrize("n", [32, 256, 2048, 32 * 1001, 1 << 20])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_q8_1_bit_exact(n, dtype):
+    x = _activation_vector(n, 5).to(dtype)
+    got = m.si_quantize_q8_1(x.cuda()).cpu().numpy().reshape(-1, 36)
+    ref = F.q8_1_to_bytes(F.q8_1_quantize(x.float().numpy()))
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+
+
+def _norm_inputs(rows, n, seed, scales=(0.1, 0.2, 1.0)):
+    keys = [gen.stream_key(seed, i, rows, n) for i in range(4)]
+    vs = [gen.to_bf16(gen.normal([keys[i]], rows * n, 0.0, s)[0].reshape(rows, n))
+          for i, s in enumerate(scales)]
+    w = gen.to_bf16(gen.normal([keys[3]], n, 1.0, 0.1)[0])
+    return vs, w
+
+
+@pytest.mark.parametrize("rows,n", [(1, 2048), (3, 256), (5, 4096), (2, 16384)])
+def test_add_rmsnorm3_against_oracle(rows, n):
+    (a, b, c), w = _norm_inputs(rows, n, 9)
+    s, y, q8 = m.si_add_rmsnorm3(a.cuda(), b.cuda(), c.cuda(), w.cuda(), 1e-6, want_q8=True)
+    s, y, q8 = s.cpu(), y.cpu(), q8.cpu().numpy().reshape(rows, -1, 36)
+    for r in range(rows):
+        rs, ry = M.add_rmsnorm3(M.as_f64(a[r]), M.as_f64(b[r]), M.as_f64(c[r]), M.as_f64(w), 1e-6)
+        assert np.array_equal(M.as_f64(s[r]), rs)              # two fp32 adds: exact
+        ok, rep = P.float_parity(M.as_f64(y[r]), ry)
+        assert ok, rep
+        # the fused Q8_1 output equals the quantiser applied to the kernel's own y
+        assert np.array_equal(q8[r], F.q8_1_to_bytes(F.q8_1_quantize(M.as_f64(y[r]))))
+
+
+def test_add_rmsnorm3_equals_unfused_chain_on_gpu():
+    (a, b, c), w = _norm_inputs(4, 2048, 11)
+    s1, y1, _ = m.si_add_rmsnorm3(a.cuda(), b.cuda(), c.cuda(), w.cuda(), 1e-6)
+    s2, y2 = m.si_test_unfused_add_rmsnorm(a.cuda(), b.cuda(), c.cuda(), w.cuda(), 1e-6)
+    assert torch.equal(s1, s2) and torch.equal(y1, y2)
+
+
+def test_add_rmsnorm_two_input_mode():
+    (a, b, _), w = _norm_inputs(2, 2048, 12)
+    s, y, _ = m.si_add_rmsnorm3(a.cuda(), b.cuda(), None, w.cuda(), 1e-6)
+    for r in range(2):
+        rs, ry = M.add_rmsnorm2(M.as_f64(a[r]), M.as_f64(b[r]), M.as_f64(w), 1e-6)
+        assert np.array_equal(M.as_f64(s[r].cpu()), rs)
+        ok, rep = P.float_parity(M.as_f64(y[r].cpu()), ry)
+        assert ok, rep
+
+
+def test_rmsnorm_zero_and_constant_rows():
+    n = 2048
+    a = torch.zeros(2, n, dtype=torch.bfloat16)
+    a[1] = 0.75
+    z = torch.zeros_like(a)
+    w = gen.to_bf16(torch.linspace(0.5, 1.5, n))
+    s, y, _ = m.si_add_rmsnorm3(a.cuda(), z.cuda(), z.cuda(), w.cuda(), 1e-6)
+    y = M.as_f64(y.cpu())
+    assert np.all(y[0] == 0)
+    ref = F.bf16(M.as_f64(w) * 0.75 / np.sqrt(0.75 ** 2 + 1e-6))
+    assert np.all(np.abs(y[1] - ref) <= P.ulp_bf16(ref))

@@ -123,6 +123,14 @@ def uniform_int(keys, n: int, lo: int, hi: int, device="cpu") -> torch.Tensor:
     return torch.remainder(v, hi - lo + 1) + lo
 
 
+def _div(a: torch.Tensor, c: float) -> torch.Tensor:
+    """IEEE division by a constant on any device. (On CUDA, dividing by a
+    Python scalar is evaluated as a multiplication by its reciprocal, which
+    can differ from the CPU result in the last bit; dividing by a tensor of
+    the same shape is a true division everywhere.)"""
+    return a / torch.full_like(a, c)
+
+
 def to_bf16(w32: torch.Tensor) -> torch.Tensor:
     """Round fp32 to bf16, round-to-nearest-even."""
     return w32.to(torch.bfloat16)
@@ -139,7 +147,7 @@ def encode_q8_0(w: torch.Tensor) -> torch.Tensor:
     assert k % QK8 == 0
     b = w.reshape(rows, k // QK8, QK8)
     amax = b.abs().amax(-1)
-    d16 = (amax / 127.0).to(torch.float16)
+    d16 = _div(amax, 127.0).to(torch.float16)
     df = d16.to(torch.float32)
     safe = torch.where(df > 0, df, torch.ones_like(df))
     q = torch.where(df[..., None] > 0, torch.round(b / safe[..., None]).clamp(-127, 127),
@@ -167,10 +175,10 @@ def q4_k_params(w: torch.Tensor):
     x = w.reshape(rows, nsb, 8, 32)
     lo = torch.clamp(x.amin(-1), max=0.0)
     hi = x.amax(-1)
-    s = (hi - lo) / 15.0
+    s = _div(hi - lo, 15.0)
     mneg = -lo
-    d16 = (s.amax(-1) / 63.0).to(torch.float16)
-    dmin16 = (mneg.amax(-1) / 63.0).to(torch.float16)
+    d16 = _div(s.amax(-1), 63.0).to(torch.float16)
+    dmin16 = _div(mneg.amax(-1), 63.0).to(torch.float16)
     df = d16.to(torch.float32)[..., None]
     dmf = dmin16.to(torch.float32)[..., None]
     one = torch.ones_like(df)
@@ -263,9 +271,11 @@ Q4K_LAYER_128E = LayerSpec(n_experts=128, inter=768, shared_inter=0, shared_type
 
 
 def _weights(seed, layer, role, experts, rows, cols, fmt, device, std=WEIGHT_STD, mean=0.0,
-             chunk=8):
+             chunk=None):
     """Encoded weights for ``experts`` (list) of one role: uint8 [len, rows, rb]."""
     rb = row_bytes(fmt, cols)
+    if chunk is None:   # experts per batch of elementwise ops (a few hundred MB of temporaries)
+        chunk = max(1, min(64, (1 << 25) // (rows * cols))) if str(device).startswith("cuda") else 8
     out = torch.empty(len(experts), rows, rb, dtype=torch.uint8, device=device)
     for i in range(0, len(experts), chunk):
         sel = experts[i:i + chunk]

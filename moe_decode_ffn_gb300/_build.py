@@ -38,35 +38,42 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, build_dir: str = BUILD, extra=()) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
     path = os.path.join(CSRC, src)
     if _stale(obj, [path] + HEADERS):
-        cmd = [nvcc()] + FLAGS + ["-c", path, "-o", obj]
+        cmd = [nvcc()] + FLAGS + list(extra) + ["-c", path, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every translation unit and link libsi_moe.so; return its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Compile every translation unit and link libsi_moe.so; return its path.
+
+    trace=True builds libsi_moe_trace.so instead, with per-phase timestamp
+    recording (-DSI_TRACE) for profiling; the product library never has it.
+    """
+    build_dir = BUILD + ("_trace" if trace else "")
+    lib = LIB.replace(".so", "_trace.so") if trace else LIB
+    extra = ["-DSI_TRACE"] if trace else []
+    os.makedirs(build_dir, exist_ok=True)
     if force:
-        for f in os.listdir(BUILD):
-            os.remove(os.path.join(BUILD, f))
+        for f in os.listdir(build_dir):
+            os.remove(os.path.join(build_dir, f))
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(_compile, SOURCES))
-    if force or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda src: _compile(src, build_dir, extra), SOURCES))
+    if force or _stale(lib, objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     if verbose:
-        print("built", LIB)
-    return LIB
+        print("built", lib)
+    return lib
 
 
 if __name__ == "__main__":

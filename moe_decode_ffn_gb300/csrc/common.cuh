@@ -35,6 +35,31 @@ SI_DEV void record_status(uint32_t *status, uint32_t code) {
 }
 
 // ---------------------------------------------------------------------------
+// Phase tracing (profiling builds only: compiled with -DSI_TRACE). Thread 0 of
+// each block stamps %globaltimer (ns) at numbered phases into a per-file
+// device buffer [kernel][block][phase]; si_trace_dump copies it out.
+// ---------------------------------------------------------------------------
+constexpr int kTraceKernels = 4, kTraceBlocks = 1024, kTracePhases = 16;
+#ifdef SI_TRACE
+SI_DEV uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define SI_TRACE_BUFFER static __device__ uint64_t g_si_trace[kTraceKernels][kTraceBlocks][kTracePhases];
+#define SI_TRACE_MARK(kernel, phase)                                                         \
+  do {                                                                                       \
+    if (threadIdx.x == 0 && blockIdx.x < kTraceBlocks && blockIdx.y == 0)                    \
+      g_si_trace[(kernel)][blockIdx.x][(phase)] = globaltimer_ns();                          \
+  } while (0)
+#else
+#define SI_TRACE_BUFFER
+#define SI_TRACE_MARK(kernel, phase) \
+  do {                               \
+  } while (0)
+#endif
+
+// ---------------------------------------------------------------------------
 // Programmatic dependent launch
 // ---------------------------------------------------------------------------
 SI_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -161,18 +186,15 @@ SI_DEV void q8_1_encode_4lanes(const float v[8], uint32_t &q_lo, uint32_t &q_hi,
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   const float d = __fdiv_rn(amax, 127.0f);
+  const bool live = d > 0.f;          // d == 0: every code is 0
+  const float dd = live ? d : 1.0f;
   int qi[8];
   int sum = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    int q = 0;
-    if (d > 0.f) {
-      float r = roundf(__fdiv_rn(v[i], d));
-      r = fminf(fmaxf(r, -127.f), 127.f);
-      q = static_cast<int>(r);
-    }
-    qi[i] = q;
-    sum += q;
+    const float r = fminf(fmaxf(roundf(__fdiv_rn(v[i], dd)), -127.f), 127.f);
+    qi[i] = live ? static_cast<int>(r) : 0;
+    sum += qi[i];
   }
   sum += __shfl_xor_sync(0xffffffffu, sum, 1);
   sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -182,6 +204,25 @@ SI_DEV void q8_1_encode_4lanes(const float v[8], uint32_t &q_lo, uint32_t &q_hi,
          (static_cast<uint32_t>(qi[7] & 0xFF) << 24);
   d16 = float_to_half_bits(d);
   s16 = float_to_half_bits(__fmul_rn(d, static_cast<float>(sum)));
+}
+
+// Same encoding with one value per lane: the 32 lanes of a warp hold one
+// block (lane i = value i). One division per lane keeps the dependent chain
+// short. Returns this lane's code; d16 / s16 identical on every lane.
+SI_DEV int q8_1_encode_warp(float v, uint16_t &d16, uint16_t &s16) {
+  float amax = fabsf(v);
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const bool live = d > 0.f;
+  const float r = fminf(fmaxf(roundf(__fdiv_rn(v, live ? d : 1.0f)), -127.f), 127.f);
+  const int q = live ? static_cast<int>(r) : 0;
+  int sum = q;
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+  d16 = float_to_half_bits(d);
+  s16 = float_to_half_bits(__fmul_rn(d, static_cast<float>(sum)));
+  return q;
 }
 
 // ---------------------------------------------------------------------------
@@ -271,6 +312,46 @@ SI_DEV void q4k_isums(const uint4 *w, const uint4 *a, int isum[8], uint32_t &dd,
     isum[2 * p] = lo;
     isum[2 * p + 1] = hi;
   }
+}
+
+// Half of a Q4_K super-block (sub-blocks 4h..4h+3, 128 weights):
+// d*sum_j sc_j*d_a(j)*isum_j - dmin*sum_j m_j*s_a(j) over those j, fp32.
+SI_DEV float q4k_half_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa,
+                          int h) {
+  const uint4 hd = w[0];
+  int sc8[8], mn8[8];
+  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
+  q4k_unpack_scales(sw, sc8, mn8);
+  int sc[4], mn[4];   // this half's four sub-blocks (selects, no runtime indexing)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    sc[i] = h ? sc8[4 + i] : sc8[i];
+    mn[i] = h ? mn8[4 + i] : mn8[i];
+  }
+  float acc_d = 0.f, acc_m = 0.f;
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    const int p = 2 * h + pp;
+    const uint4 q0 = w[1 + 2 * p], q1 = w[2 + 2 * p];
+    const uint4 al0 = a[4 * p + 0], al1 = a[4 * p + 1];
+    const uint4 ah0 = a[4 * p + 2], ah1 = a[4 * p + 3];
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+    const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+    int lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lo = __dp4a(static_cast<int>(qw[i] & 0x0F0F0F0Fu), static_cast<int>(aw_lo[i]), lo);
+      hi = __dp4a(static_cast<int>((qw[i] >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[i]), hi);
+    }
+    acc_d = fmaf(static_cast<float>(sc[2 * pp] * lo), da[2 * p], acc_d);
+    acc_d = fmaf(static_cast<float>(sc[2 * pp + 1] * hi), da[2 * p + 1], acc_d);
+    acc_m = fmaf(static_cast<float>(mn[2 * pp]), sa[2 * p], acc_m);
+    acc_m = fmaf(static_cast<float>(mn[2 * pp + 1]), sa[2 * p + 1], acc_m);
+  }
+  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
+  return d * acc_d - dmin * acc_m;
 }
 
 // d*sum_j sc_j*d_a(j)*isum_j - dmin*sum_j m_j*s_a(j), fp32.

@@ -32,8 +32,11 @@ namespace si {
 
 enum SharedFmt { kNoShared = 0, kSharedQ4K = SI_Q4_K, kSharedQ80 = SI_Q8_0 };
 
+SI_TRACE_BUFFER
+
 constexpr int kGuThreads = 512;   // 32 row pairs x (2 matrices x 8 lanes)
-constexpr int kDownThreads = 256;
+constexpr int kDownThreads = 256;    // bf16 down
+constexpr int kDownQThreads = 512;   // quantised down
 
 struct GateUpParams {
   const __nv_bfloat16 *x;
@@ -109,7 +112,7 @@ SI_DEV float row_dot_q(const uint8_t *row, bool shared, int nsb, int lane8, cons
 // gate/up + SiLU gating + Q8_1 of h, quantised weights.
 // ---------------------------------------------------------------------------
 template <int SFMT>
-__global__ void __launch_bounds__(kGuThreads, 1) gateup_q_kernel(GateUpParams p) {
+__global__ void __launch_bounds__(kGuThreads, 2) gateup_q_kernel(GateUpParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int nsb = p.H / kQKK;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                 // 4 groups
@@ -122,6 +125,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_q_kernel(GateUpParams p)
   uint8_t *wbuf = reinterpret_cast<uint8_t *>(h_s + 32);               // [2][32][rb_max]
   wbuf = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(wbuf) + 127) & ~uintptr_t(127));
 
+  SI_TRACE_MARK(1, 0);
   const int unit = blockIdx.x;
   const bool shared = (SFMT != kNoShared) && unit >= p.units_routed;
   const int nhb_r = p.I / 32;
@@ -156,21 +160,25 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_q_kernel(GateUpParams p)
   // x -> Q8_1 tile (x comes from work before the predecessor kernel).
   if (p.x_q8) tile_from_q8_1(p.x_q8, p.H, act);
   else quantize_to_tile<__nv_bfloat16>(p.x, p.H, act);
+  SI_TRACE_MARK(1, 1);
 
   grid_dep_wait();
   grid_dep_launch();
+  SI_TRACE_MARK(1, 2);
 
   if (!shared && threadIdx.x == 0) {
     const int e = load_expert(p.ids, slot, p.E, p.status);
     const size_t row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(hb) * 32;
     issue(p.wg + row0 * rb, p.wu + row0 * rb);
   }
+  SI_TRACE_MARK(1, 3);
 
   const int pr = threadIdx.x >> 4, m = (threadIdx.x >> 3) & 1, lane8 = threadIdx.x & 7;
   const int grp = pr >> 3;
   float acc = 0.f;
   if (mbar_wait_bounded(&bars[grp], 0, p.status))
     acc = row_dot_q<SFMT>((m ? up_buf : gate_buf) + pr * rb, shared, nsb, lane8, act);
+  SI_TRACE_MARK(1, 4);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
@@ -183,23 +191,18 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_q_kernel(GateUpParams p)
     p.hf[slot_off + hb * 32 + pr] = h;
   }
   __syncthreads();
+  SI_TRACE_MARK(1, 5);
   if (threadIdx.x < 32) {
-    float v[8];
-    const int part = threadIdx.x & 3;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = h_s[8 * part + i];
-    uint32_t lo, hi;
     uint16_t d16, s16;
-    q8_1_encode_4lanes(v, lo, hi, d16, s16);
-    if (threadIdx.x < 4) {
-      *reinterpret_cast<uint2 *>(p.hq + slot_off + hb * 32 + 8 * part) = make_uint2(lo, hi);
-      if (part == 0) {
-        const int bidx = (slot_off + hb * 32) / 32;
-        p.hd[bidx] = half_bits_to_float(d16);
-        p.hs[bidx] = half_bits_to_float(s16);
-      }
+    const int q = q8_1_encode_warp(h_s[threadIdx.x], d16, s16);
+    p.hq[slot_off + hb * 32 + threadIdx.x] = static_cast<int8_t>(q);
+    if (threadIdx.x == 0) {
+      const int bidx = (slot_off + hb * 32) / 32;
+      p.hd[bidx] = half_bits_to_float(d16);
+      p.hs[bidx] = half_bits_to_float(s16);
     }
   }
+  SI_TRACE_MARK(1, 6);
 }
 
 // ---------------------------------------------------------------------------
@@ -223,57 +226,74 @@ SI_DEV float block_dot_bf16(const __nv_bfloat16 *a, const __nv_bfloat16 *b, int 
   return tot;
 }
 
+// Work items of one output row: Q4_K rows split into half super-blocks
+// (128 weights), Q8_0 rows into whole 256-weight units (a Q8_0 half would
+// start off a 16-byte boundary).
 template <int SFMT>
-__global__ void __launch_bounds__(kDownThreads) down_q_kernel(DownParams p) {
+SI_DEV int down_pieces(bool shared_slot, int width) {
+  return (SFMT == kSharedQ80 && shared_slot) ? width / kQKK : 2 * (width / kQKK);
+}
+
+template <int SFMT>
+__global__ void __launch_bounds__(kDownQThreads, 2) down_q_kernel(DownParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr bool kShared = SFMT != kNoShared;
   const int n_slots = p.k + (kShared ? 1 : 0);
   const int nsb_r = p.I / kQKK, nsb_s = kShared ? p.Is / kQKK : 0;
+  const int P_r = down_pieces<SFMT>(false, p.I);
+  const int P_s = kShared ? down_pieces<SFMT>(true, p.Is) : 0;
+  const int P_max = max(P_r, P_s);
   const int nq = p.k * p.I + (kShared ? p.Is : 0);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
   float *wts = reinterpret_cast<float *>(smem + 16);           // [8]
-  float *red = wts + 8;                                        // [8]
-  float *y = red + 8;                                          // [n_slots][J]
+  float *red = wts + 8;                                        // [16]
+  float *part = red + 16;                                      // [n_slots][J][P_max]
   ActTile act;
   act.qs = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(y + n_slots * p.J) + 15) & ~uintptr_t(15));
+      (reinterpret_cast<uintptr_t>(part + n_slots * p.J * P_max) + 15) & ~uintptr_t(15));
   act.d = reinterpret_cast<float *>(act.qs + (p.k * nsb_r + nsb_s) * kActSbStride);
   act.s = act.d + nq / 32;
   uint8_t *wbuf = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(act.s + nq / 32) + 127) & ~uintptr_t(127));
 
+  SI_TRACE_MARK(2, 0);
   const int j0 = blockIdx.x * p.J;
   const int nrows = min(p.J, p.H - j0);
   if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+    mbar_init(bar, n_slots);
     fence_mbar_init();
   }
   __syncthreads();
-  // Expert ids and weights come from the router (two kernels back): read
-  // before waiting, and request the weight rows at once.
-  if (threadIdx.x == 0) {
+  // Expert ids and weights come from the router (two kernels back): one
+  // thread per slot reads its id and requests that expert's rows at once.
+  if (threadIdx.x < n_slots) {
     const uint64_t pol = policy_evict_first();
-    const uint32_t br = static_cast<uint32_t>(nrows) * p.rbd_r;
-    const uint32_t bs = kShared ? static_cast<uint32_t>(nrows) * p.rbd_s : 0u;
-    mbar_arrive_expect_tx(bar, p.k * br + bs);
-    for (int r = 0; r < p.k; ++r) {
+    const int r = threadIdx.x;
+    if (r < p.k) {
       const int e = load_expert(p.ids, r, p.E, p.status);
       wts[r] = __ldcg(p.wts + r);
+      const uint32_t br = static_cast<uint32_t>(nrows) * p.rbd_r;
+      mbar_arrive_expect_tx(bar, br);
       bulk_g2s_evict_first(wbuf + static_cast<size_t>(r) * p.J * p.rbd_r,
                            p.wd + (static_cast<size_t>(e) * p.H + j0) * p.rbd_r, br, bar, pol);
-    }
-    if (kShared)
+    } else {
+      const uint32_t bs = static_cast<uint32_t>(nrows) * p.rbd_s;
+      mbar_arrive_expect_tx(bar, bs);
       bulk_g2s_evict_first(wbuf + static_cast<size_t>(p.k) * p.J * p.rbd_r,
                            p.wsd + static_cast<size_t>(j0) * p.rbd_s, bs, bar, pol);
+    }
   }
+  SI_TRACE_MARK(2, 1);
   float sigma = 0.f;
   if (kShared) {
     const float z = block_dot_bf16(p.w_sg, p.x, p.H, red);
     sigma = __fdiv_rn(1.f, 1.f + expf(-z));
   }
+  SI_TRACE_MARK(2, 2);
 
   grid_dep_wait();
   grid_dep_launch();
+  SI_TRACE_MARK(2, 3);
 
   // h codes of every slot -> tile (super-blocks at the padded stride).
   for (int c = threadIdx.x; c < nq / 16; c += blockDim.x) {
@@ -294,36 +314,66 @@ __global__ void __launch_bounds__(kDownThreads) down_q_kernel(DownParams p) {
     act.s[b] = __ldcg(p.hs + b);
   }
   __syncthreads();
+  SI_TRACE_MARK(2, 4);
   mbar_wait_bounded(bar, 0, p.status);
+  SI_TRACE_MARK(2, 5);
 
-  for (int task = threadIdx.x; task < n_slots * p.J; task += blockDim.x) {
-    const int r = task / p.J, jl = task % p.J;
+  const int items_r = p.k * p.J * P_r;
+  const int items = items_r + (kShared ? p.J * P_s : 0);
+  for (int u = threadIdx.x; u < items; u += blockDim.x) {
+    int r, jl, q;
+    if (u < items_r) {
+      r = u / (p.J * P_r);
+      const int rem = u % (p.J * P_r);
+      jl = rem / P_r;
+      q = rem % P_r;
+    } else {
+      r = p.k;
+      jl = (u - items_r) / P_s;
+      q = (u - items_r) % P_s;
+    }
     if (jl >= nrows) continue;
     const bool sh = kShared && r == p.k;
-    const int rbd = sh ? p.rbd_s : p.rbd_r;
-    const uint8_t *row = wbuf + static_cast<size_t>(r) * p.J * p.rbd_r + static_cast<size_t>(jl) * rbd;
-    const int nsb = sh ? nsb_s : nsb_r;
+    const uint8_t *row = wbuf + static_cast<size_t>(r) * p.J * p.rbd_r +
+                         static_cast<size_t>(jl) * (sh ? p.rbd_s : p.rbd_r);
     const int sb0 = r * nsb_r;           // shared slot: k * nsb_r
     const int blk0 = (r * p.I) / 32;     // shared slot: k * I / 32
-    float acc = 0.f;
-    for (int sb = 0; sb < nsb; ++sb) {
-      const uint4 *av = reinterpret_cast<const uint4 *>(act.qs + (sb0 + sb) * kActSbStride);
-      if (SFMT == kSharedQ80 && sh)
-        acc += q80_sb_dot(reinterpret_cast<const uint4 *>(row + sb * 272), av, act.d + blk0 + 8 * sb);
-      else
-        acc += q4k_sb_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes), av,
-                          act.d + blk0 + 8 * sb, act.s + blk0 + 8 * sb);
+    float v;
+    if (SFMT == kSharedQ80 && sh) {
+      v = q80_sb_dot(reinterpret_cast<const uint4 *>(row + q * 272),
+                     reinterpret_cast<const uint4 *>(act.qs + (sb0 + q) * kActSbStride),
+                     act.d + blk0 + 8 * q);
+    } else {
+      const int sb = q >> 1;
+      v = q4k_half_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes),
+                       reinterpret_cast<const uint4 *>(act.qs + (sb0 + sb) * kActSbStride),
+                       act.d + blk0 + 8 * sb, act.s + blk0 + 8 * sb, q & 1);
     }
-    y[r * p.J + jl] = acc;
+    part[(r * p.J + jl) * P_max + q] = v;
   }
+  __syncthreads();
+  SI_TRACE_MARK(2, 6);
+  // Combine in two short parallel phases: per (slot, row) the pieces in
+  // order, then per row the slots in rank order, then the shared slot.
+  float *ys = part;   // reuse: [n_slots][J] after the pieces are summed
+  float ysum = 0.f;
+  const int tr = threadIdx.x / p.J, tj = threadIdx.x % p.J;
+  const bool tlive = threadIdx.x < n_slots * p.J && tj < nrows;
+  if (tlive) {
+    const int P = (kShared && tr == p.k) ? P_s : P_r;
+    for (int q = 0; q < P; ++q) ysum += part[(tr * p.J + tj) * P_max + q];
+  }
+  __syncthreads();
+  if (tlive) ys[tr * p.J + tj] = ysum;
   __syncthreads();
   if (threadIdx.x < nrows) {
     const int jl = threadIdx.x;
     float acc = 0.f;
-    for (int r = 0; r < p.k; ++r) acc = fmaf(wts[r], y[r * p.J + jl], acc);
+    for (int r = 0; r < p.k; ++r) acc = fmaf(wts[r], ys[r * p.J + jl], acc);
     p.routed[j0 + jl] = __float2bfloat16_rn(acc);
-    if (kShared) p.shared[j0 + jl] = __float2bfloat16_rn(sigma * y[p.k * p.J + jl]);
+    if (kShared) p.shared[j0 + jl] = __float2bfloat16_rn(sigma * ys[p.k * p.J + jl]);
   }
+  SI_TRACE_MARK(2, 7);
 }
 
 // ---------------------------------------------------------------------------
@@ -555,7 +605,8 @@ static size_t down_q_smem(const si_moe_layer &L, int J, int rbd_r, int rbd_s) {
   const bool sh = L.shared_inter > 0;
   const int n_slots = L.top_k + (sh ? 1 : 0);
   const int nq = L.top_k * L.inter + (sh ? L.shared_inter : 0);
-  size_t off = 16 + 16 * sizeof(float) + n_slots * J * sizeof(float);
+  const int p_max = 2 * max(L.inter, sh ? L.shared_inter : 0) / 256;
+  size_t off = 16 + 24 * sizeof(float) + static_cast<size_t>(n_slots) * J * p_max * sizeof(float);
   off = round_up(off, 16) + (nq / 256) * kActSbStride + 2 * (nq / 32) * sizeof(float);
   off = round_up(off, 128);
   return off + static_cast<size_t>(J) * (L.top_k * rbd_r + (sh ? rbd_s : 0)) + 128;
@@ -570,7 +621,7 @@ static cudaError_t launch_q(const GateUpParams &gp, const DownParams &dp, size_t
   if (e != cudaSuccess) return e;
   e = launch_pdl(gateup_q_kernel<SFMT>, dim3(units), dim3(kGuThreads), gsm, s, gp);
   if (e != cudaSuccess) return e;
-  return launch_pdl(down_q_kernel<SFMT>, dim3(down_ctas), dim3(kDownThreads), dsm, s, dp);
+  return launch_pdl(down_q_kernel<SFMT>, dim3(down_ctas), dim3(kDownQThreads), dsm, s, dp);
 }
 
 cudaError_t preload_ffn() {
@@ -697,3 +748,13 @@ extern "C" si_status si_test_q4k_block_dots(const void *w, int rows, int k, cons
                    static_cast<const uint8_t *>(a_q8_1), out);
   return cuda_status(e);
 }
+
+#ifdef SI_TRACE
+extern "C" int si_trace_dump_ffn(void *dst) {
+  return cudaMemcpyFromSymbol(dst, si::g_si_trace, sizeof(si::g_si_trace)) == cudaSuccess ? 0 : 4;
+}
+extern "C" int si_trace_reset_ffn(void) {
+  static uint64_t zeros[si::kTraceKernels * si::kTraceBlocks * si::kTracePhases];
+  return cudaMemcpyToSymbol(si::g_si_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 4;
+}
+#endif

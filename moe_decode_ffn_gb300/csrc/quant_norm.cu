@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const T *__restrict_
 //   y = bf16((s * r) * w); optional Q8_1 of y.
 // With b == nullptr: s = bf16(a + c) (the 2-input norm of the unfused chain).
 // ---------------------------------------------------------------------------
+SI_TRACE_BUFFER
+
 constexpr int kNormThreads = 256;
 
 __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *p, float v[8]) {
@@ -62,8 +64,10 @@ __global__ void __launch_bounds__(kNormThreads)
   __shared__ float s_red[kNormThreads / 32];
   const int row = blockIdx.x;
   const size_t base = static_cast<size_t>(row) * n;
+  SI_TRACE_MARK(3, 0);
   grid_dep_wait();
   grid_dep_launch();
+  SI_TRACE_MARK(3, 1);
   float ss = 0.f;
   for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * kNormThreads) {
     float va[8], vb[8], vc[8], s[8];
@@ -92,6 +96,7 @@ __global__ void __launch_bounds__(kNormThreads)
 #pragma unroll
   for (int i = 0; i < kNormThreads / 32; ++i) tot += s_red[i];
   const float r = rsqrtf(__fdiv_rn(tot, static_cast<float>(n)) + eps);
+  SI_TRACE_MARK(3, 2);
   for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * kNormThreads) {
     float vw[8], y[8];
     load_bf16x8(w + i0, vw);
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(kNormThreads)
       if ((g & 3) == 0) *reinterpret_cast<uint32_t *>(blk) = d16 | (static_cast<uint32_t>(s16) << 16);
     }
   }
+  SI_TRACE_MARK(3, 3);
 }
 
 // t = bf16(a + b), the separate residual-add kernel of the unfused chain.
@@ -213,3 +219,13 @@ extern "C" si_status si_test_unfused_add_rmsnorm(const void *a, const void *b, c
   // 2-input norm of (t, c): b == nullptr in the kernel means s = bf16(t + c).
   return norm_launch(t_scratch, nullptr, c, w_norm, n, n_rows, eps, sum_out, norm_out, nullptr, s);
 }
+
+#ifdef SI_TRACE
+extern "C" int si_trace_dump_norm(void *dst) {
+  return cudaMemcpyFromSymbol(dst, si::g_si_trace, sizeof(si::g_si_trace)) == cudaSuccess ? 0 : 4;
+}
+extern "C" int si_trace_reset_norm(void) {
+  static uint64_t zeros[si::kTraceKernels * si::kTraceBlocks * si::kTracePhases];
+  return cudaMemcpyToSymbol(si::g_si_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 4;
+}
+#endif

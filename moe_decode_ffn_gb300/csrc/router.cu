@@ -9,12 +9,21 @@
 // expert index). The softmax over the selected logits is the workload's
 // statement.
 //
-// GB300 layout: one warp per expert row and split; its slice of W_r is loaded
-// into registers with 16-byte loads before the kernel waits on its
-// predecessor (the router weights do not depend on it), so the weight read
-// overlaps the previous kernel's tail. Partial sums go to a [T][S][E]
-// workspace and the last block reduces them in split order: no float
-// atomics, run-to-run deterministic.
+// GB300 layout. Each thread block owns R whole expert rows; the hidden
+// dimension of a row is split over W = 8/R warps of the block (the split-K
+// reduction stays in shared memory, in a fixed order: deterministic, no
+// float atomics). Each warp's slice of W_r goes into registers with 16-byte
+// loads before the kernel waits on its predecessor (router weights do not
+// depend on it), so the weight read overlaps the previous kernel's tail.
+// Logits are written with an epoch tag; one acquire-release atomic per block
+// counts completions; the last block checks every tag (a counter that was not
+// zero at the start shows up as stale tags) and selects.
+//
+// Selection: (value, index) pairs are packed into 64-bit keys whose unsigned
+// order is the selection order (value descending, -0 == +0, then lower index
+// first), so every compare-exchange is a branch-free max/min. Each warp sorts
+// 32 keys with a shuffle bitonic network; the first k of every warp are the
+// only candidates, and each candidate's rank among them is its final rank.
 #include <float.h>
 
 #include "common.cuh"
@@ -22,8 +31,10 @@
 
 namespace si {
 
+SI_TRACE_BUFFER
+
 constexpr int kRouterThreads = 256;
-constexpr int kRowsPerCta = kRouterThreads / 32;
+constexpr int kRouterWarps = kRouterThreads / 32;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxChunkTokens = 8;
 
@@ -31,19 +42,20 @@ struct RouterParams {
   const void *x;
   const void *w;
   int H, E, k, T;
-  int S;             // splits of the hidden dimension
+  int R;             // expert rows per block
+  int W;             // warps per row (R * W == 8)
   int tc;            // tokens per chunk
-  int cpc;           // CTAs per chunk = row_tiles * S
+  int cpc;           // blocks per chunk = ceil(E / R)
   int32_t *ids;
   float *wts;
   float *logits;     // nullable
-  float *partials;   // [T][S][E]
-  uint32_t *counters;
-  uint32_t *flags;   // [n_chunks][cpc]
+  uint2 *tagged;     // [T][E] {logit bits, epoch}
+  uint32_t *counters;  // [n_chunks]
+  uint32_t *epochs;    // [n_chunks]
   uint32_t *status;
 };
 
-template <typename T> struct Vec;   // 16 bytes of weights
+template <typename T> struct Vec;   // elements per 16 bytes of weights
 template <> struct Vec<__nv_bfloat16> { static constexpr int n = 8; };
 template <> struct Vec<float> { static constexpr int n = 4; };
 
@@ -79,237 +91,235 @@ SI_DEV void load_x(const XT *p, float *v) {
   }
 }
 
-// Total order used for selection: a before b iff a.v > b.v, or equal values
-// and a.i < b.i (so -0 and +0 tie and go by index).
-SI_DEV bool before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+// ---- selection keys ---------------------------------------------------------
+SI_DEV uint64_t make_key(float v, int e) {
+  uint32_t u = __float_as_uint(v + 0.0f);            // -0 -> +0
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);    // order-preserving map to unsigned
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
+}
+SI_DEV float key_value(uint64_t k) {
+  const uint32_t u = static_cast<uint32_t>(k >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+SI_DEV int key_index(uint64_t k) { return static_cast<int>(~static_cast<uint32_t>(k)); }
+
+SI_DEV uint64_t kmax(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("max.u64 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+SI_DEV uint64_t kmin(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("min.u64 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
-SI_DEV void cmpx(float *v, int *id, int i, int j) {  // position i gets the earlier element
-  if (before(v[j], id[j], v[i], id[i])) {
-    float tv = v[i]; v[i] = v[j]; v[j] = tv;
-    int ti = id[i]; id[i] = id[j]; id[j] = ti;
-  }
-}
-
-// Bitonic sorting network on 8 (value, index) pairs, into selection order.
-SI_DEV void sort8(float *v, int *id) {
+// Bitonic sort of the warp's 32 keys (one per lane) into selection order:
+// lane 0 ends with the earliest key. 15 shuffle steps.
+SI_DEV uint64_t warp_sort32(uint64_t key, int lane) {
 #pragma unroll
-  for (int size = 2; size <= 8; size <<= 1) {
+  for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          if ((i & size) == 0) cmpx(v, id, i, j);
-          else cmpx(v, id, j, i);
-        }
-      }
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, key, stride);
+      const bool lower = (lane & stride) == 0;
+      const bool desc = (lane & size) == 0 || size == 32;
+      key = (lower == desc) ? kmax(key, other) : kmin(key, other);
     }
   }
+  return key;
 }
 
-// Butterfly over the 32 lanes: at each of the 5 levels a lane takes its
-// partner's sorted 8, keeps the first 8 of the union (elementwise best of
-// mine[j] and partner[7-j] is a bitonic sequence holding them) and re-sorts
-// with 3 half-cleaner stages. The 16 shuffles of a level are independent.
-SI_DEV void warp_top8(float *v, int *id) {
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    float pv[8];
-    int pi[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      pv[j] = __shfl_xor_sync(0xffffffffu, v[j], m);
-      pi[j] = __shfl_xor_sync(0xffffffffu, id[j], m);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (before(pv[7 - j], pi[7 - j], v[j], id[j])) {
-        v[j] = pv[7 - j];
-        id[j] = pi[7 - j];
-      }
-    }
-#pragma unroll
-    for (int stride = 4; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = i ^ stride;
-        if (j > i) cmpx(v, id, i, j);
-      }
-    }
-  }
+SI_DEV uint32_t atom_inc_acq_rel(uint32_t *p, uint32_t bound) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound)
+               : "memory");
+  return old;
 }
 
 template <typename XT, typename WT, int NCH>
 __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParams p) {
   constexpr int VEC = Vec<WT>::n;
+  SI_TRACE_MARK(0, 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / p.S, split = blockIdx.x % p.S;
+  const int r = warp / p.W, wpart = warp % p.W;
+  const int e = blockIdx.x * p.R + r;
   const int chunk = blockIdx.y;
-  const int e = tile * kRowsPerCta + warp;
-  const int KS = p.H / p.S;
-  const int k0 = split * KS;
   const bool row_live = e < p.E;
 
-  // Weight slice of this warp's row into registers (independent of the
-  // predecessor kernel).
+  // This warp's part of its row: 16-byte vectors (i * W + wpart) * 32 + lane.
   uint4 wr[NCH];
   if (row_live) {
-    const WT *wrow = static_cast<const WT *>(p.w) + static_cast<size_t>(e) * p.H + k0;
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(static_cast<const WT *>(p.w) +
+                                                        static_cast<size_t>(e) * p.H);
 #pragma unroll
-    for (int c = 0; c < NCH; ++c)
-      wr[c] = __ldg(reinterpret_cast<const uint4 *>(wrow + (c * 32 + lane) * VEC));
+    for (int c = 0; c < NCH; ++c) wr[c] = __ldg(wrow + (c * p.W + wpart) * 32 + lane);
   }
   grid_dep_wait();
   grid_dep_launch();
+  SI_TRACE_MARK(0, 1);
 
   const int t0 = chunk * p.tc;
   const int t1 = min(p.T, t0 + p.tc);
-  if (row_live) {
-    for (int t = t0; t < t1; ++t) {
-      const XT *xs = static_cast<const XT *>(p.x) + static_cast<size_t>(t) * p.H + k0;
-      float acc = 0.f;
+  const int ntok = t1 - t0;
+  const uint32_t epoch = __ldcg(&p.epochs[chunk]) + 1u;
+  __shared__ float s_part[kMaxChunkTokens][kRouterWarps];
+  for (int t = t0; t < t1; ++t) {
+    float acc = 0.f;
+    if (row_live) {
+      const XT *xs = static_cast<const XT *>(p.x) + static_cast<size_t>(t) * p.H;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         float wv[VEC], xv[VEC];
         unpack_w<WT>(wr[c], wv);
-        load_x<XT, VEC>(xs + (c * 32 + lane) * VEC, xv);
+        load_x<XT, VEC>(xs + ((c * p.W + wpart) * 32 + lane) * VEC, xv);
 #pragma unroll
         for (int i = 0; i < VEC; ++i) acc = fmaf(wv[i], xv[i], acc);
       }
+    }
 #pragma unroll
-      for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-      if (lane == 0) p.partials[(static_cast<size_t>(t) * p.S + split) * p.E + e] = acc;
+    for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (lane == 0) s_part[t - t0][warp] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < p.R * ntok) {
+    const int rr = threadIdx.x % p.R, tt = threadIdx.x / p.R;
+    const int ex = blockIdx.x * p.R + rr;
+    if (ex < p.E) {
+      float l = s_part[tt][rr * p.W];
+      for (int w = 1; w < p.W; ++w) l += s_part[tt][rr * p.W + w];
+      const size_t o = static_cast<size_t>(t0 + tt) * p.E + ex;
+      p.tagged[o] = make_uint2(__float_as_uint(l), epoch);
+      if (p.logits) p.logits[o] = l;
     }
   }
+  SI_TRACE_MARK(0, 2);
 
-  // Completion handshake: publish partials, raise this block's flag, count.
+  // Completion count: release this block's logits, acquire everyone's.
   __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int me = blockIdx.x;
-    atomicExch(&p.flags[static_cast<size_t>(chunk) * p.cpc + me], 1u);
-    __threadfence();
-    const unsigned prev = atomicInc(&p.counters[chunk], static_cast<unsigned>(p.cpc - 1));
+    const unsigned prev = atom_inc_acq_rel(&p.counters[chunk], static_cast<unsigned>(p.cpc - 1));
     s_last = (prev == static_cast<unsigned>(p.cpc - 1)) ? 1 : (prev > static_cast<unsigned>(p.cpc - 1) ? 2 : 0);
   }
   __syncthreads();
-  if (s_last == 2) {
-    // The counter held a value it can never reach: the workspace was not
-    // zeroed. Report it and poison this chunk's outputs rather than leave
-    // stale ids in place.
-    if (threadIdx.x == 0) record_status(p.status, SI_ERR_HANDSHAKE);
-    for (int i = threadIdx.x; i < (min(p.T, chunk * p.tc + p.tc) - chunk * p.tc) * p.k; i += kRouterThreads) {
-      p.ids[static_cast<size_t>(chunk) * p.tc * p.k + i] = -1;
-      p.wts[static_cast<size_t>(chunk) * p.tc * p.k + i] = 0.f;
-    }
-    return;
-  }
-  if (!s_last) return;
-  __threadfence();
+  SI_TRACE_MARK(0, 3);
+  if (s_last == 0) return;
+  int bad = (s_last == 2);
 
-  // Last block of this chunk: every flag must be up, else the counter was
-  // not at zero when the run started (workspace not zeroed, or corrupted).
-  int missing = 0;
-  for (int i = threadIdx.x; i < p.cpc; i += kRouterThreads) {
-    uint32_t *f = &p.flags[static_cast<size_t>(chunk) * p.cpc + i];
-    if (__ldcg(f) != 1u) missing = 1;
-    *f = 0u;
+  // Last block of the chunk: every logit must carry this run's epoch.
+  __shared__ float s_logit[kMaxChunkTokens][256];
+  for (int i = threadIdx.x; i < ntok * p.E; i += kRouterThreads) {
+    const uint2 v = __ldcg(&p.tagged[static_cast<size_t>(t0) * p.E + i]);
+    if (v.y != epoch) bad = 1;
+    s_logit[i / p.E][i % p.E] = __uint_as_float(v.x);
   }
-  missing = __syncthreads_or(missing);
-  if (missing) {
+  bad = __syncthreads_or(bad);
+  SI_TRACE_MARK(0, 4);
+  if (threadIdx.x == 0) p.epochs[chunk] = epoch;
+  if (bad) {
+    // The counter was not at zero when the run started (workspace not zeroed
+    // or corrupted): report, and poison this chunk's outputs rather than
+    // leave stale ids in place.
     if (threadIdx.x == 0) record_status(p.status, SI_ERR_HANDSHAKE);
-    for (int i = threadIdx.x; i < (t1 - t0) * p.k; i += kRouterThreads) {
+    for (int i = threadIdx.x; i < ntok * p.k; i += kRouterThreads) {
       p.ids[static_cast<size_t>(t0) * p.k + i] = -1;
       p.wts[static_cast<size_t>(t0) * p.k + i] = 0.f;
     }
     return;
   }
 
-  // One warp per token: reduce partials in split order, select, softmax.
-  for (int t = t0 + warp; t < t1; t += kRowsPerCta) {
-    float v[8];
-    int id[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int ex = lane + 32 * c;
-      if (ex < p.E) {
-        const float *pp = p.partials + static_cast<size_t>(t) * p.S * p.E + ex;
-        float l = __ldcg(pp);
-        for (int s = 1; s < p.S; ++s) l += __ldcg(pp + static_cast<size_t>(s) * p.E);
-        if (p.logits) p.logits[static_cast<size_t>(t) * p.E + ex] = l;
-        v[c] = l;
-        id[c] = ex;
-      } else {
-        v[c] = -FLT_MAX;      // never selected: top_k <= n_experts
-        id[c] = 0x7fffffff;
-      }
+  // Per token: every warp sorts 32 of the logits; the first 8 of each warp
+  // are the only candidates; each candidate's rank among the <= 64
+  // candidates is its rank overall (a key in the overall first k is in the
+  // first k of its own warp).
+  __shared__ uint64_t s_cand[kRouterWarps * kMaxTopK];
+  __shared__ uint64_t s_sel[kMaxTopK];
+  for (int tt = 0; tt < ntok; ++tt) {
+    const int t = t0 + tt;
+    const int ex = threadIdx.x;
+    uint64_t key = ex < p.E ? make_key(s_logit[tt][ex], ex) : 0ull;   // 0: below every real key
+    key = warp_sort32(key, lane);
+    if (lane < kMaxTopK) s_cand[warp * kMaxTopK + lane] = key;
+    __syncthreads();
+    if (threadIdx.x < kRouterWarps * kMaxTopK) {
+      const uint64_t me = s_cand[threadIdx.x];
+      int rank = 0;
+#pragma unroll 8
+      for (int j = 0; j < kRouterWarps * kMaxTopK; ++j) rank += s_cand[j] > me;
+      if (rank < p.k && me != 0ull) s_sel[rank] = me;
     }
-    sort8(v, id);
-    warp_top8(v, id);
-    if (lane == 0) {
-      float ex[kMaxTopK];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const float v0 = key_value(s_sel[0]);
+      float exv[kMaxTopK];
       float sum = 0.f;
 #pragma unroll
-      for (int r = 0; r < kMaxTopK; ++r) {
-        if (r < p.k) {
-          ex[r] = expf(v[r] - v[0]);
-          sum += ex[r];
-        }
+      for (int q = 0; q < kMaxTopK; ++q) {
+        exv[q] = q < p.k ? expf(key_value(s_sel[q]) - v0) : 0.f;
+        sum += exv[q];
       }
+      const float inv = __frcp_rn(sum);
 #pragma unroll
-      for (int r = 0; r < kMaxTopK; ++r) {
-        if (r < p.k) {
-          p.ids[static_cast<size_t>(t) * p.k + r] = id[r];
-          p.wts[static_cast<size_t>(t) * p.k + r] = __fdiv_rn(ex[r], sum);
+      for (int q = 0; q < kMaxTopK; ++q) {
+        if (q < p.k) {
+          p.ids[static_cast<size_t>(t) * p.k + q] = key_index(s_sel[q]);
+          p.wts[static_cast<size_t>(t) * p.k + q] = exv[q] * inv;
         }
       }
     }
+    __syncthreads();
   }
+  SI_TRACE_MARK(0, 6);
+}
+
+// Rows per block R and warps per row W (R * W = 8): R large enough that the
+// chunk has at most ~160 blocks (one wave on a 152-SM GB300), W such that
+// every warp holds whole 16-byte vectors of the row.
+static void router_shape(int n_experts, int hidden, int vec, int &R, int &W, int &nch) {
+  int rmin = 1;
+  while ((n_experts + rmin - 1) / rmin > 160 && rmin < 8) rmin *= 2;
+  const int nv = hidden / vec;
+  W = 8 / rmin;
+  while (W > 1 && nv % (32 * W) != 0) W /= 2;
+  R = 8 / W;
+  nch = nv / (32 * W);
 }
 
 RouterGeom router_geom(int n_experts, int hidden, int n_tokens) {
   RouterGeom g{};
-  g.row_tiles = (n_experts + kRowsPerCta - 1) / kRowsPerCta;
-  // Aim at ~2 blocks per SM of a 152-SM GB300; each lane keeps 1..8 16-byte
-  // chunks of its row (bf16: hidden/S between 256 and 2048; fp32 halves it).
-  const int target = 2 * 152;
-  int S = 1;
-  while (S * 2 * g.row_tiles <= target) S *= 2;
-  const int s_min = (hidden + 1023) / 1024;   // fp32 weights: <= 8 chunks per lane
-  const int s_max = hidden / 256;             // bf16 weights: >= 1 chunk per lane
-  if (S < s_min) S = s_min;
-  if (S > s_max) S = s_max;
-  while (hidden % (S * 256) != 0 && S > 1) S /= 2;
-  g.splits = S;
-  g.ctas_per_chunk = g.row_tiles * S;
+  int R, W, nch;
+  router_shape(n_experts, hidden, 8, R, W, nch);
+  g.row_tiles = (n_experts + R - 1) / R;
+  g.splits = W;
+  g.ctas_per_chunk = g.row_tiles;
   g.tok_per_chunk = n_tokens < kMaxChunkTokens ? n_tokens : kMaxChunkTokens;
   if (g.tok_per_chunk < 1) g.tok_per_chunk = 1;
   g.n_chunks = (n_tokens + g.tok_per_chunk - 1) / g.tok_per_chunk;
   size_t off = sizeof(WsHeader);
   g.off_counters = off;
   off = round_up(off + sizeof(uint32_t) * g.n_chunks, 256);
-  g.off_flags = off;
-  off = round_up(off + sizeof(uint32_t) * static_cast<size_t>(g.n_chunks) * g.ctas_per_chunk, 256);
-  g.off_partials = off;
-  off = round_up(off + sizeof(float) * static_cast<size_t>(n_tokens) * S * n_experts, 256);
+  g.off_flags = off;   // epochs
+  off = round_up(off + sizeof(uint32_t) * g.n_chunks, 256);
+  g.off_partials = off;  // tagged logits
+  off = round_up(off + sizeof(uint2) * static_cast<size_t>(n_tokens) * n_experts, 256);
   g.bytes = off;
   return g;
 }
 
 template <typename XT, typename WT>
-static cudaError_t launch_router_t(const RouterParams &p, int n_chunks, cudaStream_t s) {
+static cudaError_t launch_router_t(RouterParams p, int n_chunks, cudaStream_t s) {
   constexpr int VEC = Vec<WT>::n;
-  const int nch = p.H / p.S / (32 * VEC);
+  int nch;
+  router_shape(p.E, p.H, VEC, p.R, p.W, nch);
+  p.cpc = (p.E + p.R - 1) / p.R;
   const dim3 grid(p.cpc, n_chunks), block(kRouterThreads);
   switch (nch) {
     case 1: return launch_pdl(router_topk_kernel<XT, WT, 1>, grid, block, 0, s, p);
     case 2: return launch_pdl(router_topk_kernel<XT, WT, 2>, grid, block, 0, s, p);
     case 4: return launch_pdl(router_topk_kernel<XT, WT, 4>, grid, block, 0, s, p);
     case 8: return launch_pdl(router_topk_kernel<XT, WT, 8>, grid, block, 0, s, p);
+    case 16: return launch_pdl(router_topk_kernel<XT, WT, 16>, grid, block, 0, s, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -321,6 +331,7 @@ static cudaError_t preload_router_t() {
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_topk_kernel<XT, WT, 2>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_topk_kernel<XT, WT, 4>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_topk_kernel<XT, WT, 8>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_topk_kernel<XT, WT, 16>);
   return e;
 }
 
@@ -339,14 +350,17 @@ si_status router_launch(const void *x, si_dtype x_type, const void *w, si_dtype 
   uint8_t *base = static_cast<uint8_t *>(ws);
   RouterParams p{};
   p.x = x; p.w = w; p.H = hidden; p.E = n_experts; p.k = top_k; p.T = n_tokens;
-  p.S = g.splits; p.tc = g.tok_per_chunk; p.cpc = g.ctas_per_chunk;
+  p.tc = g.tok_per_chunk;
   p.ids = ids; p.wts = wts; p.logits = logits;
-  p.partials = reinterpret_cast<float *>(base + g.off_partials);
+  p.tagged = reinterpret_cast<uint2 *>(base + g.off_partials);
   p.counters = reinterpret_cast<uint32_t *>(base + g.off_counters);
-  p.flags = reinterpret_cast<uint32_t *>(base + g.off_flags);
+  p.epochs = reinterpret_cast<uint32_t *>(base + g.off_flags);
   p.status = status;
-  const int nch_bytes = hidden / g.splits * (w_type == SI_F32 ? 4 : 2) / 16 / 32;
-  if (nch_bytes < 1 || nch_bytes > 8 || (nch_bytes & (nch_bytes - 1))) return SI_ERR_UNSUPPORTED;
+  {
+    int R, W, nch;
+    router_shape(n_experts, hidden, w_type == SI_F32 ? 4 : 8, R, W, nch);
+    if (nch < 1 || nch > 16 || (nch & (nch - 1))) return SI_ERR_UNSUPPORTED;
+  }
   cudaError_t e;
   if (x_type == SI_BF16 && w_type == SI_BF16) e = launch_router_t<__nv_bfloat16, __nv_bfloat16>(p, g.n_chunks, s);
   else if (x_type == SI_F32 && w_type == SI_F32) e = launch_router_t<float, float>(p, g.n_chunks, s);
@@ -388,3 +402,13 @@ extern "C" si_status si_moe_router_topk(const void *x, si_dtype x_type, const vo
                        topk_w, logits_out, workspace, static_cast<uint32_t *>(workspace),
                        static_cast<cudaStream_t>(stream));
 }
+
+#ifdef SI_TRACE
+extern "C" int si_trace_dump_router(void *dst) {
+  return cudaMemcpyFromSymbol(dst, si::g_si_trace, sizeof(si::g_si_trace)) == cudaSuccess ? 0 : 4;
+}
+extern "C" int si_trace_reset_router(void) {
+  static uint64_t zeros[si::kTraceKernels * si::kTraceBlocks * si::kTracePhases];
+  return cudaMemcpyToSymbol(si::g_si_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 4;
+}
+#endif

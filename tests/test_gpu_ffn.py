@@ -118,3 +118,13 @@ def test_ffn_out_of_range_expert_is_reported_not_faulted():
     ws = m.workspace(m.ffn_workspace_bytes(dev))
     m.si_moe_ffn_decode(dev, x, ids.cuda(), w.cuda(), ws=ws)
     assert m.si_workspace_status(ws) == m.SI_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q8_0", "bf16"])
+def test_generator_bytes_identical_on_cpu_and_gpu(fmt):
+    """Device-generated weights are the bytes the oracle regenerates on the CPU."""
+    for role, e in ((gen.ROLE_GATE, 0), (gen.ROLE_DOWN, 77), (gen.ROLE_SH_UP, 0)):
+        cpu = gen._weights(5, 1, role, [e, e + 1], 512, 2048, fmt, "cpu")
+        dev = gen._weights(5, 1, role, [e, e + 1], 512, 2048, fmt, "cuda")
+        assert torch.equal(cpu, dev.cpu()), (fmt, role)
+    assert torch.equal(gen.make_tokens(9, 4), gen.make_tokens(9, 4, device="cuda").cpu())

@@ -19,6 +19,14 @@ pytestmark = pytest.mark.gpu
 CHAIN_TIE_REL = 1e-3
 
 
+def chain_tolerance(depth):
+    """Each layer can move an element of the residual stream across one more
+    bf16 rounding boundary than the oracle does, so after `depth` layers the
+    per-element bound is (depth + 1) ulps and the relative L2 bound grows in
+    proportion."""
+    return dict(ulps=P.ULPS * (depth + 1) / 2 + 1, rel_l2=P.REL_L2 * depth)
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     m.build()
@@ -84,9 +92,9 @@ def test_stack_graph_against_oracle_chain():
             ref = oracle_layer(spec, 200, l, xin, res, ids[t, l].tolist(), tie)
             xin = torch.from_numpy(ref["y"]).to(torch.bfloat16)
             res = torch.from_numpy(ref["sum"]).to(torch.bfloat16)
-        ok, rep = P.float_parity(bf16_np(g.y[t]), ref["y"])
+        ok, rep = P.float_parity(bf16_np(g.y[t]), ref["y"], **chain_tolerance(3))
         assert ok, "y " + rep
-        ok, rep = P.float_parity(bf16_np(g.sum[t]), ref["sum"])
+        ok, rep = P.float_parity(bf16_np(g.sum[t]), ref["sum"], **chain_tolerance(3))
         assert ok, "sum " + rep
     g.close()
 

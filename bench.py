@@ -1,0 +1,379 @@
+"""Benchmark: decode-time MoE FFN stage on GB300.
+
+Workload (the one the metric is quoted on): a 40-layer FFN-only decode stack
+of Qwen3.6-35B-A3B-shaped layers (hidden 2048, 256 experts, top-8, expert
+width 512, Q4_K routed gate/up/down, Q4_K shared expert of width 512 with a
+sigmoid gate, bf16 router, residual folded into RMSNorm), 128 sequential
+tokens, captured as one CUDA graph. One step = one replay of that graph =
+128 x 40 layer-tokens. Weights are seeded synthetic data of those shapes
+(18.2 GB resident; every token reads 679 MB of weights, far above the
+129 MB L2, so no L2 flush is needed between steps).
+
+Metric: microseconds per layer per token (lower is better), with the
+weight-read bandwidth it implies against the measured HBM peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (the plain fp64 restatement of the
+method) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU baseline times the oracle single-threaded: pin numpy's BLAS before
+# anything imports numpy.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse  # noqa: E402
+import hashlib
+import json  # noqa: E402
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE FFN decode µs/layer/token; expert weight-read HBM GB/s vs GB300 peak"
+UNIT = "us/layer/token"
+N_LAYERS, N_TOKENS, SEED = 40, 128, 4040
+WORKLOAD = ("40-layer FFN-only decode stack, Qwen3.6-35B-A3B-shaped layers (H=2048, E=256, "
+            "top-8, I=512, Q4_K routed + Q4_K shared I=512, bf16 router), 128 sequential "
+            "tokens, one CUDA graph")
+
+# Algorithmic bytes per layer-token (weights only; activations are < 20 KB):
+# router 256x2048 bf16, 8 routed experts x 3 Q4_K matrices of 512x2048,
+# shared expert 3 Q4_K matrices, sigmoid-gate vector.
+Q4K_MATRIX = 512 * 2048 // 256 * 144                    # 589,824
+BYTES_ROUTER = 256 * 2048 * 2                           # 1,048,576
+BYTES_ROUTED = 8 * 3 * Q4K_MATRIX                       # 14,155,776
+BYTES_SHARED = 3 * Q4K_MATRIX                           # 1,769,472
+BYTES_SIGMOID = 2048 * 2
+BYTES_LAYER_TOKEN = BYTES_ROUTER + BYTES_ROUTED + BYTES_SHARED + BYTES_SIGMOID   # 16,977,920
+# Gate/up kernel (the dominant one): 8 experts' gate+up rows + shared gate+up.
+BYTES_GATEUP = 8 * 2 * Q4K_MATRIX + 2 * Q4K_MATRIX      # 10,616,832
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"si_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _traffic_record(kernel_sources):
+    """Per-launch DRAM traffic of the gate/up kernel from the committed ncu
+    summary, valid only while the kernel sources match the captured ones."""
+    path = os.path.join(ROOT, "profiles", "gateup_q4k_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for src in kernel_sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def oracle_jobs(n_layer_tokens: int, device="cpu"):
+    """Inputs of a bounded sample of the workload for the CPU oracle: layer-tokens
+    (layer l, token t) of the same stack, with the router weights and the
+    selected experts' weights materialised (generated on `device`, then kept
+    on the host)."""
+    import torch
+
+    import gen
+    from oracle import moe as M
+    spec = gen.Q4K_LAYER_SHARED_Q4_K
+    x = gen.make_tokens(SEED, 2)
+    jobs = []
+    for i in range(n_layer_tokens):
+        layer = i % N_LAYERS
+        xt = x[i % 2]
+        w_router = gen.to_bf16(gen.normal([gen.stream_key(SEED, layer, gen.ROLE_ROUTER, 0)],
+                                          spec.n_experts * spec.hidden, 0.0, gen.WEIGHT_STD,
+                                          device)).reshape(spec.n_experts, spec.hidden).cpu()
+        ids = M.topk_sort(M.router_logits(M.as_f64(xt), w_router))
+        L = gen.make_layer(spec, SEED, layer, device=device, experts=ids)
+        L = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in L.items()}
+        jobs.append((L, xt))
+    return jobs
+
+
+def time_oracle(jobs):
+    """Seconds per layer-token of the oracle's whole layer (router, top-8,
+    softmax, 9 experts in integer mode, residual norm) over `jobs`."""
+    from oracle import moe as M
+    t0 = time.perf_counter()
+    for L, xt in jobs:
+        M.layer_forward(L, xt)
+    return (time.perf_counter() - t0) / len(jobs)
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    per_lt = []
+    n_each = 6
+    jobs = oracle_jobs(n_each)
+    for _ in range(max(1, args.warmup)):
+        time_oracle(jobs[:1])
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        per_lt.append(time_oracle(jobs) * 1e6)
+    ms_step = (time.perf_counter() - t_all) / args.steps * 1e3
+    v = statistics.median(per_lt)
+    sample = (f"{n_each} layer-tokens per step (layer l, token t of the 40-layer stack), oracle "
+              f"layer_forward in fp64, weights of the selected experts materialised beforehand")
+    line = {"metric": METRIC, "value": round(v, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 2),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "layers": N_LAYERS, "tokens": N_TOKENS},
+            "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+
+    import gen
+    import moe_decode_ffn_gb300 as m
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    m.build()
+    lib = m.library()
+    spec = gen.Q4K_LAYER_SHARED_Q4_K
+    layers = [m.device_layer(spec, SEED, l, device=dev) for l in range(N_LAYERS)]
+    x_in = gen.make_tokens(SEED + rank, N_TOKENS, device=dev)
+    graph = m.StackGraph(layers, x_in)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+
+    # --- device-resident throughput ----------------------------------------
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.launch(stream)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.launch(stream)
+            e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1)
+    status = m.si_workspace_status(graph.ws, stream)
+    ids_ok = bool((graph.ids >= 0).all().item() and (graph.ids < 256).all().item())
+    if pg is not None:
+        t = torch.tensor([ms], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    # whole job: world x 40 x 128 layer-tokens per step
+    value_job = ms_step * 1e3 / (N_LAYERS * N_TOKENS) / world
+    peak, peak_kind = _peaks()
+    gbs_stage = BYTES_LAYER_TOKEN / (ms_step * 1e3 / (N_LAYERS * N_TOKENS)) / 1e3
+
+    # --- end to end through the C ABI with host buffers ------------------------
+    h_in = x_in.cpu().pin_memory()
+    h_out = torch.empty_like(graph.y, device="cpu").pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            graph.x_in.copy_(h_in, non_blocking=True)
+            graph.launch(stream)
+            h_out.copy_(graph.y, non_blocking=True)
+    barrier()
+    t_e2e = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.x_in.copy_(h_in, non_blocking=True)
+            graph.launch(stream)
+            h_out.copy_(graph.y, non_blocking=True)
+    barrier()
+    e2e_ms = (time.perf_counter() - t_e2e) * 1e3 / args.steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = e2e_ms * 1e3 / (N_LAYERS * N_TOKENS) / world
+
+    # --- dominant kernel: gate/up alone, chained, with the timed run's routing --
+    ids_all = graph.ids.clone()   # [T][L][k]
+    ffn_ws = [m.workspace(m.ffn_workspace_bytes(L), dev) for L in layers]
+    gu = torch.cuda.CUDAGraph()
+    n_gu = N_LAYERS * N_TOKENS
+    with torch.cuda.stream(stream):
+        for t in range(2):
+            for l, L in enumerate(layers):
+                lib.si_moe_ffn_gateup(L.ref, 1, graph.y[t].data_ptr(), None,
+                                      ids_all[t, l].data_ptr(), ffn_ws[l].data_ptr(),
+                                      ffn_ws[l].numel(), stream.cuda_stream)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(gu, stream=stream):
+        for t in range(N_TOKENS):
+            for l, L in enumerate(layers):
+                st = lib.si_moe_ffn_gateup(L.ref, 1, graph.y[t].data_ptr(), None,
+                                           ids_all[t, l].data_ptr(), ffn_ws[l].data_ptr(),
+                                           ffn_ws[l].numel(), stream.cuda_stream)
+                assert st == 0
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            gu.replay()
+        e0.record(stream)
+        for _ in range(3):
+            gu.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    gu_us = e0.elapsed_time(e1) * 1e3 / (3 * n_gu)
+    gu_gbs = BYTES_GATEUP / (gu_us * 1e-6) / 1e9
+    traffic = _traffic_record(["moe_decode_ffn_gb300/csrc/ffn.cu",
+                               "moe_decode_ffn_gb300/csrc/common.cuh"])
+
+    if rank != 0:
+        return 0
+    cpu_us, cpu_n = (None, 0)
+    if world == 1 and not args.no_cpu_baseline:
+        jobs = oracle_jobs(args.cpu_layer_tokens, device=dev)
+        cpu_us, cpu_n = time_oracle(jobs) * 1e6, len(jobs)
+    launches = args.steps * N_LAYERS * N_TOKENS * 4
+    line = {
+        "metric": METRIC, "value": round(value_job, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": N_LAYERS, "tokens": N_TOKENS,
+                   "hidden": 2048, "experts": 256, "top_k": 8, "inter": 512, "shared_inter": 512,
+                   "expert_type": "q4_k", "shared_type": "q4_k", "router_type": "bf16",
+                   "parallelism": f"replicas{world}",
+                   "l2": "no flush: weights 18.2 GB resident, 679 MB read per token > 129 MB L2"},
+        "weight_read": {"bytes_per_layer_token": BYTES_LAYER_TOKEN,
+                        "gbs": round(gbs_stage, 1), "frac_of_peak": round(gbs_stage / peak, 4),
+                        "peak_gbs": peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": "gateup_q_kernel (routed + shared gate/up GEMV, SiLU, Q8_1 of h)",
+                     "bound": "hbm", "achieved": round(gu_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(gu_gbs / peak, 4),
+                     "traffic": traffic, "bytes_per_launch": BYTES_GATEUP,
+                     "avg_launch_us": round(gu_us, 3), "peak_kind": peak_kind},
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
+                "d2h_bytes_per_step": h_out.numel() * h_out.element_size()},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "device_status": m.status_string(status), "ids_valid": ids_ok,
+    }
+    if cpu_us is not None:
+        line["cpu_baseline"] = {"value": round(cpu_us, 1), "unit": UNIT, "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{cpu_n} layer-tokens of the same stack, fp64 oracle, "
+                                          "single thread"}
+    print(json.dumps(line), flush=True)
+    graph.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-layer-tokens", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -234,6 +234,12 @@ si_status si_workspace_status(const void *workspace, void *stream, int *status_o
 si_status si_test_q4k_block_dots(const void *w, int rows, int k, const void *a_q8_1,
                                  int32_t *out, void *stream);
 
+/* Only the gate/up kernel of si_moe_ffn_decode (same arguments; h is left in
+ * the workspace). For timing that kernel in isolation. */
+si_status si_moe_ffn_gateup(const si_moe_layer *L, int n_tokens, const void *x,
+                            const void *x_q8_1, const int32_t *topk_ids, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
 /* The unfused chain the fold replaced: t = bf16(a + b) by one kernel, then the
  * 2-input norm of (t, c) by a second. Same outputs as si_add_rmsnorm3. */
 si_status si_test_unfused_add_rmsnorm(const void *a, const void *b, const void *c,

@@ -614,13 +614,13 @@ static size_t down_q_smem(const si_moe_layer &L, int J, int rbd_r, int rbd_s) {
 
 template <int SFMT>
 static cudaError_t launch_q(const GateUpParams &gp, const DownParams &dp, size_t gsm, size_t dsm,
-                            int down_ctas, int units, cudaStream_t s) {
+                            int down_ctas, int units, cudaStream_t s, bool gateup_only) {
   cudaError_t e = allow_smem(gateup_q_kernel<SFMT>, gsm);
   if (e != cudaSuccess) return e;
   e = allow_smem(down_q_kernel<SFMT>, dsm);
   if (e != cudaSuccess) return e;
   e = launch_pdl(gateup_q_kernel<SFMT>, dim3(units), dim3(kGuThreads), gsm, s, gp);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || gateup_only) return e;
   return launch_pdl(down_q_kernel<SFMT>, dim3(down_ctas), dim3(kDownQThreads), dsm, s, dp);
 }
 
@@ -645,7 +645,7 @@ cudaError_t preload_ffn() {
 
 si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, const int32_t *ids,
                      const float *wts, void *routed, void *shared, void *ws, uint32_t *status,
-                     cudaStream_t s) {
+                     cudaStream_t s, bool gateup_only) {
   const FfnGeom g = ffn_geom(L);
   const bool sh = L.shared_inter > 0;
   uint8_t *base = static_cast<uint8_t *>(ws);
@@ -690,9 +690,10 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
     const int rb_max = sh ? max(gp.rb_r, gp.rb_s) : gp.rb_r;
     const size_t gsm = gateup_q_smem(L, rb_max);
     const size_t dsm = down_q_smem(L, dp.J, dp.rbd_r, dp.rbd_s);
-    if (!sh) e = launch_q<kNoShared>(gp, dp, gsm, dsm, down_ctas, g.n_units, s);
-    else if (L.shared_type == SI_Q4_K) e = launch_q<kSharedQ4K>(gp, dp, gsm, dsm, down_ctas, g.n_units, s);
-    else e = launch_q<kSharedQ80>(gp, dp, gsm, dsm, down_ctas, g.n_units, s);
+    if (!sh) e = launch_q<kNoShared>(gp, dp, gsm, dsm, down_ctas, g.n_units, s, gateup_only);
+    else if (L.shared_type == SI_Q4_K)
+      e = launch_q<kSharedQ4K>(gp, dp, gsm, dsm, down_ctas, g.n_units, s, gateup_only);
+    else e = launch_q<kSharedQ80>(gp, dp, gsm, dsm, down_ctas, g.n_units, s, gateup_only);
   } else {
     const size_t gsm = static_cast<size_t>(L.hidden) * sizeof(float);
     const int nq = L.top_k * L.inter + gp.Is;
@@ -701,7 +702,7 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
     if (e == cudaSuccess) e = allow_smem(down_bf16_kernel, dsm);
     if (e == cudaSuccess)
       e = launch_pdl(gateup_bf16_kernel, dim3(g.n_units), dim3(kGuThreads), gsm, s, gp);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !gateup_only)
       e = launch_pdl(down_bf16_kernel, dim3(down_ctas), dim3(kDownThreads), dsm, s, dp);
   }
   return cuda_status(e);
@@ -733,7 +734,23 @@ extern "C" si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, cons
   if (!workspace || !aligned256(workspace) || workspace_bytes < ffn_geom(*L).bytes)
     return SI_ERR_WORKSPACE;
   return ffn_launch(*L, x, x_q8_1, topk_ids, topk_w, routed_out, shared_out, workspace,
-                    static_cast<uint32_t *>(workspace), static_cast<cudaStream_t>(stream));
+                    static_cast<uint32_t *>(workspace), static_cast<cudaStream_t>(stream), false);
+}
+
+extern "C" si_status si_moe_ffn_gateup(const si_moe_layer *L, int n_tokens, const void *x,
+                                       const void *x_q8_1, const int32_t *topk_ids,
+                                       void *workspace, size_t workspace_bytes, void *stream) {
+  if (!L || !x || !topk_ids) return SI_ERR_INVALID_ARG;
+  if (n_tokens != 1) return SI_ERR_UNSUPPORTED;
+  const si_status st = ffn_check(*L);
+  if (st != SI_OK) return st;
+  if (!aligned16(x) || (x_q8_1 && (reinterpret_cast<uintptr_t>(x_q8_1) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(topk_ids) & 3u))
+    return SI_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < ffn_geom(*L).bytes)
+    return SI_ERR_WORKSPACE;
+  return ffn_launch(*L, x, x_q8_1, topk_ids, nullptr, nullptr, nullptr, workspace,
+                    static_cast<uint32_t *>(workspace), static_cast<cudaStream_t>(stream), true);
 }
 
 extern "C" si_status si_test_q4k_block_dots(const void *w, int rows, int k, const void *a_q8_1,

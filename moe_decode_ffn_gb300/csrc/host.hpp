@@ -81,7 +81,7 @@ FfnGeom ffn_geom(const si_moe_layer &L);
 si_status ffn_check(const si_moe_layer &L);
 si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, const int32_t *ids,
                      const float *wts, void *routed, void *shared, void *ws, uint32_t *status,
-                     cudaStream_t s);
+                     cudaStream_t s, bool gateup_only = false);
 
 // ---- residual norm
 si_status norm_launch(const void *a, const void *b, const void *c, const void *w, int n, int rows,

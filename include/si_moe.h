@@ -240,6 +240,11 @@ si_status si_moe_ffn_gateup(const si_moe_layer *L, int n_tokens, const void *x,
                             const void *x_q8_1, const int32_t *topk_ids, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* A kernel whose mbarrier wait can never complete: it gives up after
+ * budget_ns (<= 2 s) and writes SI_ERR_TIMEOUT to the workspace status word,
+ * as every bounded wait of the library does. For testing that path. */
+si_status si_test_wait_timeout(uint64_t budget_ns, void *workspace, void *stream);
+
 /* The unfused chain the fold replaced: t = bf16(a + b) by one kernel, then the
  * 2-input norm of (t, c) by a second. Same outputs as si_add_rmsnorm3. */
 si_status si_test_unfused_add_rmsnorm(const void *a, const void *b, const void *c,

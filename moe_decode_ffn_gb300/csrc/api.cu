@@ -112,9 +112,31 @@ static si_status layer_enqueue(const si_moe_layer &L, const void *x, const void 
                      nullptr, s);
 }
 
+// Test kernel for the bounded wait: one block waits on an mbarrier whose
+// expected bytes never arrive (no copy is issued), gives up after budget_ns
+// and records SI_ERR_TIMEOUT.
+__global__ void wait_timeout_kernel(uint64_t budget_ns, uint32_t *status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar, 16);
+  __syncthreads();
+  mbar_wait_bounded(&bar, 0, threadIdx.x == 0 ? status : nullptr, budget_ns);
+}
+
 }  // namespace si
 
 using namespace si;
+
+extern "C" si_status si_test_wait_timeout(uint64_t budget_ns, void *workspace, void *stream) {
+  if (!workspace || !aligned256(workspace) || budget_ns > 2000000000ull) return SI_ERR_INVALID_ARG;
+  return cuda_status(launch_pdl(wait_timeout_kernel, dim3(1), dim3(32), 0,
+                                static_cast<cudaStream_t>(stream), budget_ns,
+                                static_cast<uint32_t *>(workspace)));
+}
 
 struct si_graph {
   cudaGraph_t graph;

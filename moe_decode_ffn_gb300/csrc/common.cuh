@@ -18,10 +18,9 @@ constexpr int kQ4KBytes = 144;
 constexpr int kQ80Bytes = 34;
 constexpr int kQ81Bytes = 36;
 
-// Bounded waits: polls of an mbarrier before a kernel gives up and records
-// SI_ERR_TIMEOUT. Each try_wait blocks for a short hardware-defined interval,
-// so this bound is well above a second of waiting.
-constexpr uint32_t kSpinLimit = 1u << 24;
+// Bounded waits: a kernel that has waited this long on an mbarrier (its
+// bulk copies never landed) gives up and records SI_ERR_TIMEOUT.
+constexpr uint64_t kWaitBudgetNs = 1000000000ull;   // 1 s
 
 // Device status word: first 4 bytes of every workspace.
 struct WsHeader {
@@ -98,11 +97,24 @@ SI_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` with an iteration bound. Returns false on
+SI_DEV uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar` for at most `budget_ns`. Returns false on
 // timeout (after recording SI_ERR_TIMEOUT).
-SI_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t *status) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+SI_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t *status,
+                              uint64_t budget_ns = kWaitBudgetNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (now_ns() - t0 > budget_ns) break;
+  }
   record_status(status, SI_ERR_TIMEOUT);
   return false;
 }

@@ -121,6 +121,32 @@ si_status si_moe_router_topk(const void *x, si_dtype x_type, const void *w_route
                              float *logits_out, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/*
+ * si_moe_router_topk_noalloc - si_moe_router_topk without a caller workspace.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory when they route a token - for example a
+ * serving loop that forbids cudaMalloc/cudaFree after start-up (both can
+ * synchronise the whole device and stall other streams), or a plug-in running
+ * inside a host whose allocator owns all device memory. Same arguments and
+ * results as si_moe_router_topk, minus the workspace. It allocates nothing:
+ * its scratch is a fixed array compiled into the library (about 132 KB on
+ * every GPU that loads it, held until the process exits).
+ *   - Limit: n_tokens * n_experts <= 16384 (e.g. 64 tokens of 256 experts);
+ *     larger calls return SI_ERR_UNSUPPORTED and enqueue nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array: calls that may overlap on the GPU (two
+ *     streams, two threads) race and must be serialised by the caller. Each
+ *     call clears the status word and completion counters before its kernel
+ *     (an asynchronous memset on `stream`).
+ */
+si_status si_moe_router_topk_noalloc(const void *x, si_dtype x_type, const void *w_router,
+                                     si_dtype w_type, int hidden, int n_experts, int top_k,
+                                     int n_tokens, int32_t *topk_ids, float *topk_w,
+                                     float *logits_out, void *stream);
+
 /* One MoE FFN layer: shapes, formats and device weight pointers. */
 typedef struct si_moe_layer {
   int hidden;                 /* H, multiple of 256 (2048 in the studied models) */

@@ -52,6 +52,8 @@ SIGNATURES = {
     "si_moe_router_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "si_moe_router_topk": (_i32, [_vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                   _vp, _sz, _vp]),
+    "si_moe_router_topk_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                          _vp, _vp]),
     "si_moe_ffn_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
     "si_moe_ffn_decode": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _vp, _sz, _vp]),
@@ -164,6 +166,24 @@ def si_moe_router_topk(x: torch.Tensor, w_router: torch.Tensor, top_k: int = 8,
         _cuda(x, "x"), _xtype(x), _cuda(w_router, "w_router"), _xtype(w_router), H, E, top_k, T,
         _cuda(ids, "ids"), _cuda(wts, "w"), _opt(logits, "logits"), _cuda(ws, "ws"), ws.numel(),
         _stream(stream)), "si_moe_router_topk")
+    return ids, wts, logits
+
+
+def si_moe_router_topk_noalloc(x: torch.Tensor, w_router: torch.Tensor, top_k: int = 8,
+                               want_logits: bool = False, stream=None):
+    """Router + top-k through the entry point that allocates nothing on the
+    device side (its scratch is built into the library). The output tensors
+    here are the caller's; the call itself needs no workspace."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    ids = torch.empty(T, top_k, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, top_k, dtype=torch.float32, device=dev)
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None
+    _check(library().si_moe_router_topk_noalloc(
+        _cuda(x, "x"), _xtype(x), _cuda(w_router, "w_router"), _xtype(w_router), H, E, top_k, T,
+        _cuda(ids, "ids"), _cuda(wts, "w"), _opt(logits, "logits"), _stream(stream)),
+        "si_moe_router_topk_noalloc")
     return ids, wts, logits
 
 

@@ -26,6 +26,8 @@
 // only candidates, and each candidate's rank among them is its final rank.
 #include <float.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "host.hpp"
 
@@ -412,3 +414,64 @@ extern "C" int si_trace_reset_router(void) {
   return cudaMemcpyToSymbol(si::g_si_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 4;
 }
 #endif
+
+// ---------------------------------------------------------------------------
+// Router with library-owned scratch, for callers that cannot allocate device
+// memory. The scratch (status word, completion counters, epochs and the
+// tagged logits) lives in this file-scope device array instead of a caller
+// workspace; every GPU that loads the library holds it until the process
+// exits. It is sized for n_tokens * n_experts <= kNoAllocMaxEntries.
+// ---------------------------------------------------------------------------
+namespace si {
+constexpr int kNoAllocMaxEntries = 64 * 256;
+constexpr size_t kNoAllocScratchBytes = 3 * 256 + sizeof(uint2) * kNoAllocMaxEntries;
+static __device__ __align__(256) uint8_t g_router_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array for the current device. The first call
+// on a device looks it up (cudaGetSymbolAddress, with that device current)
+// and caches it; later calls only read the cache.
+static si_status noalloc_scratch(void **out) {
+  static std::mutex mu;
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SI_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_router_noalloc_scratch) != cudaSuccess || !p) return SI_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return SI_OK;
+}
+}  // namespace si
+
+extern "C" si_status si_moe_router_topk_noalloc(const void *x, si_dtype x_type, const void *w_router,
+                                                si_dtype w_type, int hidden, int n_experts,
+                                                int top_k, int n_tokens, int32_t *topk_ids,
+                                                float *topk_w, float *logits_out, void *stream) {
+  if (!x || !w_router || !topk_ids || !topk_w) return SI_ERR_INVALID_ARG;
+  if (hidden < 256 || hidden % 256 != 0 || hidden > 16384) return SI_ERR_INVALID_ARG;
+  if (n_experts < 8 || n_experts > 256 || top_k < 1 || top_k > kMaxTopK || top_k > n_experts ||
+      n_tokens < 1)
+    return SI_ERR_INVALID_ARG;
+  if ((x_type != SI_BF16 && x_type != SI_F32) || (w_type != SI_BF16 && w_type != SI_F32))
+    return SI_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w_router) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_w) & 3u) ||
+      (logits_out && (reinterpret_cast<uintptr_t>(logits_out) & 3u)))
+    return SI_ERR_INVALID_ARG;
+  // Larger problems than the fixed scratch holds are refused.
+  if (static_cast<int64_t>(n_tokens) * n_experts > kNoAllocMaxEntries) return SI_ERR_UNSUPPORTED;
+  const RouterGeom g = router_geom(n_experts, hidden, n_tokens);
+  if (g.bytes > kNoAllocScratchBytes) return SI_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  si_status st = noalloc_scratch(&scratch);
+  if (st != SI_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the status word and the
+  // completion counters must start at zero (the epochs may keep counting).
+  if (cudaMemsetAsync(scratch, 0, g.off_flags, s) != cudaSuccess) return SI_ERR_CUDA;
+  return router_launch(x, x_type, w_router, w_type, hidden, n_experts, top_k, n_tokens, topk_ids,
+                       topk_w, logits_out, scratch, static_cast<uint32_t *>(scratch), s);
+}

@@ -186,13 +186,36 @@ typedef struct si_moe_layer {
  *   x_q8_1     device Q8_1 [H/32] blocks of x, or NULL (then quantised inside)
  *   topk_ids   device int32 [k]; topk_w device fp32 [k]
  *   routed_out device bf16 [H]; shared_out device bf16 [H] (ignored if no shared)
- *   n_tokens   must be 1 (batched tokens: si_moe_ffn_batched)
+ *   n_tokens   must be 1 (several tokens: si_moe_ffn_batched)
  */
 size_t si_moe_ffn_workspace_bytes(const si_moe_layer *L, int n_tokens);
 si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, const void *x,
                             const void *x_q8_1, const int32_t *topk_ids, const float *topk_w,
                             void *routed_out, void *shared_out, void *workspace,
                             size_t workspace_bytes, void *stream);
+
+/*
+ * si_moe_ffn_batched - routed experts for n_tokens tokens with per-token
+ * routing (not on the pages, which measure batch 1; the per-token arithmetic
+ * is si_moe_ffn_decode's).
+ *
+ * The (token, rank) pairs are grouped by expert so that each selected
+ * expert's rows are read once for all of its tokens; routed[t] =
+ * sum_r topk_w[t][r] * y_{t,r} in rank order, stored as bf16.
+ *   mode       SI_FFN_AUTO (0): SI_FFN_INT8 for now;
+ *              SI_FFN_INT8 (1): Q8_1 activations, exact int32 block dots, as
+ *                               si_moe_ffn_decode (n_tokens = 1 gives its bits);
+ *              SI_FFN_TENSOR (2): tensor-core mode (not built yet: SI_ERR_UNSUPPORTED)
+ *   x          device bf16 [n_tokens][H]
+ *   topk_ids   device int32 [n_tokens][k]; topk_w device fp32 [n_tokens][k]
+ *   routed_out device bf16 [n_tokens][H]
+ * Supported: Q4_K experts, no shared expert, n_tokens * k <= 1024, H <= 8192.
+ */
+enum { SI_FFN_AUTO = 0, SI_FFN_INT8 = 1, SI_FFN_TENSOR = 2 };
+size_t si_moe_ffn_batched_workspace_bytes(const si_moe_layer *L, int n_tokens);
+si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int mode, const void *x,
+                             const int32_t *topk_ids, const float *topk_w, void *routed_out,
+                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * si_add_rmsnorm3 - residual fold into the post-MoE RMSNorm ([R] item 2).

@@ -57,6 +57,9 @@ SIGNATURES = {
     "si_moe_ffn_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
     "si_moe_ffn_decode": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _vp, _sz, _vp]),
+    "si_moe_ffn_batched_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
+    "si_moe_ffn_batched": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                  _sz, _vp]),
     "si_add_rmsnorm3": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp, _vp]),
     "si_moe_layer_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer)]),
     "si_moe_layer_decode": (_i32, [ctypes.POINTER(SiMoeLayer), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -236,6 +239,28 @@ def si_moe_ffn_decode(layer: Layer, x: torch.Tensor, ids: torch.Tensor, w: torch
         _cuda(routed, "routed"), _opt(shared, "shared"), _cuda(ws, "ws"), ws.numel(),
         _stream(stream)), "si_moe_ffn_decode")
     return routed, shared
+
+
+SI_FFN_AUTO, SI_FFN_INT8, SI_FFN_TENSOR = 0, 1, 2
+
+
+def ffn_batched_workspace_bytes(layer: Layer, n_tokens: int) -> int:
+    return int(library().si_moe_ffn_batched_workspace_bytes(layer.ref, n_tokens))
+
+
+def si_moe_ffn_batched(layer: Layer, x: torch.Tensor, ids: torch.Tensor, w: torch.Tensor,
+                       mode: int = SI_FFN_AUTO, ws: torch.Tensor | None = None, stream=None):
+    """T tokens with per-token routing: x bf16 [T, H], ids int32 [T, k], w fp32 [T, k]
+    -> routed bf16 [T, H]."""
+    T, H = x.shape
+    routed = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(ffn_batched_workspace_bytes(layer, T), x.device)
+    _check(library().si_moe_ffn_batched(
+        layer.ref, T, mode, _cuda(x, "x"), _cuda(ids, "ids"), _cuda(w, "w"),
+        _cuda(routed, "routed"), _cuda(ws, "ws"), ws.numel(), _stream(stream)),
+        "si_moe_ffn_batched")
+    return routed
 
 
 def si_add_rmsnorm3(a, b, c, w_norm, eps: float = 1e-6, want_q8: bool = False, stream=None):

@@ -202,10 +202,13 @@ si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, const void *x,
  * The (token, rank) pairs are grouped by expert so that each selected
  * expert's rows are read once for all of its tokens; routed[t] =
  * sum_r topk_w[t][r] * y_{t,r} in rank order, stored as bf16.
- *   mode       SI_FFN_AUTO (0): SI_FFN_INT8 for now;
+ *   mode       SI_FFN_AUTO (0): SI_FFN_INT8 below 16 tokens, SI_FFN_TENSOR from 16;
  *              SI_FFN_INT8 (1): Q8_1 activations, exact int32 block dots, as
  *                               si_moe_ffn_decode (n_tokens = 1 gives its bits);
- *              SI_FFN_TENSOR (2): tensor-core mode (not built yet: SI_ERR_UNSUPPORTED)
+ *              SI_FFN_TENSOR (2): tcgen05 tensor cores, fp16 operands: weights
+ *                               dequantised (w = d*sc*q - dmin*m in fp32, then
+ *                               fp16), x converted to fp16, h = silu(g)*u in
+ *                               fp32 rounded to fp16; fp32 accumulation
  *   x          device bf16 [n_tokens][H]
  *   topk_ids   device int32 [n_tokens][k]; topk_w device fp32 [n_tokens][k]
  *   routed_out device bf16 [n_tokens][H]
@@ -293,6 +296,12 @@ si_status si_moe_ffn_gateup(const si_moe_layer *L, int n_tokens, const void *x,
  * budget_ns (<= 2 s) and writes SI_ERR_TIMEOUT to the workspace status word,
  * as every bounded wait of the library does. For testing that path. */
 si_status si_test_wait_timeout(uint64_t budget_ns, void *workspace, void *stream);
+
+/* D = A * B^T for one 128 x n x k block on the tensor cores (A fp16 [128][k],
+ * B fp16 [n][k] row-major; n in {16..64} step 16, k in {16..256} step 16;
+ * D fp32 [128][n]); workspace: 256 bytes, status word. */
+si_status si_test_umma_f16(const void *a, const void *b, int n, int k, float *out,
+                           void *workspace, void *stream);
 
 /* The unfused chain the fold replaced: t = bf16(a + b) by one kernel, then the
  * 2-input norm of (t, c) by a second. Same outputs as si_add_rmsnorm3. */

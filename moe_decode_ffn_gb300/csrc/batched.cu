@@ -23,6 +23,7 @@
 //  combine routed[t][j] = sum_r w[t][r] * y[pair(t, r)][j] in rank order.
 #include "common.cuh"
 #include "host.hpp"
+#include "tc.cuh"
 
 namespace si {
 
@@ -58,6 +59,10 @@ struct BatchedParams {
   float *y;                  // [T*k][H]
   __nv_bfloat16 *routed;     // [T][H]
   uint32_t *status;
+  // tensor-core mode
+  int tensor;                // 1: x -> fp16 rows instead of Q8_1 tiles
+  __half *xh;                // [T][H] fp16
+  __half *hh;                // [T*k][I] fp16
 };
 
 SI_DEV ActTile tile_at(uint8_t *rec, int n) {
@@ -75,7 +80,15 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
   if (blockIdx.x > 0) {
     // Token tiles: block b quantises token b - 1.
     const int t = blockIdx.x - 1;
-    if (t < p.T) {
+    if (t < p.T && p.tensor) {
+      for (int i = 8 * threadIdx.x; i < p.H; i += 8 * blockDim.x) {
+        float v[8];
+        Load8<__nv_bfloat16>::run(p.x + static_cast<size_t>(t) * p.H + i, v);
+        *reinterpret_cast<uint4 *>(p.xh + static_cast<size_t>(t) * p.H + i) =
+            make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
+                       pack_half2(v[6], v[7]));
+      }
+    } else if (t < p.T) {
       ActTile tile = tile_at(p.xrec + static_cast<size_t>(t) * tile_record_bytes(p.H), p.H);
       quantize_to_tile<__nv_bfloat16>(p.x + static_cast<size_t>(t) * p.H, p.H, tile);
     }
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kGuBThreads, 1) gateup_grouped_kernel(BatchedParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int units = p.I / 32;
   const int nsb = p.H / kQKK;
   const int xrb = tile_record_bytes(p.H);
@@ -211,7 +224,7 @@ __global__ void __launch_bounds__(kGuBThreads, 1) gateup_grouped_kernel(BatchedP
 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int tiles = p.H / kDownRows;
   const int nsb = p.I / kQKK;
   const int P = 2 * nsb;                 // half super-block pieces per row
@@ -273,6 +286,303 @@ __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedPara
   }
 }
 
+
+// ===========================================================================
+// Tensor-core mode (tcgen05, kind::f16): fp16 operands, fp32 accumulators in
+// tensor memory. Weights are dequantised from Q4_K (w = d*sc*q - dmin*m in
+// fp32, one rounding, then fp16) straight into K-major tiles; activations are
+// fp16 (x exactly from bf16, h rounded from fp32).
+// ===========================================================================
+constexpr int kTcThreads = 256;
+constexpr int kTcK = 256;                       // K elements per chunk (one super-block)
+constexpr int kTcMaxN = 64;                     // tokens per pass
+constexpr int kTcABytes = 128 * kTcK * 2;       // 64 KB
+constexpr int kTcBBytes = kTcMaxN * kTcK * 2;   // 32 KB
+constexpr int kTcSmem = 2 * kTcABytes + 2 * kTcBBytes + 64;
+constexpr int kTcTmemCols = 64;
+
+// Dequantise half `hf` (sub-blocks 4hf..4hf+3) of the Q4_K super-block at
+// `sb` (global) into fp16 row `row` of a K-major tile of kTcK columns.
+SI_DEV void dequant_half_to_tile(const uint8_t *sb, int hf, uint8_t *tile, int row) {
+  const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(sb));
+  int sc8[8], mn8[8];
+  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
+  q4k_unpack_scales(sw, sc8, mn8);
+  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    const int p = 2 * hf + pp;                        // code pair: sub-blocks 2p, 2p+1
+    const int j_lo = 2 * p, j_hi = 2 * p + 1;
+    const float s_lo = __fmul_rn(d, static_cast<float>(hf ? sc8[4 + 2 * pp] : sc8[2 * pp]));
+    const float s_hi = __fmul_rn(d, static_cast<float>(hf ? sc8[5 + 2 * pp] : sc8[2 * pp + 1]));
+    const float m_lo = __fmul_rn(dmin, static_cast<float>(hf ? mn8[4 + 2 * pp] : mn8[2 * pp]));
+    const float m_hi = __fmul_rn(dmin, static_cast<float>(hf ? mn8[5 + 2 * pp] : mn8[2 * pp + 1]));
+#pragma unroll
+    for (int q16 = 0; q16 < 2; ++q16) {
+      const uint4 c = __ldg(reinterpret_cast<const uint4 *>(sb + 16 + 32 * p + 16 * q16));
+      const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {                   // 8 elements per 16-byte store
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t word = cw[2 * g + w];
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const uint32_t b0 = (word >> (16 * b)) & 0xFF, b1 = (word >> (16 * b + 8)) & 0xFF;
+            lo[2 * w + b] = pack_half2(__fsub_rn(__fmul_rn(s_lo, static_cast<float>(b0 & 15)), m_lo),
+                                       __fsub_rn(__fmul_rn(s_lo, static_cast<float>(b1 & 15)), m_lo));
+            hi[2 * w + b] = pack_half2(__fsub_rn(__fmul_rn(s_hi, static_cast<float>(b0 >> 4)), m_hi),
+                                       __fsub_rn(__fmul_rn(s_hi, static_cast<float>(b1 >> 4)), m_hi));
+          }
+        }
+        const int e0 = 16 * q16 + 8 * g;              // element inside the sub-block
+        *reinterpret_cast<uint4 *>(tile + kmajor_offset(row, 32 * j_lo + e0, kTcK)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4 *>(tile + kmajor_offset(row, 32 * j_hi + e0, kTcK)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+    }
+  }
+}
+
+// Token rows (fp16, K chunk c) into a K-major tile; rows n >= nvalid are zero.
+// Source row of tile row n: rows[n] (a global index array) or, when rows is
+// null, row_base + n.
+SI_DEV void tokens_to_tile(const __half *src, const int *rows, int row_base, int nvalid, int npad,
+                           int ld, int k0, uint8_t *tile) {
+  for (int idx = threadIdx.x; idx < npad * (kTcK / 8); idx += blockDim.x) {
+    const int n = idx / (kTcK / 8), k8 = idx % (kTcK / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (n < nvalid) {
+      const int r = rows ? __ldcg(rows + n) : row_base + n;
+      v = __ldcg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(r) * ld + k0 + 8 * k8));
+    }
+    *reinterpret_cast<uint4 *>(tile + kmajor_offset(n, 8 * k8, kTcK)) = v;
+  }
+}
+
+// One 128 x npad x (nchunks * 256) product into tensor memory, A rows given by
+// `a_row_ptr(r)` (Q4_K rows, super-block c at +144 c), B rows by `tokens`.
+// Double-buffered: the threads dequantise chunk c+1 while the tensor core
+// multiplies chunk c. Returns false if a wait ran out.
+template <typename RowPtr>
+SI_DEV bool tc_product(RowPtr a_row_ptr, const __half *bsrc, const int *brows, int brow_base,
+                       int nvalid, int npad, int ldb, int nchunks, uint8_t *smem, uint64_t *bars,
+                       uint32_t *phase, uint32_t *pending, uint32_t taddr, uint32_t *status) {
+  const uint32_t idesc = umma_idesc_f16_f32(128, npad);
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    const int b = c & 1;
+    uint8_t *A = smem + b * kTcABytes;
+    uint8_t *B = smem + 2 * kTcABytes + b * kTcBBytes;
+    if (pending[b]) {
+      ok &= mbar_wait_bounded(&bars[b], phase[b], status);
+      phase[b] ^= 1u;
+      pending[b] = 0;
+    }
+    {
+      const int row = threadIdx.x >> 1, hf = threadIdx.x & 1;   // 256 threads: 128 rows x 2 halves
+      dequant_half_to_tile(a_row_ptr(row) + c * kQ4KBytes, hf, A, row);
+    }
+    tokens_to_tile(bsrc, brows, brow_base, nvalid, npad, ldb, c * kTcK, B);
+    fence_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t a0 = smem_addr(A), b0 = smem_addr(B);
+#pragma unroll 4
+      for (int ks = 0; ks < kTcK / 16; ++ks)
+        umma_f16(taddr, umma_desc_kmajor(a0 + 256 * ks, 128, kTcK * 16),
+                 umma_desc_kmajor(b0 + 256 * ks, 128, kTcK * 16), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+      umma_commit(&bars[b]);
+    }
+    pending[b] = 1;
+  }
+  for (int b = 0; b < 2; ++b) {
+    if (pending[b]) {
+      ok &= mbar_wait_bounded(&bars[b], phase[b], status);
+      phase[b] ^= 1u;
+      pending[b] = 0;
+    }
+  }
+  tc_fence_after();
+  return ok;
+}
+
+SI_DEV void tc_setup(uint8_t *smem, uint64_t *bars, uint32_t *s_taddr) {
+  if (threadIdx.x < 32) {
+    tmem_alloc(s_taddr, kTcTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+SI_DEV void tc_teardown(uint32_t taddr) {
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x < 32) tmem_dealloc(taddr, kTcTmemCols);
+}
+
+// gate/up: block = (active expert, 64 rows i0..i0+63): tile rows 0..63 are
+// gate rows, 64..127 the same up rows, so lane r and lane r + 64 of the
+// accumulator hold g and u of row i0 + r.
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gateup_kernel(BatchedParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * kTcABytes + 2 * kTcBBytes);
+  uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + 2);
+  grid_dep_wait();
+  grid_dep_launch();
+  const int tiles = p.I / 64;
+  const int na = __ldcg(p.n_active);
+  if (static_cast<int>(blockIdx.x) >= na * tiles) return;
+  const int e = __ldcg(p.active + blockIdx.x / tiles);
+  const int i0 = (blockIdx.x % tiles) * 64;
+  const int n_e = __ldcg(p.count + e), p0 = __ldcg(p.offset + e);
+  tc_setup(smem, bars, s_taddr);
+  const uint32_t taddr = *s_taddr;
+  uint32_t phase[2] = {0, 0}, pending[2] = {0, 0};
+  const size_t rowbase = static_cast<size_t>(e) * p.I + i0;
+  auto a_row = [&](int r) -> const uint8_t * {
+    return r < 64 ? p.wg + (rowbase + r) * p.rb_gu : p.wu + (rowbase + r - 64) * p.rb_gu;
+  };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *U = reinterpret_cast<float *>(smem);     // [64][kTcMaxN], reuses tile A0 after the MMAs
+  for (int nc0 = 0; nc0 < n_e; nc0 += kTcMaxN) {
+    const int nv = min(kTcMaxN, n_e - nc0), npad = (nv + 15) & ~15;
+    tc_product(a_row, p.xh, p.pair_token + p0 + nc0, 0, nv, npad, p.H, p.H / kTcK, smem, bars,
+               phase, pending, taddr, p.status);
+    // Accumulator rows 64..127 (up) to shared memory, then rows 0..63 (gate) combine.
+    if (warp >= 2 && warp < 4) {
+      const int r = 32 * warp + lane - 64;
+      for (int c8 = 0; c8 < npad; c8 += 8) {
+        float v[8];
+        tmem_ld8(taddr + (static_cast<uint32_t>(32 * warp) << 16) + c8, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) U[r * kTcMaxN + c8 + i] = v[i];
+      }
+    }
+    __syncthreads();
+    if (warp < 2) {
+      const int r = 32 * warp + lane;
+      for (int c8 = 0; c8 < npad; c8 += 8) {
+        float v[8];
+        tmem_ld8(taddr + (static_cast<uint32_t>(32 * warp) << 16) + c8, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int n = c8 + i;
+          if (n < nv) {
+            const float g = v[i], u = U[r * kTcMaxN + n];
+            const float h = __fdiv_rn(g, 1.f + expf(-g)) * u;
+            p.hh[static_cast<size_t>(p0 + nc0 + n) * p.I + i0 + r] = __float2half_rn(h);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  tc_teardown(taddr);
+}
+
+// down: block = (active expert, 128 output rows j0..j0+127).
+__global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(BatchedParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * kTcABytes + 2 * kTcBBytes);
+  uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + 2);
+  grid_dep_wait();
+  grid_dep_launch();
+  const int tiles = p.H / 128;
+  const int na = __ldcg(p.n_active);
+  if (static_cast<int>(blockIdx.x) >= na * tiles) return;
+  const int e = __ldcg(p.active + blockIdx.x / tiles);
+  const int j0 = (blockIdx.x % tiles) * 128;
+  const int n_e = __ldcg(p.count + e), p0 = __ldcg(p.offset + e);
+  tc_setup(smem, bars, s_taddr);
+  const uint32_t taddr = *s_taddr;
+  uint32_t phase[2] = {0, 0}, pending[2] = {0, 0};
+  auto a_row = [&](int r) -> const uint8_t * {
+    return p.wd + (static_cast<size_t>(e) * p.H + j0 + r) * p.rb_d;
+  };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int nc0 = 0; nc0 < n_e; nc0 += kTcMaxN) {
+    const int nv = min(kTcMaxN, n_e - nc0), npad = (nv + 15) & ~15;
+    // h rows of this expert's pairs are contiguous: p0 + nc0 + n.
+    tc_product(a_row, p.hh, nullptr, p0 + nc0, nv, npad, p.I, p.I / kTcK, smem, bars, phase,
+               pending, taddr, p.status);
+    if (warp < 4) {
+      const int r = 32 * warp + lane;
+      for (int c8 = 0; c8 < npad; c8 += 8) {
+        float v[8];
+        tmem_ld8(taddr + (static_cast<uint32_t>(32 * warp) << 16) + c8, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c8 + i < nv) p.y[static_cast<size_t>(p0 + nc0 + c8 + i) * p.H + j0 + r] = v[i];
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  tc_teardown(taddr);
+}
+
+// Test: D = A * B^T for one 128 x n x k block (fp16 row-major inputs, k a
+// multiple of 16 up to 256, n a multiple of 16 up to 64), through the same
+// descriptors, MMA, commit and tensor-memory loads as the kernels above.
+__global__ void __launch_bounds__(kTcThreads, 1) tc_test_kernel(const __half *a, const __half *b,
+                                                               int n, int k, float *out,
+                                                               uint32_t *status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * kTcABytes + 2 * kTcBBytes);
+  uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + 2);
+  tc_setup(smem, bars, s_taddr);
+  const uint32_t taddr = *s_taddr;
+  for (int idx = threadIdx.x; idx < 128 * (k / 8); idx += blockDim.x) {
+    const int r = idx / (k / 8), k8 = idx % (k / 8);
+    *reinterpret_cast<uint4 *>(smem + kmajor_offset(r, 8 * k8, kTcK)) =
+        *reinterpret_cast<const uint4 *>(a + r * k + 8 * k8);
+  }
+  for (int idx = threadIdx.x; idx < n * (k / 8); idx += blockDim.x) {
+    const int r = idx / (k / 8), k8 = idx % (k / 8);
+    *reinterpret_cast<uint4 *>(smem + 2 * kTcABytes + kmajor_offset(r, 8 * k8, kTcK)) =
+        *reinterpret_cast<const uint4 *>(b + r * k + 8 * k8);
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc_fence_after();
+    const uint32_t idesc = umma_idesc_f16_f32(128, n);
+    for (int ks = 0; ks < k / 16; ++ks)
+      umma_f16(taddr, umma_desc_kmajor(smem_addr(smem) + 256 * ks, 128, kTcK * 16),
+               umma_desc_kmajor(smem_addr(smem + 2 * kTcABytes) + 256 * ks, 128, kTcK * 16), idesc,
+               ks > 0 ? 1u : 0u);
+    umma_commit(&bars[0]);
+  }
+  mbar_wait_bounded(&bars[0], 0, status);
+  tc_fence_after();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < 4) {
+    for (int c8 = 0; c8 < n; c8 += 8) {
+      float v[8];
+      tmem_ld8(taddr + (static_cast<uint32_t>(32 * warp) << 16) + c8, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[(32 * warp + lane) * n + c8 + i] = v[i];
+    }
+  }
+  tc_teardown(taddr);
+}
+
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(BatchedParams p) {
   grid_dep_wait();
@@ -291,7 +601,7 @@ __global__ void __launch_bounds__(256) combine_kernel(BatchedParams p) {
 // ---------------------------------------------------------------------------
 struct BatchedGeom {
   size_t off_count, off_offset, off_active, off_nactive, off_pair_token, off_pair_of, off_xrec,
-      off_hrec, off_y, bytes;
+      off_hrec, off_y, off_xh, off_hh, bytes;
 };
 
 static BatchedGeom batched_geom(const si_moe_layer &L, int T) {
@@ -311,6 +621,8 @@ static BatchedGeom batched_geom(const si_moe_layer &L, int T) {
   take(g.off_xrec, static_cast<size_t>(T) * tile_record_bytes(L.hidden));
   take(g.off_hrec, P * tile_record_bytes(L.inter));
   take(g.off_y, P * L.hidden * 4);
+  take(g.off_xh, static_cast<size_t>(T) * L.hidden * 2);
+  take(g.off_hh, P * L.inter * 2);
   g.bytes = off;
   return g;
 }
@@ -344,6 +656,8 @@ cudaError_t preload_batched() {
   const void *ks[] = {reinterpret_cast<const void *>(batched_prep_kernel),
                       reinterpret_cast<const void *>(gateup_grouped_kernel),
                       reinterpret_cast<const void *>(down_grouped_kernel),
+                      reinterpret_cast<const void *>(tc_gateup_kernel),
+                      reinterpret_cast<const void *>(tc_down_kernel),
                       reinterpret_cast<const void *>(combine_kernel)};
   for (const void *k : ks) {
     const cudaError_t e = cudaFuncGetAttributes(&a, k);
@@ -367,7 +681,7 @@ extern "C" si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int
                                         size_t workspace_bytes, void *stream) {
   if (!L || !x || !topk_ids || !topk_w || !routed_out) return SI_ERR_INVALID_ARG;
   if (mode != 0 && mode != 1 && mode != 2) return SI_ERR_INVALID_ARG;
-  if (mode == 2) return SI_ERR_UNSUPPORTED;   // tensor-core mode: not built yet
+  const bool tensor = mode == 2 || (mode == 0 && n_tokens >= 16);
   const si_status st = batched_check(*L, n_tokens);
   if (st != SI_OK) return st;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
@@ -397,7 +711,27 @@ extern "C" si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int
   p.y = reinterpret_cast<float *>(base + g.off_y);
   p.routed = static_cast<__nv_bfloat16 *>(routed_out);
   p.status = reinterpret_cast<uint32_t *>(base);
+  p.tensor = tensor ? 1 : 0;
+  p.xh = reinterpret_cast<__half *>(base + g.off_xh);
+  p.hh = reinterpret_cast<__half *>(base + g.off_hh);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (tensor) {
+    if (L->hidden % 128 || L->inter % 256) return SI_ERR_UNSUPPORTED;
+    const int max_active = n_tokens * L->top_k < L->n_experts ? n_tokens * L->top_k : L->n_experts;
+    cudaError_t e = allow_smem(tc_gateup_kernel, kTcSmem);
+    if (e == cudaSuccess) e = allow_smem(tc_down_kernel, kTcSmem);
+    if (e == cudaSuccess)
+      e = launch_pdl(batched_prep_kernel, dim3(1 + n_tokens), dim3(kPrepThreads), 0, s, p);
+    if (e == cudaSuccess)
+      e = launch_pdl(tc_gateup_kernel, dim3(max_active * (L->inter / 64)), dim3(kTcThreads),
+                     kTcSmem, s, p);
+    if (e == cudaSuccess)
+      e = launch_pdl(tc_down_kernel, dim3(max_active * (L->hidden / 128)), dim3(kTcThreads),
+                     kTcSmem, s, p);
+    if (e == cudaSuccess)
+      e = launch_pdl(combine_kernel, dim3((L->hidden + 255) / 256, n_tokens), dim3(256), 0, s, p);
+    return cuda_status(e);
+  }
   const int units = L->inter / 32, tiles = L->hidden / kDownRows;
   const int max_active = n_tokens * L->top_k < L->n_experts ? n_tokens * L->top_k : L->n_experts;
   const size_t gsm = gateup_grouped_smem(*L), dsm = down_grouped_smem(*L);
@@ -412,5 +746,17 @@ extern "C" si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int
     e = launch_pdl(down_grouped_kernel, dim3(max_active * tiles), dim3(kDownBThreads), dsm, s, p);
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel, dim3((L->hidden + 255) / 256, n_tokens), dim3(256), 0, s, p);
+  return cuda_status(e);
+}
+
+extern "C" si_status si_test_umma_f16(const void *a, const void *b, int n, int k, float *out,
+                                      void *workspace, void *stream) {
+  if (!a || !b || !out || !workspace || !aligned16(a) || !aligned16(b)) return SI_ERR_INVALID_ARG;
+  if (n < 16 || n > kTcMaxN || n % 16 || k < 16 || k > kTcK || k % 16) return SI_ERR_INVALID_ARG;
+  cudaError_t e = allow_smem(tc_test_kernel, kTcSmem);
+  if (e == cudaSuccess)
+    e = launch_pdl(tc_test_kernel, dim3(1), dim3(kTcThreads), kTcSmem,
+                   static_cast<cudaStream_t>(stream), static_cast<const __half *>(a),
+                   static_cast<const __half *>(b), n, k, out, static_cast<uint32_t *>(workspace));
   return cuda_status(e);
 }

@@ -105,3 +105,64 @@ def test_batched_rejects_unsupported():
     assert e.value.status == m.SI_ERR_INVALID_ARG
     shared_layer = device_layer(gen.Q4K_LAYER_SHARED_Q4_K, 100, 0)
     assert m.ffn_batched_workspace_bytes(shared_layer, 2) == 0
+
+
+# ---------------------------------------------------------------------------
+# tensor-core mode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,k", [(16, 16), (32, 64), (64, 256), (48, 128)])
+def test_umma_f16_block_exact(n, k):
+    """Small integers: every product and sum is exact in fp32, so the tensor
+    core result must equal the integer matrix product exactly."""
+    g = torch.Generator().manual_seed(n * 1000 + k)
+    a = torch.randint(-4, 5, (128, k), generator=g).to(torch.float16)
+    b = torch.randint(-4, 5, (n, k), generator=g).to(torch.float16)
+    out = torch.empty(128, n, dtype=torch.float32, device="cuda")
+    ws = m.workspace(256)
+    da, db = a.cuda(), b.cuda()      # keep the device copies alive until the kernel has run
+    st = m.library().si_test_umma_f16(da.data_ptr(), db.data_ptr(), n, k, out.data_ptr(),
+                                      ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == m.SI_OK
+    assert m.si_workspace_status(ws) == m.SI_OK
+    ref = a.double().numpy() @ b.double().numpy().T
+    assert np.array_equal(out.cpu().double().numpy(), ref)
+
+
+def check_tokens_fp16(routed, x, ids, w, tokens):
+    host = host_layer_all(SPEC, SEED, 0)
+    for t in tokens:
+        f = M.moe_ffn(host, M.as_f64(x[t]), ids[t].tolist(), w[t].double().numpy(), mode="fp16")
+        ok, rep = P.float_parity(bf16_np(routed[t]), F.bf16(f["routed"]))
+        assert ok, f"token {t}: {rep}"
+
+
+@pytest.mark.parametrize("T", [16, 64])
+def test_batched_tensor_against_oracle_fp16_mode(T):
+    dev = device_layer(SPEC, SEED, 0)
+    ids, w = routing(T + 100, T)
+    x = gen.make_tokens(950 + T, T)
+    routed = m.si_moe_ffn_batched(dev, x.cuda(), ids.cuda(), w.cuda(), m.SI_FFN_TENSOR)
+    torch.cuda.synchronize()
+    check_tokens_fp16(routed.cpu(), x, ids, w, range(0, T, 5))
+
+
+def test_batched_tensor_tokens_sharing_experts():
+    T = 40
+    dev = device_layer(SPEC, SEED, 0)
+    ids, w = routing(8, T, same=True)
+    x = gen.make_tokens(951, T)
+    ws = m.workspace(m.ffn_batched_workspace_bytes(dev, T))
+    routed = m.si_moe_ffn_batched(dev, x.cuda(), ids.cuda(), w.cuda(), m.SI_FFN_TENSOR, ws=ws)
+    torch.cuda.synchronize()
+    assert m.si_workspace_status(ws) == m.SI_OK
+    check_tokens_fp16(routed.cpu(), x, ids, w, [0, 21, 39])
+
+
+def test_batched_auto_mode_switches_at_16_tokens():
+    dev = device_layer(SPEC, SEED, 0)
+    ids, w = routing(9, 16)
+    x = gen.make_tokens(952, 16).cuda()
+    auto = m.si_moe_ffn_batched(dev, x, ids.cuda(), w.cuda(), m.SI_FFN_AUTO)
+    tensor = m.si_moe_ffn_batched(dev, x, ids.cuda(), w.cuda(), m.SI_FFN_TENSOR)
+    assert torch.equal(auto, tensor)

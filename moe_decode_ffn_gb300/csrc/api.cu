@@ -206,6 +206,10 @@ extern "C" size_t si_moe_stack_workspace_bytes(const si_moe_layer *layers, int n
     if (layer_check(layers[l]) != SI_OK) return 0;
     off += stack_layer_bytes(layers[l]);
   }
+  if (stack_supported(layers, n_layers)) {
+    const size_t pk = stack_workspace_bytes(layers, n_layers);
+    if (pk > off) off = pk;
+  }
   return off;
 }
 
@@ -231,35 +235,46 @@ extern "C" si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n
     return SI_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (preload_router() != cudaSuccess || preload_ffn() != cudaSuccess ||
-      preload_norm() != cudaSuccess)
+      preload_norm() != cudaSuccess || preload_stack() != cudaSuccess)
     return SI_ERR_CUDA;
   cudaStreamCaptureStatus cs;
   if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return SI_ERR_CUDA;
   if (cs != cudaStreamCaptureStatusNone) return SI_ERR_INVALID_ARG;
+  // The persistent kernel serves stacks of Q4_K layers; other layer types run
+  // as four kernels per layer.
+  const bool persistent = stack_supported(layers, n_layers);
+  if (persistent) {
+    const si_status sp = stack_prepare(layers, n_layers, workspace, s);
+    if (sp != SI_OK) return sp;
+  }
   if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return SI_ERR_CUDA;
 
   uint8_t *base = static_cast<uint8_t *>(workspace);
   uint32_t *status = reinterpret_cast<uint32_t *>(base);
   si_status st = SI_OK;
-  for (int t = 0; t < n_tokens && st == SI_OK; ++t) {
-    const __nv_bfloat16 *xt = static_cast<const __nv_bfloat16 *>(x_in) + static_cast<size_t>(t) * H;
-    const void *x = xt, *res = xt;
-    size_t off = sizeof(WsHeader);
-    for (int l = 0; l < n_layers && st == SI_OK; ++l) {
-      const si_moe_layer &L = layers[l];
-      uint8_t *lws = base + off;
-      const size_t lb = layer_geom(L).bytes;
-      void *sum = lws + lb;
-      void *y = lws + lb + 2 * static_cast<size_t>(H);
-      if (l == n_layers - 1) {
-        y = static_cast<__nv_bfloat16 *>(y_out) + static_cast<size_t>(t) * H;
-        if (sum_out) sum = static_cast<__nv_bfloat16 *>(sum_out) + static_cast<size_t>(t) * H;
+  if (persistent) {
+    st = stack_launch(layers, n_layers, n_tokens, x_in, y_out, sum_out, ids_out, workspace, s);
+  } else {
+    for (int t = 0; t < n_tokens && st == SI_OK; ++t) {
+      const __nv_bfloat16 *xt = static_cast<const __nv_bfloat16 *>(x_in) + static_cast<size_t>(t) * H;
+      const void *x = xt, *res = xt;
+      size_t off = sizeof(WsHeader);
+      for (int l = 0; l < n_layers && st == SI_OK; ++l) {
+        const si_moe_layer &L = layers[l];
+        uint8_t *lws = base + off;
+        const size_t lb = layer_geom(L).bytes;
+        void *sum = lws + lb;
+        void *y = lws + lb + 2 * static_cast<size_t>(H);
+        if (l == n_layers - 1) {
+          y = static_cast<__nv_bfloat16 *>(y_out) + static_cast<size_t>(t) * H;
+          if (sum_out) sum = static_cast<__nv_bfloat16 *>(sum_out) + static_cast<size_t>(t) * H;
+        }
+        int32_t *ids = ids_out ? ids_out + (static_cast<size_t>(t) * n_layers + l) * k : nullptr;
+        st = layer_enqueue(L, x, res, sum, y, ids, nullptr, nullptr, nullptr, lws, status, s);
+        x = y;
+        res = sum;
+        off += stack_layer_bytes(L);
       }
-      int32_t *ids = ids_out ? ids_out + (static_cast<size_t>(t) * n_layers + l) * k : nullptr;
-      st = layer_enqueue(L, x, res, sum, y, ids, nullptr, nullptr, nullptr, lws, status, s);
-      x = y;
-      res = sum;
-      off += stack_layer_bytes(L);
     }
   }
   cudaGraph_t graph = nullptr;

@@ -51,10 +51,20 @@ SI_DEV uint64_t globaltimer_ns() {
     if (threadIdx.x == 0 && blockIdx.x < kTraceBlocks && blockIdx.y == 0)                    \
       g_si_trace[(kernel)][blockIdx.x][(phase)] = globaltimer_ns();                          \
   } while (0)
+// Latest %globaltimer over the block's threads (any thread may call it).
+#define SI_TRACE_LATEST(kernel, phase)                                                       \
+  do {                                                                                       \
+    if (blockIdx.x < kTraceBlocks && blockIdx.y == 0)                                        \
+      atomicMax(reinterpret_cast<unsigned long long *>(&g_si_trace[(kernel)][blockIdx.x][(phase)]), \
+                static_cast<unsigned long long>(globaltimer_ns()));                          \
+  } while (0)
 #else
 #define SI_TRACE_BUFFER
 #define SI_TRACE_MARK(kernel, phase) \
   do {                               \
+  } while (0)
+#define SI_TRACE_LATEST(kernel, phase) \
+  do {                                 \
   } while (0)
 #endif
 
@@ -104,10 +114,10 @@ SI_DEV uint64_t now_ns() {
 }
 
 // Wait for phase `parity` of `bar` for at most `budget_ns`. Returns false on
-// timeout (after recording SI_ERR_TIMEOUT).
-SI_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t *status,
-                              uint64_t budget_ns = kWaitBudgetNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+// timeout (after recording SI_ERR_TIMEOUT). The spin loop is out of line so
+// that every call site stays one try_wait long.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
+                                                   uint32_t *status, uint64_t budget_ns) {
   const uint64_t t0 = now_ns();
   for (;;) {
 #pragma unroll 1
@@ -117,6 +127,11 @@ SI_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t *status,
   }
   record_status(status, SI_ERR_TIMEOUT);
   return false;
+}
+SI_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t *status,
+                              uint64_t budget_ns = kWaitBudgetNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, status, budget_ns);
 }
 
 // Global -> shared bulk copy completing on `bar` (bytes and both addresses
@@ -326,8 +341,63 @@ SI_DEV void q4k_isums(const uint4 *w, const uint4 *a, int isum[8], uint32_t &dd,
   }
 }
 
-// Half of a Q4_K super-block (sub-blocks 4h..4h+3, 128 weights):
-// d*sum_j sc_j*d_a(j)*isum_j - dmin*sum_j m_j*s_a(j) over those j, fp32.
+// Pairs [p0, p0 + np) of one Q4_K super-block (pair p = sub-blocks 2p and
+// 2p + 1, 64 weights): d * sum_j sc_j*d_a(j)*isum_j - dmin * sum_j m_j*s_a(j)
+// over those j, the two sums accumulated in sub-block order, then one
+// rounding per product and one for the difference. w: the 144-byte
+// super-block, a: its 256 activation codes (both 16-byte aligned, shared
+// memory); da, sa: the activation scales and sums of its 8 blocks. A rolled
+// loop kept out of line: one copy of the code serves every caller.
+static __device__ __noinline__ float q4k_dot_pairs(const uint8_t *w, const uint8_t *a,
+                                                   const float *da, const float *sa, int p0,
+                                                   int np) {
+  float acc_d = 0.f, acc_m = 0.f;
+  const uint8_t *sb = w + 4;   // the 12 scale bytes
+#pragma unroll 1
+  for (int p = p0; p < p0 + np; ++p) {
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(w + 16 + 32 * p);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(w + 32 + 32 * p);
+    const uint4 *ap = reinterpret_cast<const uint4 *>(a + 64 * p);
+    const uint4 al0 = ap[0], al1 = ap[1], ah0 = ap[2], ah1 = ap[3];
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+    const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+    int lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lo = __dp4a(static_cast<int>(qw[i] & 0x0F0F0F0Fu), static_cast<int>(aw_lo[i]), lo);
+      hi = __dp4a(static_cast<int>((qw[i] >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[i]), hi);
+    }
+    // 6-bit scale and min of sub-blocks j = 2p, 2p + 1 (j < 4: low 6 bits of
+    // bytes j, j + 4; j >= 4: nibbles of byte j + 4 plus the top 2 bits of
+    // bytes j - 4, j)
+    int sc[2], mn[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = 2 * p + e;
+      if (j < 4) {
+        sc[e] = sb[j] & 63;
+        mn[e] = sb[j + 4] & 63;
+      } else {
+        sc[e] = (sb[j + 4] & 0x0F) | ((sb[j - 4] >> 6) << 4);
+        mn[e] = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);
+      }
+    }
+    acc_d = fmaf(static_cast<float>(sc[0] * lo), da[2 * p], acc_d);
+    acc_d = fmaf(static_cast<float>(sc[1] * hi), da[2 * p + 1], acc_d);
+    acc_m = fmaf(static_cast<float>(mn[0]), sa[2 * p], acc_m);
+    acc_m = fmaf(static_cast<float>(mn[1]), sa[2 * p + 1], acc_m);
+  }
+  const uint32_t dd = *reinterpret_cast<const uint32_t *>(w);
+  const float d = half_bits_to_float(static_cast<uint16_t>(dd & 0xFFFF));
+  const float dmin = half_bits_to_float(static_cast<uint16_t>(dd >> 16));
+  return __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
+}
+
+// The same two functions fully unrolled and inline, for kernels that run
+// once per launch (their code is fetched once): half of a super-block
+// (sub-blocks 4h..4h+3, 128 weights) and the whole super-block. Same order of
+// accumulation and rounding as q4k_dot_pairs, so the same bits.
 SI_DEV float q4k_half_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa,
                           int h) {
   const uint4 hd = w[0];
@@ -363,10 +433,9 @@ SI_DEV float q4k_half_dot(const uint4 *w, const uint4 *a, const float *da, const
   }
   const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
   const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
-  return d * acc_d - dmin * acc_m;
+  return __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
 }
 
-// d*sum_j sc_j*d_a(j)*isum_j - dmin*sum_j m_j*s_a(j), fp32.
 SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa) {
   int isum[8], sc[8], mn[8];
   uint32_t dd, sw[3];
@@ -380,7 +449,7 @@ SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const f
   }
   const float d = half_bits_to_float(static_cast<uint16_t>(dd & 0xFFFF));
   const float dmin = half_bits_to_float(static_cast<uint16_t>(dd >> 16));
-  return d * acc_d - dmin * acc_m;
+  return __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
 }
 
 // Q8_0 x Q8_1 over 256 weights = 8 Q8_0 blocks (272 bytes, 16-byte aligned).

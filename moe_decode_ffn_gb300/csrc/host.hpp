@@ -53,6 +53,17 @@ cudaError_t preload_router();
 cudaError_t preload_ffn();
 cudaError_t preload_norm();
 
+// ---- persistent layer-stack kernel (stack.cu)
+// Whether one cooperative launch can run these layers (shapes, formats, SM
+// count, shared memory); the workspace it needs; copying the per-layer pointer
+// table into that workspace (synchronous, outside capture); the launch.
+bool stack_supported(const si_moe_layer *layers, int n_layers);
+size_t stack_workspace_bytes(const si_moe_layer *layers, int n_layers);
+si_status stack_prepare(const si_moe_layer *layers, int n_layers, void *ws, cudaStream_t s);
+si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, const void *x_in,
+                       void *y_out, void *sum_out, int32_t *ids_out, void *ws, cudaStream_t s);
+cudaError_t preload_stack();
+
 // ---- router geometry (depends only on the shapes, so the workspace size does too)
 struct RouterGeom {
   int row_tiles;     // ceil(E / 8): one warp per expert row

@@ -99,8 +99,12 @@ def test_stack_graph_against_oracle_chain():
     g.close()
 
 
-def test_stack_graph_equals_eager_layers_and_replays_bit_exact():
-    spec = gen.Q4K_LAYER_SHARED_Q8_0
+@pytest.mark.parametrize("name", ["q4k_shared_q8_0", "q4k_shared_q4k"])
+def test_stack_graph_equals_eager_layers_and_replays_bit_exact(name):
+    """The Q4_K-shared stack runs as one persistent kernel, the Q8_0-shared one
+    as four kernels per layer: both must reproduce the per-layer calls bit for
+    bit, and every replay of the graph must give the same bits."""
+    spec = SPECS[name]
     layers = _stack_layers(spec, 4, seed=300)
     x = gen.make_tokens(900, 3).cuda()
     g = m.StackGraph(layers, x)

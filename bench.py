@@ -53,8 +53,8 @@ BYTES_ROUTED = 8 * 3 * Q4K_MATRIX                       # 14,155,776
 BYTES_SHARED = 3 * Q4K_MATRIX                           # 1,769,472
 BYTES_SIGMOID = 2048 * 2
 BYTES_LAYER_TOKEN = BYTES_ROUTER + BYTES_ROUTED + BYTES_SHARED + BYTES_SIGMOID   # 16,977,920
-# Gate/up kernel (the dominant one): 8 experts' gate+up rows + shared gate+up.
-BYTES_GATEUP = 8 * 2 * Q4K_MATRIX + 2 * Q4K_MATRIX      # 10,616,832
+STACK_KERNEL_SOURCES = ["moe_decode_ffn_gb300/csrc/stack.cu", "moe_decode_ffn_gb300/csrc/common.cuh",
+                        "moe_decode_ffn_gb300/csrc/topk.cuh"]
 
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -126,9 +126,10 @@ def _dist():
 
 
 def _traffic_record(kernel_sources):
-    """Per-launch DRAM traffic of the gate/up kernel from the committed ncu
-    summary, valid only while the kernel sources match the captured ones."""
-    path = os.path.join(ROOT, "profiles", "gateup_q4k_traffic.json")
+    """DRAM bytes per layer-token of the persistent stack kernel from the
+    committed ncu record, valid only while the kernel sources match the
+    captured ones."""
+    path = os.path.join(ROOT, "profiles", "stack_q4k_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -140,7 +141,7 @@ def _traffic_record(kernel_sources):
             h.update(f.read())
     if rec.get("source_sha256") != h.hexdigest():
         return None
-    return rec.get("bytes_per_launch")
+    return rec.get("bytes_per_layer_token")
 
 
 def oracle_jobs(n_layer_tokens: int, device="cpu"):
@@ -285,37 +286,21 @@ def run_gpu(args):
         e2e_ms = float(t.item())
     e2e_value = e2e_ms * 1e3 / (N_LAYERS * N_TOKENS) / world
 
-    # --- dominant kernel: gate/up alone, chained, with the timed run's routing --
-    ids_all = graph.ids.clone()   # [T][L][k]
-    ffn_ws = [m.workspace(m.ffn_workspace_bytes(L), dev) for L in layers]
-    gu = torch.cuda.CUDAGraph()
-    n_gu = N_LAYERS * N_TOKENS
-    with torch.cuda.stream(stream):
-        for t in range(2):
-            for l, L in enumerate(layers):
-                lib.si_moe_ffn_gateup(L.ref, 1, graph.y[t].data_ptr(), None,
-                                      ids_all[t, l].data_ptr(), ffn_ws[l].data_ptr(),
-                                      ffn_ws[l].numel(), stream.cuda_stream)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(gu, stream=stream):
-        for t in range(N_TOKENS):
-            for l, L in enumerate(layers):
-                st = lib.si_moe_ffn_gateup(L.ref, 1, graph.y[t].data_ptr(), None,
-                                           ids_all[t, l].data_ptr(), ffn_ws[l].data_ptr(),
-                                           ffn_ws[l].numel(), stream.cuda_stream)
-                assert st == 0
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            gu.replay()
-        e0.record(stream)
-        for _ in range(3):
-            gu.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    gu_us = e0.elapsed_time(e1) * 1e3 / (3 * n_gu)
-    gu_gbs = BYTES_GATEUP / (gu_us * 1e-6) / 1e9
-    traffic = _traffic_record(["moe_decode_ffn_gb300/csrc/ffn.cu",
-                               "moe_decode_ffn_gb300/csrc/common.cuh"])
+    # --- the same stack through four kernels per layer (context) --------------
+    per_layer_us = None
+    if graph.persistent and not args.no_per_layer_path:
+        gl = m.StackGraph(layers, x_in, mode=m.SI_STACK_PER_LAYER)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                gl.launch(stream)
+            e0.record(stream)
+            for _ in range(3):
+                gl.launch(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        per_layer_us = e0.elapsed_time(e1) * 1e3 / (3 * N_LAYERS * N_TOKENS)
+        gl.close()
+    traffic_lt = _traffic_record(STACK_KERNEL_SOURCES) if graph.persistent else None
 
     if rank != 0:
         return 0
@@ -323,7 +308,14 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         jobs = oracle_jobs(args.cpu_layer_tokens, device=dev)
         cpu_us, cpu_n = time_oracle(jobs) * 1e6, len(jobs)
-    launches = args.steps * N_LAYERS * N_TOKENS * 4
+    launches = args.steps * (1 if graph.persistent else N_LAYERS * N_TOKENS * 4)
+    # The timed path is one persistent kernel launch per step (the dominant and
+    # only kernel): algorithmic bytes per launch = weight bytes of all
+    # 40 x 128 layer-tokens.
+    lt_per_launch = N_LAYERS * N_TOKENS if graph.persistent else 1
+    launch_us = ms_step * 1e3 / (1 if graph.persistent else N_LAYERS * N_TOKENS * 4)
+    bytes_launch = BYTES_LAYER_TOKEN * lt_per_launch
+    achieved = bytes_launch / (launch_us * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(value_job, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
@@ -337,15 +329,21 @@ def run_gpu(args):
         "weight_read": {"bytes_per_layer_token": BYTES_LAYER_TOKEN,
                         "gbs": round(gbs_stage, 1), "frac_of_peak": round(gbs_stage / peak, 4),
                         "peak_gbs": peak, "peak_kind": peak_kind},
-        "roofline": {"kernel": "gateup_q_kernel (routed + shared gate/up GEMV, SiLU, Q8_1 of h)",
-                     "bound": "hbm", "achieved": round(gu_gbs, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(gu_gbs / peak, 4),
-                     "traffic": traffic, "bytes_per_launch": BYTES_GATEUP,
-                     "avg_launch_us": round(gu_us, 3), "peak_kind": peak_kind},
+        "roofline": {"kernel": ("stack_kernel (persistent: router + top-k, routed and shared "
+                                "experts, residual + RMSNorm of all 40 layers x 128 tokens)"
+                                if graph.persistent else "four kernels per layer"),
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": (round(traffic_lt * lt_per_launch) if traffic_lt else None),
+                     "bytes_per_launch": bytes_launch, "avg_launch_us": round(launch_us, 1),
+                     "peak_kind": peak_kind},
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
                 "d2h_bytes_per_step": h_out.numel() * h_out.element_size()},
         "gpu_launches": launches,
+        "per_layer_path": ({"value": round(per_layer_us, 3), "unit": UNIT,
+                            "what": "same stack, four kernels per layer and token"}
+                           if per_layer_us is not None else None),
         "clocks": clk.summary(),
         "device_status": m.status_string(status), "ids_valid": ids_ok,
     }
@@ -367,6 +365,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-layer-tokens", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-layer-path", action="store_true",
+                    help="skip timing the four-kernels-per-layer path")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -271,6 +271,33 @@ si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n_layers, in
                                     const void *x_in, void *y_out, void *sum_out,
                                     int32_t *ids_out, void *workspace, size_t workspace_bytes,
                                     void *stream, si_graph **graph_out);
+/*
+ * The same with the execution path chosen by the caller:
+ *   SI_STACK_AUTO        as si_moe_stack_graph_create: the persistent kernel
+ *                        whenever it supports the layers, else per layer;
+ *   SI_STACK_PER_LAYER   four kernels per layer and token (router + top-k,
+ *                        gate/up, down, add + RMSNorm), chained with
+ *                        programmatic dependent launch;
+ *   SI_STACK_PERSISTENT  one cooperative kernel, one block per SM, for the
+ *                        whole stack ("perf(qwen3.6): fuse decode kernel
+ *                        launches", Summary: decode is launch bound); returns
+ *                        SI_ERR_UNSUPPORTED unless every layer has Q4_K routed
+ *                        experts, a Q4_K or no shared expert and a bf16 router,
+ *                        all layers share one shape with H a multiple of 2048
+ *                        (<= 4096), E even (<= 256), top_k <= 8, n_layers <= 128,
+ *                        and one block per SM covers every gate/up unit of 32
+ *                        rows. Its workspace also carries the epoch of its
+ *                        exchange tags, which advances with every replay.
+ * Both paths give bit-identical results. si_graph_is_persistent returns 1 for
+ * a graph holding the persistent kernel, 0 for the per-layer path, -1 for NULL.
+ */
+enum { SI_STACK_AUTO = 0, SI_STACK_PER_LAYER = 1, SI_STACK_PERSISTENT = 2 };
+si_status si_moe_stack_graph_create_mode(const si_moe_layer *layers, int n_layers, int n_tokens,
+                                         const void *x_in, void *y_out, void *sum_out,
+                                         int32_t *ids_out, void *workspace,
+                                         size_t workspace_bytes, int mode, void *stream,
+                                         si_graph **graph_out);
+int si_graph_is_persistent(const si_graph *graph);
 si_status si_graph_launch(si_graph *graph, void *stream);
 void si_graph_destroy(si_graph *graph);
 

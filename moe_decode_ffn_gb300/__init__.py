@@ -67,6 +67,10 @@ SIGNATURES = {
     "si_moe_stack_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
     "si_moe_stack_graph_create": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _i32, _vp, _vp, _vp,
                                          _vp, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
+    "si_moe_stack_graph_create_mode": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _i32, _vp, _vp,
+                                              _vp, _vp, _vp, _sz, _i32, _vp,
+                                              ctypes.POINTER(_vp)]),
+    "si_graph_is_persistent": (_i32, [_vp]),
     "si_graph_launch": (_i32, [_vp, _vp]),
     "si_graph_destroy": (None, [_vp]),
     "si_workspace_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
@@ -300,10 +304,17 @@ def si_moe_layer_decode(layer: Layer, x, residual=None, ws=None, stream=None) ->
     return out
 
 
-class StackGraph:
-    """n_layers x n_tokens decode captured as one CUDA graph (buffers owned here)."""
+SI_STACK_AUTO, SI_STACK_PER_LAYER, SI_STACK_PERSISTENT = 0, 1, 2
 
-    def __init__(self, layers, x_in: torch.Tensor, want_ids: bool = True, stream=None):
+
+class StackGraph:
+    """n_layers x n_tokens decode captured as one CUDA graph (buffers owned here).
+
+    mode: SI_STACK_AUTO (the persistent kernel when it supports the layers),
+    SI_STACK_PER_LAYER or SI_STACK_PERSISTENT."""
+
+    def __init__(self, layers, x_in: torch.Tensor, want_ids: bool = True, stream=None,
+                 mode: int = SI_STACK_AUTO):
         self.layers = list(layers)
         arr = (SiMoeLayer * len(self.layers))(*[l.c for l in self.layers])
         self._arr = arr
@@ -320,12 +331,13 @@ class StackGraph:
         h = _vp()
         cap = torch.cuda.Stream(device=dev)
         cap.wait_stream(torch.cuda.current_stream())
-        _check(library().si_moe_stack_graph_create(
+        _check(library().si_moe_stack_graph_create_mode(
             arr, len(self.layers), T, _cuda(x_in, "x_in"), _cuda(self.y, "y"),
             _cuda(self.sum, "sum"), _opt(self.ids, "ids"), _cuda(self.ws, "ws"), self.ws.numel(),
-            _stream(cap), ctypes.byref(h)), "si_moe_stack_graph_create")
+            mode, _stream(cap), ctypes.byref(h)), "si_moe_stack_graph_create_mode")
         self.handle = h
         self.stream = stream
+        self.persistent = bool(library().si_graph_is_persistent(h))
 
     def launch(self, stream=None):
         _check(library().si_graph_launch(self.handle, _stream(stream)), "si_graph_launch")

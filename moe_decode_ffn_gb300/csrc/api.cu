@@ -141,6 +141,7 @@ extern "C" si_status si_test_wait_timeout(uint64_t budget_ns, void *workspace, v
 struct si_graph {
   cudaGraph_t graph;
   cudaGraphExec_t exec;
+  int persistent;   // 1: one persistent kernel; 0: four kernels per layer and token
 };
 
 extern "C" const char *si_status_string(int status) {
@@ -213,12 +214,13 @@ extern "C" size_t si_moe_stack_workspace_bytes(const si_moe_layer *layers, int n
   return off;
 }
 
-extern "C" si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n_layers,
-                                               int n_tokens, const void *x_in, void *y_out,
-                                               void *sum_out, int32_t *ids_out, void *workspace,
-                                               size_t workspace_bytes, void *stream,
-                                               si_graph **graph_out) {
-  if (!layers || n_layers < 1 || n_tokens < 1 || !x_in || !y_out || !graph_out)
+extern "C" si_status si_moe_stack_graph_create_mode(const si_moe_layer *layers, int n_layers,
+                                                    int n_tokens, const void *x_in, void *y_out,
+                                                    void *sum_out, int32_t *ids_out, void *workspace,
+                                                    size_t workspace_bytes, int mode, void *stream,
+                                                    si_graph **graph_out) {
+  if (!layers || n_layers < 1 || n_tokens < 1 || !x_in || !y_out || !graph_out ||
+      (mode != SI_STACK_AUTO && mode != SI_STACK_PER_LAYER && mode != SI_STACK_PERSISTENT))
     return SI_ERR_INVALID_ARG;
   *graph_out = nullptr;
   const int H = layers[0].hidden, k = layers[0].top_k;
@@ -242,7 +244,9 @@ extern "C" si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n
   if (cs != cudaStreamCaptureStatusNone) return SI_ERR_INVALID_ARG;
   // The persistent kernel serves stacks of Q4_K layers; other layer types run
   // as four kernels per layer.
-  const bool persistent = stack_supported(layers, n_layers);
+  const bool can_persist = stack_supported(layers, n_layers);
+  if (mode == SI_STACK_PERSISTENT && !can_persist) return SI_ERR_UNSUPPORTED;
+  const bool persistent = can_persist && mode != SI_STACK_PER_LAYER;
   if (persistent) {
     const si_status sp = stack_prepare(layers, n_layers, workspace, s);
     if (sp != SI_OK) return sp;
@@ -288,7 +292,7 @@ extern "C" si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n
     cudaGraphDestroy(graph);
     return SI_ERR_CUDA;
   }
-  si_graph *g = new (std::nothrow) si_graph{graph, exec};
+  si_graph *g = new (std::nothrow) si_graph{graph, exec, persistent ? 1 : 0};
   if (!g) {
     cudaGraphExecDestroy(exec);
     cudaGraphDestroy(graph);
@@ -296,6 +300,20 @@ extern "C" si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n
   }
   *graph_out = g;
   return SI_OK;
+}
+
+extern "C" si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n_layers,
+                                               int n_tokens, const void *x_in, void *y_out,
+                                               void *sum_out, int32_t *ids_out, void *workspace,
+                                               size_t workspace_bytes, void *stream,
+                                               si_graph **graph_out) {
+  return si_moe_stack_graph_create_mode(layers, n_layers, n_tokens, x_in, y_out, sum_out, ids_out,
+                                        workspace, workspace_bytes, SI_STACK_AUTO, stream,
+                                        graph_out);
+}
+
+extern "C" int si_graph_is_persistent(const si_graph *graph) {
+  return graph ? graph->persistent : -1;
 }
 
 extern "C" si_status si_graph_launch(si_graph *graph, void *stream) {

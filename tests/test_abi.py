@@ -75,6 +75,10 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert lib.si_moe_ffn_decode(ctypes.byref(L), 1, 16, None, 16, 16, 16, None, 256, 1 << 20,
                                  None) == m.SI_ERR_INVALID_ARG
     assert lib.si_graph_launch(None, None) == m.SI_ERR_INVALID_ARG
+    assert lib.si_graph_is_persistent(None) == -1
+    h = ctypes.c_void_p()
+    assert lib.si_moe_stack_graph_create_mode(ctypes.byref(L), 1, 1, 16, 16, None, None, 256,
+                                              1 << 20, 7, None, ctypes.byref(h)) == m.SI_ERR_INVALID_ARG
 
 
 def test_layer_descriptor_validation(lib):

@@ -123,3 +123,28 @@ def test_stack_graph_equals_eager_layers_and_replays_bit_exact(name):
             xin, res = out["y"], out["sum"]
         assert torch.equal(xin, y1[t]) and torch.equal(res, s1[t])
     g.close()
+
+
+def test_stack_paths_agree_bit_exact_and_report_their_kind():
+    """The same Q4_K stack through the persistent kernel and through four
+    kernels per layer: identical bits; a stack the persistent kernel does not
+    serve is refused when that path is forced."""
+    spec = gen.Q4K_LAYER_SHARED_Q4_K
+    layers = _stack_layers(spec, 3, seed=310)
+    x = gen.make_tokens(910, 2).cuda()
+    gp = m.StackGraph(layers, x, mode=m.SI_STACK_PERSISTENT)
+    gl = m.StackGraph(layers, x, mode=m.SI_STACK_PER_LAYER)
+    ga = m.StackGraph(layers, x)
+    assert gp.persistent and not gl.persistent and ga.persistent
+    for g in (gp, gl):
+        g.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(gp.y, gl.y) and torch.equal(gp.sum, gl.sum) and torch.equal(gp.ids, gl.ids)
+    for g in (gp, gl, ga):
+        assert m.si_workspace_status(g.ws) == m.SI_OK
+        g.close()
+    q8 = _stack_layers(gen.Q4K_LAYER_SHARED_Q8_0, 2, seed=311)
+    with pytest.raises(m.SiError) as e:
+        m.StackGraph(q8, x, mode=m.SI_STACK_PERSISTENT)
+    assert e.value.status == m.SI_ERR_UNSUPPORTED
+    assert not m.StackGraph(q8, x).persistent

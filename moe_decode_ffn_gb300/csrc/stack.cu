@@ -49,6 +49,7 @@ SI_TRACE_BUFFER
 constexpr int kStkThreads = 512;
 constexpr int kSlot = 16;           // u64 elements per 128-byte slot
 constexpr int kStkFixedBytes = 2048;
+constexpr int kArmT = 480;          // the thread that arms every barrier (warp 15, lane 0)
 
 struct StackLayerPtrs {             // 80 bytes
   const __nv_bfloat16 *w_router, *w_sg, *w_norm;
@@ -196,9 +197,9 @@ SI_DEV float sigma_dot(const __nv_bfloat16 *w, const float *y, int n, float *red
 // ---- copies ---------------------------------------------------------------------
 // Issuing one bulk copy occupies the issuing thread for a few hundred cycles
 // whatever its size, so copies are few and large, and are issued one per
-// warp (lane 0) by warps that have nothing else to do at that moment. Thread
-// 0 arms every barrier (arrive + expected bytes) before a __syncthreads that
-// precedes the copies.
+// warp (lane 0) by warps that have nothing else to do at that moment. One
+// thread (kArmT) arms every barrier (arrive + expected bytes) before a
+// __syncthreads that precedes the copies.
 SI_DEV void arm(uint64_t *bars, int b, uint32_t bytes, uint32_t &armed, uint32_t &used) {
   mbar_arrive_expect_tx(&bars[b], bytes);
   armed ^= 1u << b;
@@ -387,14 +388,15 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   __syncthreads();
   const uint32_t base = *s_base;
 
-  // Thread 0: `armed` holds, per barrier, the parity of the number of phases
-  // armed so far, `used` which barriers were ever armed. On an error exit it
-  // waits for the last armed phase of each, so no copy is left in flight.
+  // Thread kArmT: `armed` holds, per barrier, the parity of the number of
+  // phases armed so far, `used` which barriers were ever armed. On an error
+  // exit it waits for the last armed phase of each, so no copy is left in
+  // flight.
   uint32_t armed = 0u, used = 0u;
   int t = 0, l = 0;   // token and layer of iteration it
   const uint32_t gbytes = static_cast<uint32_t>((nrr + (kShared ? 1 : 0) + 1) * H * 2);
   const uint32_t gubytes = 8u * p.rb;    // one group: 8 gate (or up) rows
-  if (threadIdx.x == 0 && n_iters > 0) {
+  if (threadIdx.x == kArmT && n_iters > 0) {
     // iteration 0's routing-independent bytes and shared gate/up unit
     const StackLayerPtrs &L0 = s_layers[0];
     arm(bars, 0, gbytes, armed, used);
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   for (int it = 0;; ++it) {
     const uint32_t tag = base + static_cast<uint32_t>(it) + 1u, par = it & 1u;
     SI_TRACE_MARK(0, 0);
-    if (threadIdx.x == 0 && it < n_iters) {   // copies issued during this iteration's logit gather
+    if (threadIdx.x == kArmT && it < n_iters) {   // copies issued during this iteration's logit gather
       if (it + 1 < n_iters) arm(bars, (it + 1) & 1, gbytes, armed, used);
       if (kShared && nrows > 0) arm(bars, 7, static_cast<uint32_t>(nrows) * p.rbsd, armed, used);
     }
@@ -450,7 +452,6 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       __syncthreads();
     }
     SI_TRACE_MARK(0, 1);
-    quantize_y(y, H, xt);   // ends with __syncthreads
 
     // [R] router rows: W warps per row, vector (i * W + wpart) * 32 + lane
     {
@@ -493,6 +494,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
                 tagged(tag, __float_as_uint(lg[1])));
       }
     }
+    // the gate/up activations, while the logits travel
+    quantize_y(y, H, xt);   // ends with __syncthreads
     SI_TRACE_MARK(0, 2);
 
     // [S] gather every logit; top-k + softmax in every block
@@ -509,7 +512,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
           s_logit[threadIdx.x + G] = __uint_as_float(static_cast<uint32_t>(b));
       } else if (lane == 0) {
         // warps without a slot to poll: the next iteration's router rows,
-        // shared-gate vector and norm weights; this iteration's shared down rows
+        // shared-gate vector and norm weights; this iteration's shared down
+        // rows; and the arming of this iteration's routed copies
+        if (threadIdx.x == kArmT) {
+          if (my_unit >= 0 && !shared_unit)
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) arm(bars, 2 + g, 2 * gubytes, armed, used);
+          if (nrows > 0) arm(bars, 6, static_cast<uint32_t>(k * nrows * p.rbd), armed, used);
+        }
         const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];
         uint8_t *dst = pbuf + ((it + 1) & 1) * pstr;
         uint64_t *bar = &bars[(it + 1) & 1];
@@ -533,12 +543,6 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       if (lane < 8) s_cand[warp * 8 + lane] = key;
     }
     SI_TRACE_MARK(0, 9);
-    if (threadIdx.x == 0) {
-      if (my_unit >= 0 && !shared_unit)
-#pragma unroll 1
-        for (int g = 0; g < 4; ++g) arm(bars, 2 + g, 2 * gubytes, armed, used);
-      if (nrows > 0) arm(bars, 6, static_cast<uint32_t>(k * nrows * p.rbd), armed, used);
-    }
     __syncthreads();
     {
       // rank of candidate tid / 8 among the 64: 8 threads compare 8 each
@@ -556,7 +560,9 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     SI_TRACE_MARK(0, 10);
     // routed bytes, one copy per warp: warps 0..7 this block's gate/up unit
     // (warp w: group w & 3 of the gate (w < 4) or up rows, 8 rows each),
-    // warps 8 .. 8 + k - 1 its down rows of each selected expert
+    // warps 8 .. 8 + k - 1 its down rows of each selected expert; a block with
+    // a gate/up unit issues the down rows only once its own gate/up rows have
+    // arrived, so that they do not compete with the more urgent bytes
     if (lane == 0) {
       const StackLayerPtrs &Lp = s_layers[l];
       if (warp < 8 && my_unit >= 0 && !shared_unit) {
@@ -567,7 +573,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         bulk_g2s_evict_first(gu_buf + warp * gubytes, (warp < 4 ? Lp.wg : Lp.wu) + row0 * p.rb,
                              gubytes, &bars[2 + (warp & 3)], pol);
       }
-      if (warp >= 8 && warp < 8 + k && nrows > 0) {
+      if (warp >= 8 && warp < 8 + k && nrows > 0 && my_unit < 0) {
         int e = key_index(s_sel[warp - 8]);
         if (e < 0 || e >= E) e = 0;
         bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
@@ -581,6 +587,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     if (my_unit >= 0) {
       float acc = 0.f;
       const bool ok = mbar_wait_bounded(&bars[2 + (pr >> 3)], par, p.status);
+      if (lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {   // deferred down rows
+        const StackLayerPtrs &Lp = s_layers[l];
+        int e = key_index(s_sel[warp - 8]);
+        if (e < 0 || e >= E) e = 0;
+        bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
+                             Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
+                             static_cast<uint32_t>(nrows) * p.rbd, &bars[6], pol);
+      }
       if (ok) {
         const uint8_t *row = gu_buf + (gm * 32 + pr) * p.rb;
         for (int sb = lane8; sb < nsb; sb += 8)
@@ -593,7 +607,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
       const float other = __shfl_xor_sync(0xffffffffu, acc, 8);
       if ((threadIdx.x & 15) == 0) h_s[pr] = __fdiv_rn(acc, 1.f + expf(-acc)) * other;
-      if (threadIdx.x == 0 && shared_unit && it + 1 < n_iters)
+      if (threadIdx.x == kArmT && shared_unit && it + 1 < n_iters)
 #pragma unroll 1
         for (int g = 0; g < 4; ++g) arm(bars, 2 + g, 2 * gubytes, armed, used);
       if (__syncthreads_or(!ok)) goto fail;
@@ -717,7 +731,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   }
   goto finish;
 fail:
-  if (threadIdx.x == 0)
+  if (threadIdx.x == kArmT)
 #pragma unroll 1
     for (int b = 0; b < 8; ++b)
       if ((used >> b) & 1u) mbar_wait_bounded(&bars[b], ((armed >> b) & 1u) ^ 1u, p.status);

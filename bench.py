@@ -357,6 +357,133 @@ def run_gpu(args):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# --configs: one line per workload configuration (not the headline line)
+# ----------------------------------------------------------------------------
+BYTES_CFG1 = 256 * 2048 * 2 + 8 * 3 * 512 * 2048 * 2 + 3 * 512 * 2048 * 2 + 2048 * 2  # 57,675,776
+Q80_MATRIX = 512 * 2048 // 32 * 34                                                   # 1,114,112
+BYTES_CFG3_Q80 = BYTES_ROUTER + BYTES_ROUTED + 3 * Q80_MATRIX + BYTES_SIGMOID         # 18,550,784
+Q4K_EXPERT_128E = 3 * (768 * 2048 // 256 * 144)                                       # 2,654,208
+
+
+def _time_replays(fn, stream, warm=3, reps=10):
+    """Device time per call of fn() (which enqueues on `stream`), by CUDA events."""
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def run_configs(args):
+    import torch
+
+    import gen
+    import moe_decode_ffn_gb300 as m
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    m.build()
+    lib = m.library()
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.Stream(device=dev)
+    out = []
+
+    def emit(cfg, what, us, unit, nbytes=None, **extra):
+        line = {"config": cfg, "what": what, "value": round(us, 3), "unit": unit}
+        if nbytes is not None:
+            gbs = nbytes / (us * 1e-6) / 1e9
+            line.update({"bytes": nbytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                         "peak_gbs": peak, "peak_kind": peak_kind})
+        line.update(extra)
+        out.append(line)
+        print(json.dumps(line), flush=True)
+
+    # configs 1 and 3: 8 distinct layers x 16 tokens per replay, so every
+    # layer-token reads its weights from HBM (8 layers exceed the L2)
+    NL, NT = 8, 16
+    x = gen.make_tokens(SEED + 7, NT, device=dev)
+    for cfg, spec, nbytes in (("1: bf16 layer", gen.BF16_LAYER, BYTES_CFG1),
+                              ("3: Q4_K layer, Q8_0 shared", gen.Q4K_LAYER_SHARED_Q8_0, BYTES_CFG3_Q80),
+                              ("3: Q4_K layer, Q4_K shared", gen.Q4K_LAYER_SHARED_Q4_K, BYTES_LAYER_TOKEN)):
+        layers = [m.device_layer(spec, SEED + 100, l, device=dev) for l in range(NL)]
+        modes = [m.SI_STACK_AUTO]
+        if spec is gen.Q4K_LAYER_SHARED_Q4_K:
+            modes = [m.SI_STACK_PERSISTENT, m.SI_STACK_PER_LAYER]
+        for mode in modes:
+            g = m.StackGraph(layers, x, mode=mode)
+            us = _time_replays(lambda: g.launch(stream), stream) / (NL * NT)
+            st = m.si_workspace_status(g.ws, stream)
+            emit(cfg, "one layer, one token (8 distinct layers x 16 tokens per graph)", us,
+                 "us/layer/token", nbytes,
+                 path="persistent kernel" if g.persistent else "four kernels per layer",
+                 device_status=m.status_string(st))
+            g.close()
+        del layers
+        torch.cuda.empty_cache()
+
+    # config 2: router + top-k on fp32 tie-stress inputs (E = 256 and 128), one
+    # token per call, 64 calls per graph over 8 router matrices
+    for E in (256, 128):
+        mats = [gen.tie_stress_group(SEED, g, E, 8, device=dev) for g in range(8)]
+        ws = m.workspace(m.router_workspace_bytes(E, 2048, 1), dev)
+        ids = torch.empty(1, 8, dtype=torch.int32, device=dev)
+        wts = torch.empty(1, 8, dtype=torch.float32, device=dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for W, X, _ in mats:
+                for c in range(8):
+                    st = lib.si_moe_router_topk(X[c].data_ptr(), m.SI_F32, W.data_ptr(), m.SI_F32, 2048,
+                                                E, 8, 1, ids.data_ptr(), wts.data_ptr(), None,
+                                                ws.data_ptr(), ws.numel(), stream.cuda_stream)
+                    assert st == 0
+        us = _time_replays(graph.replay, stream) / 64
+        emit(f"2: router tie stress, E={E}", "fused router GEMV + top-8 + softmax, fp32, 1 token",
+             us, "us/call", E * 2048 * 4,
+             note="8 distinct router matrices (16 MB at E=256) rotate, L2-resident")
+        del graph
+
+    # config 5: 128 experts, I=768, no shared, Q4_K; batched FFN (gate/up + down
+    # + combine) for T tokens with per-token routing; 8 distinct layers per graph
+    spec = gen.Q4K_LAYER_128E
+    layers = [m.device_layer(spec, SEED + 200, l, device=dev) for l in range(8)]
+    for T in (1, 4, 16, 64):
+        xs = gen.make_tokens(SEED + 300 + T, T, device=dev)
+        routs = []
+        for l in range(8):
+            keys = gen.raw64([gen.stream_key(SEED + l, t, 901) for t in range(T)], 128)
+            ids = torch.argsort(keys, dim=1)[:, :8].to(torch.int32).to(dev)
+            w = torch.full((T, 8), 0.125, dtype=torch.float32, device=dev)
+            routs.append((ids, w))
+        U = sum(int(torch.unique(r[0]).numel()) for r in routs) / 8
+        for mode, name in ((m.SI_FFN_INT8, "int8 dp4a GEMV"), (m.SI_FFN_TENSOR, "tcgen05 fp16 MMA")):
+            if mode == m.SI_FFN_TENSOR and T < 16:
+                continue
+            wss = [m.workspace(m.ffn_batched_workspace_bytes(L, T), dev) for L in layers]
+            outs = [torch.empty(T, 2048, dtype=torch.bfloat16, device=dev) for _ in layers]
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for L, (ids, w), ws, o in zip(layers, routs, wss, outs):
+                    st = lib.si_moe_ffn_batched(L.ref, T, mode, xs.data_ptr(), ids.data_ptr(),
+                                                w.data_ptr(), o.data_ptr(), ws.data_ptr(), ws.numel(),
+                                                stream.cuda_stream)
+                    assert st == 0
+            us = _time_replays(graph.replay, stream) / 8
+            st = max(m.si_workspace_status(ws, stream) for ws in wss)
+            emit(f"5: 128 experts, I=768, T={T}", f"batched routed FFN, {name}", us, "us/layer",
+                 round(U * Q4K_EXPERT_128E), distinct_experts=U, us_per_layer_token=round(us / T, 3),
+                 device_status=m.status_string(st))
+            del graph
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -367,11 +494,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-layer-path", action="store_true",
                     help="skip timing the four-kernels-per-layer path")
+    ap.add_argument("--configs", action="store_true",
+                    help="instead of the headline line, one line per workload configuration")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.configs:
+        return run_configs(args)
     return run_gpu(args)
 
 

@@ -202,7 +202,11 @@ si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, const void *x,
  * The (token, rank) pairs are grouped by expert so that each selected
  * expert's rows are read once for all of its tokens; routed[t] =
  * sum_r topk_w[t][r] * y_{t,r} in rank order, stored as bf16.
- *   mode       SI_FFN_AUTO (0): SI_FFN_INT8 below 16 tokens, SI_FFN_TENSOR from 16;
+ *   mode       SI_FFN_AUTO (0): SI_FFN_INT8, the faster mode at every supported
+ *                               batch on GB300 (with 128 experts a batch of
+ *                               64 tokens gives each selected expert ~4 tokens:
+ *                               not dense enough to pay for dequantising the
+ *                               weights for the tensor cores);
  *              SI_FFN_INT8 (1): Q8_1 activations, exact int32 block dots, as
  *                               si_moe_ffn_decode (n_tokens = 1 gives its bits);
  *              SI_FFN_TENSOR (2): tcgen05 tensor cores, fp16 operands: weights
@@ -323,6 +327,12 @@ si_status si_moe_ffn_gateup(const si_moe_layer *L, int n_tokens, const void *x,
  * budget_ns (<= 2 s) and writes SI_ERR_TIMEOUT to the workspace status word,
  * as every bounded wait of the library does. For testing that path. */
 si_status si_test_wait_timeout(uint64_t budget_ns, void *workspace, void *stream);
+
+/* The tagged-slot poll of the persistent stack kernel on a slot that never
+ * receives the awaited tag: it gives up after budget_ns (<= 2 s) and writes
+ * SI_ERR_TIMEOUT to the status word. workspace: 512 bytes, zero-filled (the
+ * slot is the 16 bytes after the 256-byte status header). */
+si_status si_test_poll_timeout(uint64_t budget_ns, void *workspace, void *stream);
 
 /* D = A * B^T for one 128 x n x k block on the tensor cores (A fp16 [128][k],
  * B fp16 [n][k] row-major; n in {16..64} step 16, k in {16..256} step 16;

@@ -77,6 +77,7 @@ SIGNATURES = {
     "si_moe_ffn_gateup": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "si_test_q4k_block_dots": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp]),
     "si_test_wait_timeout": (_i32, [ctypes.c_uint64, _vp, _vp]),
+    "si_test_poll_timeout": (_i32, [ctypes.c_uint64, _vp, _vp]),
     "si_test_umma_f16": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp]),
     "si_test_unfused_add_rmsnorm": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
                                            _vp]),

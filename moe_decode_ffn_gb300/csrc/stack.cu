@@ -106,7 +106,8 @@ SI_DEV bool pair_ok(uint64_t a, uint64_t b, uint32_t tag) { return tag_ok(a, tag
 // Re-read the pair at p until both elements carry `tag`, at most
 // kWaitBudgetNs; records SI_ERR_TIMEOUT and returns false if they never do.
 static __device__ __noinline__ bool poll_pair(const uint64_t *p, uint32_t tag, uint64_t &a,
-                                              uint64_t &b, uint32_t *status) {
+                                              uint64_t &b, uint32_t *status,
+                                              uint64_t budget_ns = kWaitBudgetNs) {
   const uint64_t t0 = now_ns();
   for (;;) {
 #pragma unroll 1
@@ -114,7 +115,7 @@ static __device__ __noinline__ bool poll_pair(const uint64_t *p, uint32_t tag, u
       ld_tag2(p, a, b);
       if (pair_ok(a, b, tag)) return true;
     }
-    if (now_ns() - t0 > kWaitBudgetNs) {
+    if (now_ns() - t0 > budget_ns) {
       record_status(status, SI_ERR_TIMEOUT);
       return false;
     }
@@ -927,7 +928,26 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, p));
 }
 
+// Test only: one thread polls a pair that never carries the awaited tag.
+__global__ void poll_timeout_kernel(const uint64_t *line, uint64_t budget_ns, uint32_t *status) {
+  if (threadIdx.x == 0) {
+    uint64_t a, b;
+    ld_tag2(line, a, b);
+    if (!pair_ok(a, b, 0xFFFFFFFFu)) poll_pair(line, 0xFFFFFFFFu, a, b, status, budget_ns);
+  }
+}
+
 }  // namespace si
+
+extern "C" si_status si_test_poll_timeout(uint64_t budget_ns, void *workspace, void *stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || budget_ns > 2000000000ull)
+    return SI_ERR_INVALID_ARG;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  si::poll_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint64_t *>(ws + sizeof(si::WsHeader)), budget_ns,
+      reinterpret_cast<uint32_t *>(ws));
+  return si::cuda_status(cudaGetLastError());
+}
 
 #ifdef SI_TRACE
 extern "C" int si_trace_dump_stack(void *dst) {

@@ -4,6 +4,11 @@ expert), n_tokens tokens through n_layers layers captured as one CUDA graph
 and replayed `launches` times, then the workspace status is checked.
 
     python -m moe_decode_ffn_gb300.profile_case --layers 4 --tokens 8 --launches 3 [--per-layer]
+    python -m moe_decode_ffn_gb300.profile_case --batched 64 --mode tensor --launches 3
+
+The second form runs the batched routed FFN of one Qwen3-30B-A3B-shaped layer
+(128 experts, I=768, no shared expert, Q4_K) for T tokens with per-token
+routing, in the integer (int8) or tensor-core (tensor) mode.
 
 It exits non-zero if the device recorded an error, so a profiler is only ever
 run on a command that has just exited 0 on its own.
@@ -22,6 +27,8 @@ def main(argv=None) -> int:
     ap.add_argument("--seed", type=int, default=21)
     ap.add_argument("--per-layer", action="store_true", help="four kernels per layer instead of "
                     "the persistent kernel")
+    ap.add_argument("--batched", type=int, default=0, help="T: batched FFN of T tokens instead")
+    ap.add_argument("--mode", default="tensor", choices=["tensor", "int8"])
     args = ap.parse_args(argv)
 
     import torch
@@ -30,6 +37,21 @@ def main(argv=None) -> int:
     import moe_decode_ffn_gb300 as m
 
     m.build()
+    if args.batched:
+        T = args.batched
+        L = m.device_layer(gen.Q4K_LAYER_128E, args.seed, 0)
+        x = gen.make_tokens(args.seed + 1, T, device="cuda")
+        keys = gen.raw64([gen.stream_key(args.seed, t, 901) for t in range(T)], 128)
+        ids = torch.argsort(keys, dim=1)[:, :8].to(torch.int32).cuda()
+        w = torch.full((T, 8), 0.125, dtype=torch.float32, device="cuda")
+        mode = m.SI_FFN_TENSOR if args.mode == "tensor" else m.SI_FFN_INT8
+        ws = m.workspace(m.ffn_batched_workspace_bytes(L, T))
+        for _ in range(args.launches):
+            m.si_moe_ffn_batched(L, x, ids, w, mode, ws=ws)
+        torch.cuda.synchronize()
+        st = m.si_workspace_status(ws)
+        print(f"batched T={T} mode={args.mode} launches={args.launches} status={m.status_string(st)}")
+        return 0 if st == m.SI_OK else 1
     spec = gen.Q4K_LAYER_SHARED_Q4_K
     layers = [m.device_layer(spec, args.seed, l) for l in range(args.layers)]
     x = gen.make_tokens(args.seed + 1, args.tokens, device="cuda")

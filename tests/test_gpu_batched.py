@@ -159,10 +159,10 @@ def test_batched_tensor_tokens_sharing_experts():
     check_tokens_fp16(routed.cpu(), x, ids, w, [0, 21, 39])
 
 
-def test_batched_auto_mode_switches_at_16_tokens():
+def test_batched_auto_mode_is_the_integer_path():
     dev = device_layer(SPEC, SEED, 0)
     ids, w = routing(9, 16)
     x = gen.make_tokens(952, 16).cuda()
     auto = m.si_moe_ffn_batched(dev, x, ids.cuda(), w.cuda(), m.SI_FFN_AUTO)
-    tensor = m.si_moe_ffn_batched(dev, x, ids.cuda(), w.cuda(), m.SI_FFN_TENSOR)
-    assert torch.equal(auto, tensor)
+    int8 = m.si_moe_ffn_batched(dev, x, ids.cuda(), w.cuda(), m.SI_FFN_INT8)
+    assert torch.equal(auto, int8)

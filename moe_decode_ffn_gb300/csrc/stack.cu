@@ -562,8 +562,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     // routed bytes, one copy per warp: warps 0..7 this block's gate/up unit
     // (warp w: group w & 3 of the gate (w < 4) or up rows, 8 rows each),
     // warps 8 .. 8 + k - 1 its down rows of each selected expert; a block with
-    // a gate/up unit issues the down rows only once its own gate/up rows have
-    // arrived, so that they do not compete with the more urgent bytes
+    // a gate/up unit issues the down rows only once it has consumed its own
+    // gate/up rows, so that they do not compete with the more urgent bytes
     if (lane == 0) {
       const StackLayerPtrs &Lp = s_layers[l];
       if (warp < 8 && my_unit >= 0 && !shared_unit) {
@@ -588,14 +588,6 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     if (my_unit >= 0) {
       float acc = 0.f;
       const bool ok = mbar_wait_bounded(&bars[2 + (pr >> 3)], par, p.status);
-      if (lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {   // deferred down rows
-        const StackLayerPtrs &Lp = s_layers[l];
-        int e = key_index(s_sel[warp - 8]);
-        if (e < 0 || e >= E) e = 0;
-        bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
-                             Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
-                             static_cast<uint32_t>(nrows) * p.rbd, &bars[6], pol);
-      }
       if (ok) {
         const uint8_t *row = gu_buf + (gm * 32 + pr) * p.rb;
         for (int sb = lane8; sb < nsb; sb += 8)
@@ -612,6 +604,16 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
 #pragma unroll 1
         for (int g = 0; g < 4; ++g) arm(bars, 2 + g, 2 * gubytes, armed, used);
       if (__syncthreads_or(!ok)) goto fail;
+      if (lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {
+        // the down rows, now that this block's gate/up rows are in: they are
+        // needed only after the h exchange
+        const StackLayerPtrs &Lp = s_layers[l];
+        int e = key_index(s_sel[warp - 8]);
+        if (e < 0 || e >= E) e = 0;
+        bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
+                             Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
+                             static_cast<uint32_t>(nrows) * p.rbd, &bars[6], pol);
+      }
       if (lane == 0 && warp >= 8 && shared_unit && it + 1 < n_iters) {
         // the next iteration's shared gate/up unit (warps 8..15, one group each)
         const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];

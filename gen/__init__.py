@@ -55,6 +55,7 @@ NORM_MEAN, NORM_STD = 1.0, 0.1
 
 QK_K = 256          # weights per Q4_K super-block
 Q4_K_BYTES = 144    # bytes per Q4_K super-block
+Q5_K_BYTES = 176    # bytes per Q5_K super-block
 QK8 = 32            # weights per Q8_0 / Q8_1 block
 Q8_0_BYTES = 34
 Q8_1_BYTES = 36
@@ -222,9 +223,60 @@ def encode_q4_k(w: torch.Tensor) -> torch.Tensor:
     return pack_q4_k(*q4_k_params(w))
 
 
+def q5_k_params(w: torch.Tensor):
+    """The min/max quantiser of q4_k_params with 5-bit codes: s_j = (hi - lo)/31,
+    q clamped to [0, 31]; the rest (fp16 d/dmin from the largest s/m' over 63,
+    6-bit sc/m by rint) as there. Returns (d16, dmin16, sc, m, q)."""
+    rows, k = w.shape
+    assert k % QK_K == 0
+    nsb = k // QK_K
+    x = w.reshape(rows, nsb, 8, 32)
+    lo = torch.clamp(x.amin(-1), max=0.0)
+    hi = x.amax(-1)
+    s = _div(hi - lo, 31.0)
+    mneg = -lo
+    d16 = _div(s.amax(-1), 63.0).to(torch.float16)
+    dmin16 = _div(mneg.amax(-1), 63.0).to(torch.float16)
+    df = d16.to(torch.float32)[..., None]
+    dmf = dmin16.to(torch.float32)[..., None]
+    one = torch.ones_like(df)
+    sc = torch.where(df > 0, torch.round(s / torch.where(df > 0, df, one)).clamp(0, 63),
+                     torch.zeros_like(s))
+    m = torch.where(dmf > 0, torch.round(mneg / torch.where(dmf > 0, dmf, one)).clamp(0, 63),
+                    torch.zeros_like(s))
+    den = (df * sc)[..., None]
+    num = x + (dmf * m)[..., None]
+    q = torch.where(den > 0, torch.round(num / torch.where(den > 0, den, torch.ones_like(den)))
+                    .clamp(0, 31), torch.zeros_like(num))
+    return d16, dmin16, sc.to(torch.int64), m.to(torch.int64), q.to(torch.int64)
+
+
+def pack_q5_k(d16, dmin16, sc, m, q) -> torch.Tensor:
+    """Q5_K super-blocks, GGUF layout, 176 bytes: the Q4_K header (d, dmin,
+    12 scale bytes), then qh[32] with bit j of byte i = bit 4 of element i of
+    sub-block j, then the low 4 bits of the codes in Q4_K's code layout."""
+    rows, nsb = d16.shape
+    q4 = pack_q4_k(d16, dmin16, sc, m, q & 15).reshape(rows, nsb, Q4_K_BYTES)
+    hi = (q >> 4) & 1                                            # [rows, nsb, 8, 32]
+    weights = (1 << torch.arange(8, device=q.device, dtype=torch.int64)).reshape(1, 1, 8, 1)
+    qh = (hi * weights).sum(dim=2)                               # [rows, nsb, 32]
+    out = torch.empty(rows, nsb, Q5_K_BYTES, dtype=torch.uint8, device=d16.device)
+    out[..., 0:16] = q4[..., 0:16]
+    out[..., 16:48] = qh.to(torch.uint8)
+    out[..., 48:176] = q4[..., 16:144]
+    return out.reshape(rows, nsb * Q5_K_BYTES)
+
+
+def encode_q5_k(w: torch.Tensor) -> torch.Tensor:
+    """fp32 [rows, K] -> uint8 [rows, K/256*176] Q5_K super-blocks."""
+    return pack_q5_k(*q5_k_params(w))
+
+
 def row_bytes(fmt: str, k: int) -> int:
     if fmt == "q4_k":
         return k // QK_K * Q4_K_BYTES
+    if fmt == "q5_k":
+        return k // QK_K * Q5_K_BYTES
     if fmt == "q8_0":
         return k // QK8 * Q8_0_BYTES
     if fmt == "bf16":
@@ -237,6 +289,8 @@ def encode(w32: torch.Tensor, fmt: str) -> torch.Tensor:
     tensor [rows, row_bytes(fmt, K)] (bf16 is its little-endian bytes)."""
     if fmt == "q4_k":
         return encode_q4_k(w32)
+    if fmt == "q5_k":
+        return encode_q5_k(w32)
     if fmt == "q8_0":
         return encode_q8_0(w32)
     if fmt == "bf16":
@@ -259,6 +313,7 @@ class LayerSpec:
     shared_inter: int = 512       # 0: no shared expert
     shared_type: str = "q8_0"     # "q8_0" | "q4_k" | "bf16"
     eps: float = 1e-6
+    down_type: str = ""           # routed down format; "" = expert_type ("q5_k": Q4_K gate/up)
 
 
 # One layer, one token, bf16 everywhere, shared expert I=512.
@@ -268,6 +323,9 @@ Q4K_LAYER_SHARED_Q8_0 = LayerSpec(expert_type="q4_k", shared_type="q8_0")
 Q4K_LAYER_SHARED_Q4_K = LayerSpec(expert_type="q4_k", shared_type="q4_k")
 # Qwen3-30B-A3B-shaped layer: 128 experts, I=768, no shared expert.
 Q4K_LAYER_128E = LayerSpec(n_experts=128, inter=768, shared_inter=0, shared_type="q4_k")
+# The shipped Qwen3.6-35B-A3B formats before the load-time requant: routed
+# gate/up Q4_K, routed down Q5_K, shared expert Q8_0.
+NATIVE_LAYER_Q5K_DOWN = LayerSpec(expert_type="q4_k", down_type="q5_k", shared_type="q8_0")
 
 
 def _weights(seed, layer, role, experts, rows, cols, fmt, device, std=WEIGHT_STD, mean=0.0,
@@ -310,7 +368,8 @@ def make_layer(spec: LayerSpec, seed: int, layer: int = 0, device="cpu", experts
                             ).reshape(spec.n_experts, H),
         "gate": _weights(seed, layer, ROLE_GATE, ids, I, H, spec.expert_type, device),
         "up": _weights(seed, layer, ROLE_UP, ids, I, H, spec.expert_type, device),
-        "down": _weights(seed, layer, ROLE_DOWN, ids, H, I, spec.expert_type, device),
+        "down": _weights(seed, layer, ROLE_DOWN, ids, H, I, spec.down_type or spec.expert_type,
+                         device),
         "w_norm": to_bf16(normal([stream_key(seed, layer, ROLE_NORM, 0)], H, NORM_MEAN,
                                  NORM_STD, device)).reshape(H),
     }

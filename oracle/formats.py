@@ -6,6 +6,13 @@ CUDA path.
 
 Sources (sparkinfer pull-request pages):
 * "Q4_K shared-expert FFN kernels + Q8_0/Q5_K->Q4_K requant of the MoE FFN
+  stage" (PR #359), Summary, bullets 1 and 2: the routed down projection ships
+  as Q5_K and the shared expert as Q8_0; both are requantised to Q4_K once at
+  load. The page names the formats but prints neither the Q5_K layout nor the
+  requant procedure: the GGUF Q5_K layout is taken, and the requant is read as
+  "dequantise to fp32, then quantise to Q4_K with the library's Q4_K
+  quantiser" (min/max per 32-wide sub-block; see q4_k_quantize).
+* "Q4_K shared-expert FFN kernels + Q8_0/Q5_K->Q4_K requant of the MoE FFN
   stage" (PR #359), Summary: Q8_0 is 34 bytes per 32-weight block; Q4_K cuts
   about 47% of the bytes; activations are quantised to Q8_1 ("FNQ Q8_1",
   "quant_h Q8_1") and dotted with int8 dp4a.
@@ -20,6 +27,7 @@ import numpy as np
 
 QK_K = 256
 Q4_K_BYTES = 144
+Q5_K_BYTES = 176
 QK8 = 32
 Q8_0_BYTES = 34
 Q8_1_BYTES = 36
@@ -119,6 +127,91 @@ def q4_k_rows(mat) -> np.ndarray:
     """[rows, nsb*144] uint8 -> [rows, nsb, 144]."""
     mat = np.asarray(mat, dtype=np.uint8)
     return mat.reshape(mat.shape[0], -1, Q4_K_BYTES)
+
+
+def q4_k_pack(d, dmin, sc, m, q) -> np.ndarray:
+    """Inverse of q4_k_fields: d, dmin exact fp16 values [...], sc, m ints in
+    [0, 63] [..., 8], q ints in [0, 15] [..., 8, 32] -> uint8 [..., 144]."""
+    d = np.asarray(d, dtype=np.float64)
+    out = np.zeros(d.shape + (Q4_K_BYTES,), dtype=np.uint8)
+    out[..., 0:2] = np.ascontiguousarray(d.astype(np.float16)).view(np.uint8).reshape(d.shape + (2,))
+    dm = np.asarray(dmin, dtype=np.float64)
+    out[..., 2:4] = np.ascontiguousarray(dm.astype(np.float16)).view(np.uint8).reshape(d.shape + (2,))
+    sc = np.asarray(sc, dtype=np.int64)
+    m = np.asarray(m, dtype=np.int64)
+    for j in range(4):
+        out[..., 4 + j] = (sc[..., j] & 63) | ((sc[..., j + 4] >> 4) << 6)
+        out[..., 8 + j] = (m[..., j] & 63) | ((m[..., j + 4] >> 4) << 6)
+        out[..., 12 + j] = (sc[..., j + 4] & 15) | ((m[..., j + 4] & 15) << 4)
+    q = np.asarray(q, dtype=np.int64)
+    for pp in range(4):
+        out[..., 16 + 32 * pp:48 + 32 * pp] = q[..., 2 * pp, :] | (q[..., 2 * pp + 1, :] << 4)
+    return out
+
+
+def q4_k_quantize(w) -> np.ndarray:
+    """The library's Q4_K quantiser, on fp32 weights [rows, K] (K % 256 == 0),
+    every step an IEEE fp32 operation (numpy float32 arithmetic is correctly
+    rounded), rint = round half to even. Per 32-wide sub-block j of a super-block:
+      lo = min(0, min w), hi = max w, s_j = (hi - lo) / 15, m'_j = -lo;
+      d = fp16(max_j s_j / 63), dmin = fp16(max_j m'_j / 63);
+      sc_j = rint(s_j / d) and m_j = rint(m'_j / dmin), clamped to [0, 63],
+      0 where the divisor is 0;
+      q = rint((w + dmin * m_j) / (d * sc_j)) clamped to [0, 15], 0 where the
+      divisor is 0 (d * sc_j and dmin * m_j are exact in fp32).
+    Returns uint8 [rows, K/256*144]."""
+    f = np.float32
+    w = np.asarray(w, dtype=np.float32)
+    rows, k = w.shape
+    nsb = k // QK_K
+    x = w.reshape(rows, nsb, 8, 32)
+    lo = np.minimum(x.min(axis=-1), f(0))
+    hi = x.max(axis=-1)
+    s = (hi - lo) / f(15)
+    mneg = -lo
+    d16 = (s.max(axis=-1) / f(63)).astype(np.float16)
+    dm16 = (mneg.max(axis=-1) / f(63)).astype(np.float16)
+    d = d16.astype(np.float32)[..., None]
+    dm = dm16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        sc = np.where(d > 0, np.clip(np.rint(s / np.where(d > 0, d, f(1))), 0, 63), 0).astype(np.int64)
+        m = np.where(dm > 0, np.clip(np.rint(mneg / np.where(dm > 0, dm, f(1))), 0, 63), 0).astype(np.int64)
+        den = (d * sc.astype(np.float32))[..., None]
+        num = x + (dm * m.astype(np.float32))[..., None]
+        q = np.where(den > 0, np.clip(np.rint(num / np.where(den > 0, den, f(1))), 0, 15), 0)
+    out = q4_k_pack(d16.astype(np.float64), dm16.astype(np.float64), sc, m, q.astype(np.int64))
+    return out.reshape(rows, nsb * Q4_K_BYTES)
+
+
+# ----------------------------------------------------------------------------
+# Q5_K super-block: 176 bytes per 256 weights
+# ----------------------------------------------------------------------------
+
+def q5_k_fields(blocks):
+    """Unpack Q5_K super-blocks [..., 176] (uint8), GGUF layout: bytes 0-1 fp16
+    d, 2-3 fp16 dmin, 4-15 the 6-bit scales and mins packed as in Q4_K, 16-47
+    qh[32] (the fifth bits), 48-175 the low 4 bits of the 256 codes laid out as
+    Q4_K's codes. Element i of sub-block j: q = low nibble as in Q4_K
+    + 16 * bit j of qh[i]. Returns d, dmin, sc, m, q (q in [0, 31])."""
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    as_q4 = np.concatenate([blocks[..., 0:16], blocks[..., 48:176]], axis=-1)
+    d, dmin, sc, m, q = q4_k_fields(as_q4)
+    qh = blocks[..., 16:48].astype(np.int64)                     # [..., 32]
+    for j in range(8):
+        q[..., j, :] += ((qh >> j) & 1) << 4
+    return d, dmin, sc, m, q
+
+
+def q5_k_dequant(blocks) -> np.ndarray:
+    """w = d * sc_j * q - dmin * m_j, float64 [..., 256]."""
+    d, dmin, sc, m, q = q5_k_fields(blocks)
+    w = d[..., None, None] * sc[..., None] * q - (dmin[..., None] * m)[..., None]
+    return w.reshape(w.shape[:-2] + (QK_K,))
+
+
+def q5_k_rows(mat) -> np.ndarray:
+    mat = np.asarray(mat, dtype=np.uint8)
+    return mat.reshape(mat.shape[0], -1, Q5_K_BYTES)
 
 
 # ----------------------------------------------------------------------------

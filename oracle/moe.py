@@ -122,6 +122,19 @@ def matvec_q4_k(w_rows, a: dict) -> np.ndarray:
     return term.reshape(rows, -1).sum(axis=1)
 
 
+def matvec_q5_k(w_rows, a: dict) -> np.ndarray:
+    """Q5_K weights x Q8_1 activations, integer mode: as matvec_q4_k with
+    5-bit codes (the same exact integer block sums, the same combination)."""
+    d, dmin, sc, m, q = F.q5_k_fields(F.q5_k_rows(w_rows))
+    rows, nsb = d.shape
+    qa = a["q"].reshape(nsb, 8, 32)
+    isum = np.einsum("rsji,sji->rsj", q, qa).astype(np.float64)
+    da = a["d"].reshape(nsb, 8)
+    sa = a["s"].reshape(nsb, 8)
+    term = d[..., None] * sc * da[None] * isum - dmin[..., None] * m * sa[None]
+    return term.reshape(rows, -1).sum(axis=1)
+
+
 def matvec_q8_0(w_rows, a: dict) -> np.ndarray:
     """Q8_0 weights x Q8_1 activations: acc += d_w(b) * d_a(b) * sum_i q_w q_a."""
     dw, qw = F.q8_0_fields(F.q8_0_rows(w_rows))                  # [rows, nb], [rows, nb, 32]
@@ -138,6 +151,8 @@ def matvec_bf16(w_rows, x) -> np.ndarray:
 def matvec(fmt: str, w_rows, act):
     if fmt == "q4_k":
         return matvec_q4_k(_np(w_rows), act)
+    if fmt == "q5_k":
+        return matvec_q5_k(_np(w_rows), act)
     if fmt == "q8_0":
         return matvec_q8_0(_np(w_rows), act)
     if fmt == "bf16":
@@ -150,6 +165,8 @@ def dequant_rows(fmt: str, w_rows) -> np.ndarray:
     w = _np(w_rows)
     if fmt == "q4_k":
         return F.q4_k_dequant(F.q4_k_rows(w)).reshape(w.shape[0], -1)
+    if fmt == "q5_k":
+        return F.q5_k_dequant(F.q5_k_rows(w)).reshape(w.shape[0], -1)
     if fmt == "q8_0":
         return F.q8_0_dequant(F.q8_0_rows(w)).reshape(w.shape[0], -1)
     if fmt == "bf16":
@@ -158,11 +175,25 @@ def dequant_rows(fmt: str, w_rows) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# Load-time requant ([Q] Summary, bullets 1 and 2)
+# ----------------------------------------------------------------------------
+
+def requant_q4_k(fmt: str, w_rows) -> np.ndarray:
+    """Q8_0 or Q5_K rows [rows, bytes] -> Q4_K rows: the source weights
+    dequantised and rounded to fp32 (each product of the definition is exact in
+    fp32, so this is one rounding of the exact value), then q4_k_quantize."""
+    w32 = F.fp32(dequant_rows(fmt, w_rows)).astype(np.float32)
+    return F.q4_k_quantize(w32)
+
+
+# ----------------------------------------------------------------------------
 # Expert FFN  [S] Summary item 1, [Q] Summary
 # ----------------------------------------------------------------------------
 
-def expert_ffn(fmt: str, gate, up, down, x, x_q8_1: dict | None = None) -> dict:
-    """One expert on one token: h = silu(G x) * (U x); y = D h.
+def expert_ffn(fmt: str, gate, up, down, x, x_q8_1: dict | None = None,
+               down_fmt: str | None = None) -> dict:
+    """One expert on one token: h = silu(G x) * (U x); y = D h (D in
+    ``down_fmt``, default ``fmt``: the pages' native routed down is Q5_K).
 
     Quantised weights (integer mode): x enters as its Q8_1 blocks; h is
     rounded to fp32 and quantised to Q8_1 before the down GEMV.
@@ -179,12 +210,13 @@ def expert_ffn(fmt: str, gate, up, down, x, x_q8_1: dict | None = None) -> dict:
     u = matvec(fmt, up, a)
     h = silu(g) * u
     ah = F.q8_1_quantize(F.fp32(h))
-    return {"g": g, "u": u, "h": h, "h_q8_1": ah, "y": matvec(fmt, down, ah)}
+    return {"g": g, "u": u, "h": h, "h_q8_1": ah, "y": matvec(down_fmt or fmt, down, ah)}
 
 
-def expert_ffn_float(fmt: str, gate, up, down, x) -> dict:
+def expert_ffn_float(fmt: str, gate, up, down, x, down_fmt: str | None = None) -> dict:
     """Diagnostic float mode: dequantised weights x unquantised activations."""
-    G, U, D = (dequant_rows(fmt, m) for m in (gate, up, down))
+    G, U = (dequant_rows(fmt, m) for m in (gate, up))
+    D = dequant_rows(down_fmt or fmt, down)
     xx = np.asarray(x, dtype=np.float64)
     g, u = G @ xx, U @ xx
     h = silu(g) * u
@@ -252,10 +284,16 @@ def moe_ffn(L, x, ids, w, mode: str = "int") -> dict:
     xx = as_f64(x)
     a = F.q8_1_quantize(F.fp32(xx)) if (spec.expert_type != "bf16" and mode == "int") else None
     ys = []
+    down_fmt = getattr(spec, "down_type", None) or spec.expert_type
     for e in ids:
         s = _expert_slot(L, e)
         args = (spec.expert_type, L["gate"][s], L["up"][s], L["down"][s], xx)
-        ys.append(ffn(*args, a) if mode == "int" else ffn(*args))
+        if mode == "int":
+            ys.append(ffn(*args, a, down_fmt=down_fmt))
+        elif mode == "float":
+            ys.append(ffn(*args, down_fmt=down_fmt))
+        else:
+            ys.append(ffn(*args))
     routed = np.zeros(spec.hidden)
     for r in range(len(ids)):
         routed = routed + w[r] * ys[r]["y"]

@@ -69,6 +69,7 @@ typedef enum {
   SI_Q8_0 = 8,
   SI_Q8_1 = 9,
   SI_Q4_K = 12,
+  SI_Q5_K = 13,
   SI_BF16 = 30
 } si_dtype;
 
@@ -168,6 +169,11 @@ typedef struct si_moe_layer {
   si_dtype router_type;       /* SI_BF16 or SI_F32 */
   const void *w_norm;         /* bf16 [H], RMSNorm weight */
   float eps;                  /* RMSNorm epsilon */
+  /* Format of w_down when it differs from expert_type; 0 (SI_F32, never an
+   * expert format) = expert_type. With Q4_K gate/up, SI_Q5_K is accepted: the
+   * format the routed down ships in before the load-time requant ([Q] Summary,
+   * bullet 2); such layers run as four kernels per layer. */
+  si_dtype down_type;
 } si_moe_layer;
 
 /*
@@ -223,6 +229,26 @@ size_t si_moe_ffn_batched_workspace_bytes(const si_moe_layer *L, int n_tokens);
 si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int mode, const void *x,
                              const int32_t *topk_ids, const float *topk_w, void *routed_out,
                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * si_requant_q4_k - load-time requant of a weight matrix to Q4_K ([Q]
+ * Summary bullets 1 and 2: the shared expert ships as Q8_0, the routed down
+ * projection as Q5_K; both are requantised to Q4_K once, at model load).
+ * Each row's weights are dequantised to fp32 and quantised with the library's
+ * Q4_K quantiser, every step one IEEE fp32 operation: per 32-wide sub-block
+ * lo = min w (if negative, else +0), hi = max w (if positive, else +0),
+ * s = (hi - lo)/15, m' = -lo; d = fp16(max s / 63), dmin = fp16(max m' / 63);
+ * sc = rint(s/d), m = rint(m'/dmin) in [0, 63]; q = rint((w + dmin*m)/(d*sc))
+ * in [0, 15]; 0 wherever a divisor is 0; GGUF K-quant bytes.
+ *   src       device, rows x si_row_bytes(src_type, cols) bytes, rows contiguous
+ *   src_type  SI_Q8_0 or SI_Q5_K (176 bytes per 256 weights: fp16 d, fp16 dmin,
+ *             12 scale bytes as Q4_K, 32 bytes of fifth bits, 128 code bytes)
+ *   cols      weights per row, a multiple of 256
+ *   dst       device, rows x (cols / 256 * 144) bytes
+ * Not in place (src and dst must not overlap). Enqueues one kernel.
+ */
+si_status si_requant_q4_k(const void *src, si_dtype src_type, int64_t rows, int64_t cols,
+                          void *dst, void *stream);
 
 /*
  * si_add_rmsnorm3 - residual fold into the post-MoE RMSNorm ([R] item 2).

@@ -18,9 +18,9 @@ from ._build import LIB, build  # noqa: F401
 
 SI_OK, SI_ERR_INVALID_ARG, SI_ERR_UNSUPPORTED, SI_ERR_WORKSPACE = 0, 1, 2, 3
 SI_ERR_CUDA, SI_ERR_HANDSHAKE, SI_ERR_TIMEOUT = 4, 5, 6
-SI_F32, SI_F16, SI_Q8_0, SI_Q8_1, SI_Q4_K, SI_BF16 = 0, 1, 8, 9, 12, 30
+SI_F32, SI_F16, SI_Q8_0, SI_Q8_1, SI_Q4_K, SI_Q5_K, SI_BF16 = 0, 1, 8, 9, 12, 13, 30
 DTYPES = {"f32": SI_F32, "f16": SI_F16, "q8_0": SI_Q8_0, "q8_1": SI_Q8_1, "q4_k": SI_Q4_K,
-          "bf16": SI_BF16}
+          "q5_k": SI_Q5_K, "bf16": SI_BF16}
 
 _vp = ctypes.c_void_p
 _i32, _i64, _sz, _f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -40,6 +40,7 @@ class SiMoeLayer(ctypes.Structure):
         ("shared_inter", _i32), ("shared_type", _i32),
         ("ws_gate", _vp), ("ws_up", _vp), ("ws_down", _vp), ("w_shared_sigmoid", _vp),
         ("w_router", _vp), ("router_type", _i32), ("w_norm", _vp), ("eps", _f32),
+        ("down_type", _i32),
     ]
 
 
@@ -71,6 +72,7 @@ SIGNATURES = {
                                               _vp, _vp, _vp, _sz, _i32, _vp,
                                               ctypes.POINTER(_vp)]),
     "si_graph_is_persistent": (_i32, [_vp]),
+    "si_requant_q4_k": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "si_graph_launch": (_i32, [_vp, _vp]),
     "si_graph_destroy": (None, [_vp]),
     "si_workspace_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
@@ -220,6 +222,7 @@ class Layer:
         if "w_norm" in t:
             s.w_norm = _cuda(t["w_norm"], "w_norm")
         s.eps = spec.eps
+        s.down_type = DTYPES[spec.down_type] if getattr(spec, "down_type", "") else SI_F32
         self.c = s
 
     @property
@@ -353,6 +356,17 @@ class StackGraph:
             self.close()
         except Exception:
             pass
+
+
+def si_requant_q4_k(src: torch.Tensor, src_type: str, rows: int, cols: int,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Load-time requant: Q8_0 or Q5_K rows (uint8 [rows, row bytes]) -> Q4_K
+    rows (uint8 [rows, cols / 256 * 144])."""
+    if out is None:
+        out = torch.empty(rows, cols // 256 * 144, dtype=torch.uint8, device=src.device)
+    _check(library().si_requant_q4_k(_cuda(src, "src"), DTYPES[src_type], rows, cols,
+                                     _cuda(out, "out"), _stream(stream)), "si_requant_q4_k")
+    return out
 
 
 def si_workspace_status(ws: torch.Tensor, stream=None) -> int:

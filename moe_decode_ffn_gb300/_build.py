@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsi_moe.so")
-SOURCES = ["quant_norm.cu", "router.cu", "ffn.cu", "batched.cu", "stack.cu", "api.cu"]
+SOURCES = ["quant_norm.cu", "router.cu", "ffn.cu", "batched.cu", "stack.cu", "requant.cu", "api.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "host.hpp"),
            os.path.join(CSRC, "topk.cuh"), os.path.join(CSRC, "tc.cuh"),
            os.path.join(ROOT, "include", "si_moe.h")]

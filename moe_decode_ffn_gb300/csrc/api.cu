@@ -167,6 +167,7 @@ extern "C" size_t si_row_bytes(si_dtype type, int64_t k) {
     case SI_Q8_0: return k % 32 ? 0 : static_cast<size_t>(k / 32) * kQ80Bytes;
     case SI_Q8_1: return k % 32 ? 0 : static_cast<size_t>(k / 32) * kQ81Bytes;
     case SI_Q4_K: return k % 256 ? 0 : static_cast<size_t>(k / 256) * kQ4KBytes;
+    case SI_Q5_K: return k % 256 ? 0 : static_cast<size_t>(k / 256) * kQ5KBytes;
     default: return 0;
   }
 }

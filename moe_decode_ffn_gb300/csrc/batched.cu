@@ -637,7 +637,8 @@ static si_status batched_check(const si_moe_layer &L, int T) {
   if (!L.w_gate || !L.w_up || !L.w_down || !aligned16(L.w_gate) || !aligned16(L.w_up) ||
       !aligned16(L.w_down))
     return SI_ERR_INVALID_ARG;
-  if (L.expert_type != SI_Q4_K || L.shared_inter != 0) return SI_ERR_UNSUPPORTED;
+  if (L.expert_type != SI_Q4_K || down_type_of(L) != SI_Q4_K || L.shared_inter != 0)
+    return SI_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(T) * L.top_k > 1024) return SI_ERR_UNSUPPORTED;   // grouping buffer
   return SI_OK;
 }

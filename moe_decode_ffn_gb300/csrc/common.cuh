@@ -452,6 +452,54 @@ SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const f
   return __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
 }
 
+// Q5_K super-block (176 bytes: fp16 d, fp16 dmin, 12 scale bytes as Q4_K,
+// qh[32] fifth bits, 128 code bytes as Q4_K's codes) x Q8_1, half h
+// (sub-blocks 4h..4h+3): the Q4_K half dot with each code's fifth bit (bit j
+// of qh[i] for element i of sub-block j) OR-ed in as 16 before the dp4a.
+constexpr int kQ5KBytes = 176;
+SI_DEV float q5k_half_dot(const uint8_t *w, const uint4 *a, const float *da, const float *sa, int h) {
+  const uint4 hd = *reinterpret_cast<const uint4 *>(w);
+  int sc8[8], mn8[8];
+  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
+  q4k_unpack_scales(sw, sc8, mn8);
+  int sc[4], mn[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    sc[i] = h ? sc8[4 + i] : sc8[i];
+    mn[i] = h ? mn8[4 + i] : mn8[i];
+  }
+  const uint4 qh0 = *reinterpret_cast<const uint4 *>(w + 16);
+  const uint4 qh1 = *reinterpret_cast<const uint4 *>(w + 32);
+  const uint32_t qhw[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
+  float acc_d = 0.f, acc_m = 0.f;
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    const int p = 2 * h + pp;
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(w + 48 + 32 * p);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(w + 64 + 32 * p);
+    const uint4 al0 = a[4 * p + 0], al1 = a[4 * p + 1];
+    const uint4 ah0 = a[4 * p + 2], ah1 = a[4 * p + 3];
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+    const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+    int lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t b_lo = ((qhw[i] >> (2 * p)) & 0x01010101u) << 4;
+      const uint32_t b_hi = ((qhw[i] >> (2 * p + 1)) & 0x01010101u) << 4;
+      lo = __dp4a(static_cast<int>((qw[i] & 0x0F0F0F0Fu) | b_lo), static_cast<int>(aw_lo[i]), lo);
+      hi = __dp4a(static_cast<int>(((qw[i] >> 4) & 0x0F0F0F0Fu) | b_hi), static_cast<int>(aw_hi[i]), hi);
+    }
+    acc_d = fmaf(static_cast<float>(sc[2 * pp] * lo), da[2 * p], acc_d);
+    acc_d = fmaf(static_cast<float>(sc[2 * pp + 1] * hi), da[2 * p + 1], acc_d);
+    acc_m = fmaf(static_cast<float>(mn[2 * pp]), sa[2 * p], acc_m);
+    acc_m = fmaf(static_cast<float>(mn[2 * pp + 1]), sa[2 * p + 1], acc_m);
+  }
+  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
+  return __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
+}
+
 // Q8_0 x Q8_1 over 256 weights = 8 Q8_0 blocks (272 bytes, 16-byte aligned).
 SI_DEV float q80_sb_dot(const uint4 *w, const uint4 *a, const float *da) {
   uint32_t ww[68];

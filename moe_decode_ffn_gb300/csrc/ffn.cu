@@ -61,6 +61,7 @@ struct DownParams {
   int H, E, k, I, Is, J;
   const uint8_t *wd, *wsd;    // routed [E][H] rows of I, shared [H] rows of Is
   int rbd_r, rbd_s;
+  int down_q5;                // routed down rows are Q5_K (else Q4_K)
   const int8_t *hq;
   const float *hd, *hs, *hf;
   __nv_bfloat16 *routed, *shared;
@@ -343,6 +344,11 @@ __global__ void __launch_bounds__(kDownQThreads, 2) down_q_kernel(DownParams p) 
       v = q80_sb_dot(reinterpret_cast<const uint4 *>(row + q * 272),
                      reinterpret_cast<const uint4 *>(act.qs + (sb0 + q) * kActSbStride),
                      act.d + blk0 + 8 * q);
+    } else if (p.down_q5 && !sh) {
+      const int sb = q >> 1;
+      v = q5k_half_dot(row + sb * kQ5KBytes,
+                       reinterpret_cast<const uint4 *>(act.qs + (sb0 + sb) * kActSbStride),
+                       act.d + blk0 + 8 * sb, act.s + blk0 + 8 * sb, q & 1);
     } else {
       const int sb = q >> 1;
       v = q4k_half_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes),
@@ -539,6 +545,7 @@ __global__ void q4k_block_dots_kernel(const uint8_t *w, int rows, int k, const u
 static int row_bytes_of(si_dtype t, int k) {
   switch (t) {
     case SI_Q4_K: return k / 256 * kQ4KBytes;
+    case SI_Q5_K: return k / 256 * kQ5KBytes;
     case SI_Q8_0: return k / 32 * kQ80Bytes;
     case SI_BF16: return 2 * k;
     default: return 0;
@@ -582,12 +589,14 @@ si_status ffn_check(const si_moe_layer &L) {
   }
   if (L.expert_type == SI_Q4_K) {
     if (sh && L.shared_type != SI_Q4_K && L.shared_type != SI_Q8_0) return SI_ERR_UNSUPPORTED;
+    if (down_type_of(L) != SI_Q4_K && down_type_of(L) != SI_Q5_K) return SI_ERR_UNSUPPORTED;
     // the gate/up shared-memory buffer holds 64 rows of the widest format
     const int rb = sh ? max(row_bytes_of(SI_Q4_K, L.hidden), row_bytes_of(L.shared_type, L.hidden))
                       : row_bytes_of(SI_Q4_K, L.hidden);
     if (64u * rb + 4096u + L.hidden / 256 * 400u > 227u * 1024u) return SI_ERR_UNSUPPORTED;
   } else if (L.expert_type == SI_BF16) {
     if (sh && L.shared_type != SI_BF16) return SI_ERR_UNSUPPORTED;
+    if (down_type_of(L) != SI_BF16) return SI_ERR_UNSUPPORTED;
   } else {
     return SI_ERR_UNSUPPORTED;
   }
@@ -677,7 +686,8 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
   dp.J = (L.hidden + sms - 1) / sms;
   dp.wd = static_cast<const uint8_t *>(L.w_down);
   dp.wsd = static_cast<const uint8_t *>(L.ws_down);
-  dp.rbd_r = row_bytes_of(L.expert_type, L.inter);
+  dp.rbd_r = row_bytes_of(down_type_of(L), L.inter);
+  dp.down_q5 = down_type_of(L) == SI_Q5_K ? 1 : 0;
   dp.rbd_s = sh ? row_bytes_of(L.shared_type, L.shared_inter) : 0;
   dp.hq = gp.hq; dp.hd = gp.hd; dp.hs = gp.hs; dp.hf = gp.hf;
   dp.routed = static_cast<__nv_bfloat16 *>(routed);

@@ -48,6 +48,11 @@ inline cudaError_t allow_smem(K kernel, size_t bytes) {
   return ensure_smem(reinterpret_cast<const void *>(kernel), bytes);
 }
 
+// The routed down format of a layer (down_type 0 = expert_type).
+inline si_dtype down_type_of(const si_moe_layer &L) {
+  return L.down_type == SI_F32 ? L.expert_type : L.down_type;
+}
+
 // Load every kernel of the library (called before stream capture starts).
 cudaError_t preload_router();
 cudaError_t preload_ffn();

@@ -821,6 +821,7 @@ bool stack_supported(const si_moe_layer *layers, int n_layers) {
     const si_moe_layer &M = layers[l];
     if (M.hidden != L.hidden || M.n_experts != L.n_experts || M.top_k != L.top_k ||
         M.inter != L.inter || M.shared_inter != L.shared_inter || M.expert_type != SI_Q4_K ||
+        down_type_of(M) != SI_Q4_K ||
         M.router_type != SI_BF16 || (M.shared_inter > 0 && M.shared_type != SI_Q4_K) ||
         M.eps != L.eps)
       return false;

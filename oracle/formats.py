@@ -153,7 +153,9 @@ def q4_k_quantize(w) -> np.ndarray:
     """The library's Q4_K quantiser, on fp32 weights [rows, K] (K % 256 == 0),
     every step an IEEE fp32 operation (numpy float32 arithmetic is correctly
     rounded), rint = round half to even. Per 32-wide sub-block j of a super-block:
-      lo = min(0, min w), hi = max w, s_j = (hi - lo) / 15, m'_j = -lo;
+      lo = min w if it is negative, else +0; hi = max w if it is positive, else
+      +0 (so that the sign of a zero never reaches the bytes);
+      s_j = (hi - lo) / 15, m'_j = -lo;
       d = fp16(max_j s_j / 63), dmin = fp16(max_j m'_j / 63);
       sc_j = rint(s_j / d) and m_j = rint(m'_j / dmin), clamped to [0, 63],
       0 where the divisor is 0;
@@ -165,8 +167,9 @@ def q4_k_quantize(w) -> np.ndarray:
     rows, k = w.shape
     nsb = k // QK_K
     x = w.reshape(rows, nsb, 8, 32)
-    lo = np.minimum(x.min(axis=-1), f(0))
-    hi = x.max(axis=-1)
+    mn, mx = x.min(axis=-1), x.max(axis=-1)
+    lo = np.where(mn < 0, mn, f(0)).astype(np.float32)     # +0 unless negative
+    hi = np.where(mx > 0, mx, f(0)).astype(np.float32)     # +0 unless positive
     s = (hi - lo) / f(15)
     mneg = -lo
     d16 = (s.max(axis=-1) / f(63)).astype(np.float16)

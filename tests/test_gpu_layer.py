@@ -38,6 +38,7 @@ SPECS = {
     "q4k_shared_q4k": gen.Q4K_LAYER_SHARED_Q4_K,
     "bf16": gen.BF16_LAYER,
     "q4k_128e_i768": gen.Q4K_LAYER_128E,
+    "native_q5k_down_q8_0_shared": gen.NATIVE_LAYER_Q5K_DOWN,
 }
 
 

@@ -363,6 +363,9 @@ def run_gpu(args):
 BYTES_CFG1 = 256 * 2048 * 2 + 8 * 3 * 512 * 2048 * 2 + 3 * 512 * 2048 * 2 + 2048 * 2  # 57,675,776
 Q80_MATRIX = 512 * 2048 // 32 * 34                                                   # 1,114,112
 BYTES_CFG3_Q80 = BYTES_ROUTER + BYTES_ROUTED + 3 * Q80_MATRIX + BYTES_SIGMOID         # 18,550,784
+Q5K_MATRIX = 512 * 2048 // 256 * 176                                                  # 720,896
+BYTES_NATIVE = (BYTES_ROUTER + 8 * (2 * Q4K_MATRIX + Q5K_MATRIX) + 3 * Q80_MATRIX
+                + BYTES_SIGMOID)                                                      # 19,599,360
 Q4K_EXPERT_128E = 3 * (768 * 2048 // 256 * 144)                                       # 2,654,208
 
 
@@ -412,7 +415,9 @@ def run_configs(args):
     x = gen.make_tokens(SEED + 7, NT, device=dev)
     for cfg, spec, nbytes in (("1: bf16 layer", gen.BF16_LAYER, BYTES_CFG1),
                               ("3: Q4_K layer, Q8_0 shared", gen.Q4K_LAYER_SHARED_Q8_0, BYTES_CFG3_Q80),
-                              ("3: Q4_K layer, Q4_K shared", gen.Q4K_LAYER_SHARED_Q4_K, BYTES_LAYER_TOKEN)):
+                              ("3: Q4_K layer, Q4_K shared", gen.Q4K_LAYER_SHARED_Q4_K, BYTES_LAYER_TOKEN),
+                              ("3n: shipped formats (Q5_K routed down, Q8_0 shared)",
+                               gen.NATIVE_LAYER_Q5K_DOWN, BYTES_NATIVE)):
         layers = [m.device_layer(spec, SEED + 100, l, device=dev) for l in range(NL)]
         modes = [m.SI_STACK_AUTO]
         if spec is gen.Q4K_LAYER_SHARED_Q4_K:
@@ -428,6 +433,26 @@ def run_configs(args):
             g.close()
         del layers
         torch.cuda.empty_cache()
+
+    # load-time requant of one shipped layer to Q4_K: routed down Q5_K
+    # (256 x 2048 rows of 512) and the Q8_0 shared expert
+    spec = gen.NATIVE_LAYER_Q5K_DOWN
+    Ln = gen.make_layer(spec, SEED + 400, 0, device=dev)
+    E, H, I, Is = spec.n_experts, spec.hidden, spec.inter, spec.shared_inter
+    jobs = [(Ln["down"].reshape(E * H, -1), "q5_k", E * H, I), (Ln["sh_gate"], "q8_0", Is, H),
+            (Ln["sh_up"], "q8_0", Is, H), (Ln["sh_down"], "q8_0", H, Is)]
+    outs = [torch.empty(r, c // 256 * 144, dtype=torch.uint8, device=dev) for _, _, r, c in jobs]
+
+    def requant_all():
+        for (src, fmt, r, c), o in zip(jobs, outs):
+            m.si_requant_q4_k(src, fmt, r, c, out=o, stream=stream)
+
+    us = _time_replays(requant_all, stream, warm=2, reps=5)
+    moved = sum(src.numel() for src, _, _, _ in jobs) + sum(o.numel() for o in outs)
+    emit("requant", "one shipped layer to Q4_K (Q5_K routed down + Q8_0 shared), load time",
+         us, "us/layer", moved, note="bytes = source read + Q4_K written")
+    del Ln, jobs, outs
+    torch.cuda.empty_cache()
 
     # config 2: router + top-k on fp32 tie-stress inputs (E = 256 and 128), one
     # token per call, 64 calls per graph over 8 router matrices

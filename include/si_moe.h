@@ -154,7 +154,7 @@ typedef struct si_moe_layer {
   int n_experts;              /* E, 8..256 */
   int top_k;                  /* k, 1..8 */
   int inter;                  /* I, routed expert width, multiple of 256 */
-  si_dtype expert_type;       /* SI_Q4_K or SI_BF16 */
+  si_dtype expert_type;       /* SI_Q4_K or SI_BF16 (gate and up; down too unless down_type) */
   const void *w_gate;         /* [E][I] rows of H */
   const void *w_up;           /* [E][I] rows of H */
   const void *w_down;         /* [E][H] rows of I */

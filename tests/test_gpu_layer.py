@@ -149,3 +149,32 @@ def test_stack_paths_agree_bit_exact_and_report_their_kind():
         m.StackGraph(q8, x, mode=m.SI_STACK_PERSISTENT)
     assert e.value.status == m.SI_ERR_UNSUPPORTED
     assert not m.StackGraph(q8, x).persistent
+
+
+PERSISTENT_SHAPES = {
+    "e128_shared_q4k": gen.LayerSpec(n_experts=128, shared_type="q4_k"),
+    "e256_no_shared": gen.LayerSpec(shared_inter=0, shared_type="q4_k"),
+    "e64_top4_shared_q4k": gen.LayerSpec(n_experts=64, top_k=4, shared_type="q4_k"),
+    "i256_shared_q4k": gen.LayerSpec(inter=256, shared_type="q4_k"),
+}
+
+
+@pytest.mark.parametrize("name", list(PERSISTENT_SHAPES))
+def test_persistent_kernel_shapes_equal_the_per_layer_path(name):
+    """Other shapes the persistent kernel takes (router rows split over 8
+    warps when E <= SMs, no shared expert, top-4, narrower experts): the same
+    bits as four kernels per layer, and a clean status."""
+    spec = PERSISTENT_SHAPES[name]
+    layers = [device_layer(spec, 400 + len(name), l) for l in range(2)]
+    x = gen.make_tokens(920, 3).cuda()
+    gp = m.StackGraph(layers, x, mode=m.SI_STACK_PERSISTENT)
+    gl = m.StackGraph(layers, x, mode=m.SI_STACK_PER_LAYER)
+    for _ in range(2):                      # a replay continues the exchange epochs
+        gp.launch()
+    gl.launch()
+    torch.cuda.synchronize()
+    assert m.si_workspace_status(gp.ws) == m.SI_OK and m.si_workspace_status(gl.ws) == m.SI_OK
+    assert torch.equal(gp.ids, gl.ids)
+    assert torch.equal(gp.y, gl.y) and torch.equal(gp.sum, gl.sum)
+    gp.close()
+    gl.close()

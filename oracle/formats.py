@@ -38,21 +38,29 @@ Q8_1_BYTES = 36
 # binary float with p significant bits and a smallest quantum 2**qmin.
 # ----------------------------------------------------------------------------
 
-def _round_sig(v, p: int, qmin: int) -> np.ndarray:
+def _round_sig(v, p: int, qmin: int, emax: int) -> np.ndarray:
+    """Round to nearest even on a grid of p significant bits with subnormal
+    quantum 2**qmin; a result above the largest finite value (2 - 2**(1-p)) *
+    2**emax overflows to infinity of the same sign, as IEEE 754 rounding to
+    nearest does."""
     v = np.asarray(v, dtype=np.float64)
     _, e = np.frexp(v)                              # v = m * 2**e, 0.5 <= |m| < 1
     q = np.ldexp(1.0, np.maximum(e - p, qmin))      # spacing of the target grid at v
-    return np.rint(v / q) * q                       # exact scaling; rint is RNE
+    r = np.rint(v / q) * q                          # exact scaling; rint is RNE
+    big = (2.0 - 2.0 ** (1 - p)) * 2.0 ** emax
+    return np.where(np.abs(r) > big, np.copysign(np.inf, v), r)
 
 
 def bf16(v) -> np.ndarray:
-    """Round to bfloat16 (8 significant bits), returned as float64 values."""
-    return _round_sig(v, 8, -133)
+    """Round to bfloat16 (8 significant bits, largest finite (2 - 2**-7) *
+    2**127), returned as float64 values."""
+    return _round_sig(v, 8, -133, 127)
 
 
 def fp16(v) -> np.ndarray:
-    """Round to IEEE binary16 (11 significant bits, subnormal quantum 2**-24)."""
-    return _round_sig(v, 11, -24)
+    """Round to IEEE binary16 (11 significant bits, subnormal quantum 2**-24,
+    largest finite 65504)."""
+    return _round_sig(v, 11, -24, 15)
 
 
 def fp32(v) -> np.ndarray:

@@ -51,6 +51,23 @@ def test_fp16_rounding_matches_numpy_cast():
     assert np.array_equal(F.fp16(v.astype(np.float64)), ref)
 
 
+def test_fp16_and_bf16_overflow_like_the_library_casts():
+    """Past the largest finite value the rounding overflows to infinity:
+    65504 is the largest binary16, 65520 (halfway to 2**16) rounds up to inf."""
+    v = np.concatenate([np.linspace(65000.0, 66000.0, 4001), [65519.99, 65520.0, 1e6, 3e38]])
+    v = np.concatenate([v, -v]).astype(np.float32)
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16).astype(np.float64)
+    got = F.fp16(v.astype(np.float64))
+    assert np.array_equal(got, ref)
+    assert F.fp16(65519.0) == 65504.0 and F.fp16(65520.0) == np.inf and F.fp16(-7e4) == -np.inf
+    big = np.float32(3.3895313892515355e38)                 # (2 - 2**-7) * 2**127
+    w = np.array([big, np.nextafter(big, np.float32(np.inf)), np.finfo(np.float32).max,
+                  -np.finfo(np.float32).max, 3.39e38, 3.4e38], dtype=np.float32)
+    ref16 = torch.from_numpy(w).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(F.bf16(w.astype(np.float64)), ref16)
+
+
 def test_fp16_ties_to_even():
     # 1 + 2^-11 is halfway between 1 and 1 + 2^-10: nearest-even gives 1.
     assert F.fp16(1.0 + 2.0 ** -11) == 1.0

@@ -25,6 +25,10 @@
 //    back), so they are requested before waiting on gate/up; only the h tile
 //    (a few KB) is read after the wait. The rank-order combination and the
 //    sigmoid gate are applied in the same block.
+//  * bf16 weights (four times the bytes, no dequantisation): a warp per two
+//    row pairs, x staged once as packed bf16; each gate/up unit also issues L2 bulk
+//    prefetches for its share of its slot's down rows, so the down kernel
+//    reads L2 while DRAM streams without a gap between the two launches.
 #include "common.cuh"
 #include "host.hpp"
 
@@ -35,7 +39,7 @@ enum SharedFmt { kNoShared = 0, kSharedQ4K = SI_Q4_K, kSharedQ80 = SI_Q8_0 };
 SI_TRACE_BUFFER
 
 constexpr int kGuThreads = 512;   // 32 row pairs x (2 matrices x 8 lanes)
-constexpr int kDownThreads = 256;    // bf16 down
+constexpr int kDownThreads = 512;    // bf16 down
 constexpr int kDownQThreads = 512;   // quantised down
 
 struct GateUpParams {
@@ -47,6 +51,8 @@ struct GateUpParams {
   const uint8_t *wsg, *wsu; // shared [Is] rows
   int rb_r, rb_s;           // gate/up row bytes, routed / shared
   int units_routed;         // k * I / 32
+  const uint8_t *wd, *wsd;  // down rows (bf16 weights: staged into L2 by the gate/up units)
+  int rbd_r, rbd_s;
   int8_t *hq;               // [k*I + Is] codes
   float *hd, *hs;           // [(k*I + Is)/32] block scale / sum (fp16 values)
   float *hf;                // [k*I + Is] h in fp32
@@ -385,62 +391,97 @@ __global__ void __launch_bounds__(kDownQThreads, 2) down_q_kernel(DownParams p) 
 // ---------------------------------------------------------------------------
 // bf16 weights: fp32 activations, warp-level dot products.
 // ---------------------------------------------------------------------------
+// Global -> L2 bulk prefetch (no destination, no completion; address and
+// bytes multiples of 16). A later read of the range hits L2.
+SI_DEV void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// Lane `lane` of every warp owns columns c0 + 256 c + 8 lane .. + 7 (c < 8)
+// of each 2048-wide chunk; x sits in shared memory as packed bf16 (exact), so
+// a lane's 16-byte reads of it are consecutive across the warp (no bank
+// conflicts).
+//
+// One 2048-wide chunk of a gate row and an up row against x: eight 16-byte
+// loads of each row in flight per lane, then fmas in column order.
+SI_DEV void pair_chunk(const __nv_bfloat16 *gr, const __nv_bfloat16 *ur, const uint4 *xs, int c0,
+                       int H, int lane, float &ag, float &au) {
+  uint4 gw[8], uw[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int k0 = c0 + (c * 32 + lane) * 8;
+    if (k0 < H) {
+      gw[c] = __ldcs(reinterpret_cast<const uint4 *>(gr + k0));
+      uw[c] = __ldcs(reinterpret_cast<const uint4 *>(ur + k0));
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int k0 = c0 + (c * 32 + lane) * 8;
+    if (k0 < H) {
+      float gv[8], uv[8], xv[8];
+      Load8<__nv_bfloat16>::run(&gw[c], gv);
+      Load8<__nv_bfloat16>::run(&uw[c], uv);
+      Load8<__nv_bfloat16>::run(&xs[k0 / 8], xv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ag = fmaf(gv[i], xv[i], ag);
+        au = fmaf(uv[i], xv[i], au);
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kGuThreads, 1) gateup_bf16_kernel(GateUpParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  float *xs = reinterpret_cast<float *>(smem);   // [H]
+  uint4 *xs = reinterpret_cast<uint4 *>(smem);   // [H / 8]
   const int unit = blockIdx.x;
   const bool shared = p.Is > 0 && unit >= p.units_routed;
   const int nhb_r = p.I / 32;
   const int slot = shared ? p.k : unit / nhb_r;
   const int hb = shared ? unit - p.units_routed : unit % nhb_r;
-  for (int i0 = 8 * threadIdx.x; i0 < p.H; i0 += 8 * blockDim.x) {
-    float v[8];
-    Load8<__nv_bfloat16>::run(p.x + i0, v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xs[i0 + i] = v[i];
-  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < p.H / 8; i += blockDim.x)   // x is final before the router ran
+    xs[i] = __ldcg(reinterpret_cast<const uint4 *>(p.x) + i);
   __syncthreads();
   grid_dep_wait();
   grid_dep_launch();
   const __nv_bfloat16 *g_rows, *u_rows;
+  const uint8_t *down;
+  size_t rbd;
   if (shared) {
     g_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wsg) + static_cast<size_t>(hb) * 32 * p.H;
     u_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wsu) + static_cast<size_t>(hb) * 32 * p.H;
+    down = p.wsd;
+    rbd = static_cast<size_t>(p.rbd_s);
   } else {
     const int e = load_expert(p.ids, slot, p.E, p.status);
     const size_t row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(hb) * 32;
     g_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wg) + row0 * p.H;
     u_rows = reinterpret_cast<const __nv_bfloat16 *>(p.wu) + row0 * p.H;
+    down = p.wd ? p.wd + static_cast<size_t>(e) * p.H * p.rbd_r : nullptr;
+    rbd = static_cast<size_t>(p.rbd_r);
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot_off = slot * p.I;
-  for (int pr = 2 * warp; pr < 2 * warp + 2; ++pr) {
+#pragma unroll 1
+  for (int q = 0; q < 2; ++q) {   // the warp's two row pairs, one after the other
+    const int pr = 2 * warp + q;
     const __nv_bfloat16 *gr = g_rows + static_cast<size_t>(pr) * p.H;
     const __nv_bfloat16 *ur = u_rows + static_cast<size_t>(pr) * p.H;
     float ag = 0.f, au = 0.f;
-    for (int c0 = 0; c0 < p.H; c0 += 256 * 8) {
-      uint4 gw[8], uw[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int k0 = c0 + (c * 32 + lane) * 8;
-        if (k0 < p.H) {
-          gw[c] = __ldcs(reinterpret_cast<const uint4 *>(gr + k0));
-          uw[c] = __ldcs(reinterpret_cast<const uint4 *>(ur + k0));
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int k0 = c0 + (c * 32 + lane) * 8;
-        if (k0 < p.H) {
-          float gv[8], uv[8];
-          Load8<__nv_bfloat16>::run(&gw[c], gv);
-          Load8<__nv_bfloat16>::run(&uw[c], uv);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            ag = fmaf(gv[i], xs[k0 + i], ag);
-            au = fmaf(uv[i], xs[k0 + i], au);
-          }
-        }
+#pragma unroll 1
+    for (int c0 = 0; c0 < p.H; c0 += 2048) {
+      pair_chunk(gr, ur, xs, c0, p.H, lane, ag, au);
+      if (q == 0 && c0 == 0 && lane == 0 && warp < 4 && down) {
+        // this unit's share of its slot's down rows, staged into L2 for the
+        // down kernel while the gate/up rows stream (same bytes, no gap
+        // between the two kernels' reads): rows [hb * per, ...), four pieces
+        const int n_hb = shared ? p.Is / 32 : nhb_r;
+        const int per = (p.H + n_hb - 1) / n_hb;
+        const int r0 = min(p.H, hb * per), r1 = min(p.H, r0 + per);
+        const int n4 = (r1 - r0 + 3) / 4;
+        const int a = min(r1, r0 + warp * n4), b = min(r1, a + n4);
+        if (b > a)
+          bulk_prefetch_l2(down + static_cast<size_t>(a) * rbd, static_cast<uint32_t>((b - a) * rbd));
       }
     }
 #pragma unroll
@@ -448,7 +489,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_bf16_kernel(GateUpParams
       ag += __shfl_xor_sync(0xffffffffu, ag, m);
       au += __shfl_xor_sync(0xffffffffu, au, m);
     }
-    if (lane == 0) p.hf[slot_off + hb * 32 + pr] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
+    if (lane == 0) p.hf[slot * p.I + hb * 32 + pr] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
   }
 }
 
@@ -458,8 +499,8 @@ __global__ void __launch_bounds__(kDownThreads) down_bf16_kernel(DownParams p) {
   const int n_slots = p.k + (has_shared ? 1 : 0);
   const int nq = p.k * p.I + p.Is;
   float *wts = reinterpret_cast<float *>(smem);   // [8]
-  float *red = wts + 8;                           // [8]
-  int *eid = reinterpret_cast<int *>(red + 8);    // [8]
+  float *red = wts + 8;                           // [kDownThreads / 32]
+  int *eid = reinterpret_cast<int *>(red + kDownThreads / 32);   // [8]
   float *y = reinterpret_cast<float *>(eid + 8);  // [n_slots][J]
   float *hs = reinterpret_cast<float *>(            // [nq], 16-byte aligned
       (reinterpret_cast<uintptr_t>(y + n_slots * p.J) + 15) & ~uintptr_t(15));
@@ -494,12 +535,26 @@ __global__ void __launch_bounds__(kDownThreads) down_bf16_kernel(DownParams p) {
              : reinterpret_cast<const __nv_bfloat16 *>(p.wd) +
                    (static_cast<size_t>(eid[r]) * p.H + j0 + jl) * p.I;
       const float *hv = hs + r * p.I;
-      for (int c = l8 * 8; c < width; c += 64) {
-        float wv[8];
-        const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(row + c));
-        Load8<__nv_bfloat16>::run(&u, wv);
+      // eight 16-byte loads per lane in flight (the rows were staged into L2
+      // by the gate/up units), then fmas in column order
+#pragma unroll 1
+      for (int cc = 0; cc < width; cc += 512) {
+        uint4 u[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], hv[c + i], acc);
+        for (int it = 0; it < 8; ++it) {
+          const int c = cc + l8 * 8 + 64 * it;
+          if (c < width) u[it] = __ldcs(reinterpret_cast<const uint4 *>(row + c));
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int c = cc + l8 * 8 + 64 * it;
+          if (c < width) {
+            float wv[8];
+            Load8<__nv_bfloat16>::run(&u[it], wv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], hv[c + i], acc);
+          }
+        }
       }
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
@@ -694,6 +749,12 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
   dp.shared = static_cast<__nv_bfloat16 *>(shared);
   dp.status = gp.status;
   const int down_ctas = (L.hidden + dp.J - 1) / dp.J;
+  if (L.expert_type == SI_BF16 && !gateup_only) {
+    gp.wd = dp.wd;
+    gp.wsd = dp.wsd;
+    gp.rbd_r = dp.rbd_r;
+    gp.rbd_s = dp.rbd_s;
+  }
 
   cudaError_t e;
   if (L.expert_type == SI_Q4_K) {
@@ -705,9 +766,9 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
       e = launch_q<kSharedQ4K>(gp, dp, gsm, dsm, down_ctas, g.n_units, s, gateup_only);
     else e = launch_q<kSharedQ80>(gp, dp, gsm, dsm, down_ctas, g.n_units, s, gateup_only);
   } else {
-    const size_t gsm = static_cast<size_t>(L.hidden) * sizeof(float);
+    const size_t gsm = static_cast<size_t>(L.hidden) * 2;
     const int nq = L.top_k * L.inter + gp.Is;
-    const size_t dsm = 24 * sizeof(float) + (g.n_slots * dp.J + nq) * sizeof(float) + 16;
+    const size_t dsm = (16 + kDownThreads / 32) * sizeof(float) + (g.n_slots * dp.J + nq) * sizeof(float) + 16;
     e = allow_smem(gateup_bf16_kernel, gsm);
     if (e == cudaSuccess) e = allow_smem(down_bf16_kernel, dsm);
     if (e == cudaSuccess)

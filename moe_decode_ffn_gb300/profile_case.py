@@ -4,11 +4,15 @@ expert), n_tokens tokens through n_layers layers captured as one CUDA graph
 and replayed `launches` times, then the workspace status is checked.
 
     python -m moe_decode_ffn_gb300.profile_case --layers 4 --tokens 8 --launches 3 [--per-layer]
+    python -m moe_decode_ffn_gb300.profile_case --spec bf16 --layers 4 --tokens 2 --launches 2
     python -m moe_decode_ffn_gb300.profile_case --batched 64 --mode tensor --launches 3
 
-The second form runs the batched routed FFN of one Qwen3-30B-A3B-shaped layer
+The last form runs the batched routed FFN of one Qwen3-30B-A3B-shaped layer
 (128 experts, I=768, no shared expert, Q4_K) for T tokens with per-token
 routing, in the integer (int8) or tensor-core (tensor) mode.
+
+`--spec bf16` takes the bf16 layer of the same shape (bf16 routed and shared
+experts, four kernels per layer) instead of the all-Q4_K one.
 
 It exits non-zero if the device recorded an error, so a profiler is only ever
 run on a command that has just exited 0 on its own.
@@ -29,6 +33,7 @@ def main(argv=None) -> int:
                     "the persistent kernel")
     ap.add_argument("--batched", type=int, default=0, help="T: batched FFN of T tokens instead")
     ap.add_argument("--mode", default="tensor", choices=["tensor", "int8"])
+    ap.add_argument("--spec", default="q4k", choices=["q4k", "bf16"])
     args = ap.parse_args(argv)
 
     import torch
@@ -52,7 +57,7 @@ def main(argv=None) -> int:
         st = m.si_workspace_status(ws)
         print(f"batched T={T} mode={args.mode} launches={args.launches} status={m.status_string(st)}")
         return 0 if st == m.SI_OK else 1
-    spec = gen.Q4K_LAYER_SHARED_Q4_K
+    spec = gen.BF16_LAYER if args.spec == "bf16" else gen.Q4K_LAYER_SHARED_Q4_K
     layers = [m.device_layer(spec, args.seed, l) for l in range(args.layers)]
     x = gen.make_tokens(args.seed + 1, args.tokens, device="cuda")
     mode = m.SI_STACK_PER_LAYER if args.per_layer else m.SI_STACK_AUTO

@@ -398,40 +398,35 @@ SI_DEV void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
 }
 
 // Lane `lane` of every warp owns columns c0 + 256 c + 8 lane .. + 7 (c < 8)
-// of each 2048-wide chunk; x sits in shared memory as packed bf16 (exact), so
-// a lane's 16-byte reads of it are consecutive across the warp (no bank
-// conflicts).
-//
-// One 2048-wide chunk of a gate row and an up row against x: eight 16-byte
-// loads of each row in flight per lane, then fmas in column order.
-SI_DEV void pair_chunk(const __nv_bfloat16 *gr, const __nv_bfloat16 *ur, const uint4 *xs, int c0,
-                       int H, int lane, float &ag, float &au) {
-  uint4 gw[8], uw[8];
+// of each 2048-wide chunk of a row; x sits in shared memory as packed bf16
+// (exact), so a lane's 16-byte reads of it are consecutive across the warp
+// (no bank conflicts).
+SI_DEV void load_row8(const __nv_bfloat16 *row, int c0, int H, int lane, uint4 w[8]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const int k0 = c0 + (c * 32 + lane) * 8;
-    if (k0 < H) {
-      gw[c] = __ldcs(reinterpret_cast<const uint4 *>(gr + k0));
-      uw[c] = __ldcs(reinterpret_cast<const uint4 *>(ur + k0));
-    }
+    if (k0 < H) w[c] = __ldcs(reinterpret_cast<const uint4 *>(row + k0));
   }
+}
+
+SI_DEV void dot_row8(const uint4 w[8], const uint4 *xs, int c0, int H, int lane, float &acc) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const int k0 = c0 + (c * 32 + lane) * 8;
     if (k0 < H) {
-      float gv[8], uv[8], xv[8];
-      Load8<__nv_bfloat16>::run(&gw[c], gv);
-      Load8<__nv_bfloat16>::run(&uw[c], uv);
+      float wv[8], xv[8];
+      Load8<__nv_bfloat16>::run(&w[c], wv);
       Load8<__nv_bfloat16>::run(&xs[k0 / 8], xv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        ag = fmaf(gv[i], xv[i], ag);
-        au = fmaf(uv[i], xv[i], au);
-      }
+      for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], xv[i], acc);
     }
   }
 }
 
+// Gate/up, bf16: warp w owns row pairs 2w and 2w + 1 of the unit. Its rows
+// are taken as a sequence of items (pair, 2048-wide chunk, gate or up) with
+// two register buffers: the next item's eight 16-byte loads per lane are in
+// flight while the current one is dotted.
 __global__ void __launch_bounds__(kGuThreads, 1) gateup_bf16_kernel(GateUpParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint4 *xs = reinterpret_cast<uint4 *>(smem);   // [H / 8]
@@ -462,54 +457,134 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_bf16_kernel(GateUpParams
     down = p.wd ? p.wd + static_cast<size_t>(e) * p.H * p.rbd_r : nullptr;
     rbd = static_cast<size_t>(p.rbd_r);
   }
+  const int per_pair = 2 * ((p.H + 2047) / 2048), n_items = 2 * per_pair;
+  // item it: pair it / per_pair, chunk (it % per_pair) / 2, gate (even) or up (odd)
+  auto item_row = [&](int it, int &c0) {
+    const int q = it / per_pair, rem = it - q * per_pair;
+    c0 = (rem >> 1) * 2048;
+    return ((rem & 1) ? u_rows : g_rows) + static_cast<size_t>(2 * warp + q) * p.H;
+  };
+  uint4 wa[8], wb[8];
+  int ca, cb;
+  load_row8(item_row(0, ca), ca, p.H, lane, wa);
+  float ag = 0.f, au = 0.f;
 #pragma unroll 1
-  for (int q = 0; q < 2; ++q) {   // the warp's two row pairs, one after the other
-    const int pr = 2 * warp + q;
-    const __nv_bfloat16 *gr = g_rows + static_cast<size_t>(pr) * p.H;
-    const __nv_bfloat16 *ur = u_rows + static_cast<size_t>(pr) * p.H;
-    float ag = 0.f, au = 0.f;
-#pragma unroll 1
-    for (int c0 = 0; c0 < p.H; c0 += 2048) {
-      pair_chunk(gr, ur, xs, c0, p.H, lane, ag, au);
-      if (q == 0 && c0 == 0 && lane == 0 && warp < 4 && down) {
-        // this unit's share of its slot's down rows, staged into L2 for the
-        // down kernel while the gate/up rows stream (same bytes, no gap
-        // between the two kernels' reads): rows [hb * per, ...), four pieces
-        const int n_hb = shared ? p.Is / 32 : nhb_r;
-        const int per = (p.H + n_hb - 1) / n_hb;
-        const int r0 = min(p.H, hb * per), r1 = min(p.H, r0 + per);
-        const int n4 = (r1 - r0 + 3) / 4;
-        const int a = min(r1, r0 + warp * n4), b = min(r1, a + n4);
-        if (b > a)
-          bulk_prefetch_l2(down + static_cast<size_t>(a) * rbd, static_cast<uint32_t>((b - a) * rbd));
-      }
+  for (int it = 0; it < n_items; it += 2) {
+    load_row8(item_row(it + 1, cb), cb, p.H, lane, wb);
+    if (it == 0 && lane == 0 && warp < 4 && down) {
+      // this unit's share of its slot's down rows, staged into L2 for the
+      // down kernel while the gate/up rows stream (same bytes, no gap between
+      // the two kernels' reads): rows [hb * per, ...) in four pieces
+      const int n_hb = shared ? p.Is / 32 : nhb_r;
+      const int per = (p.H + n_hb - 1) / n_hb;
+      const int r0 = min(p.H, hb * per), r1 = min(p.H, r0 + per);
+      const int n4 = (r1 - r0 + 3) / 4;
+      const int a = min(r1, r0 + warp * n4), b = min(r1, a + n4);
+      if (b > a)
+        bulk_prefetch_l2(down + static_cast<size_t>(a) * rbd, static_cast<uint32_t>((b - a) * rbd));
     }
+    dot_row8(wa, xs, ca, p.H, lane, ag);
+    if (it + 2 < n_items) load_row8(item_row(it + 2, ca), ca, p.H, lane, wa);
+    dot_row8(wb, xs, cb, p.H, lane, au);
+    if ((it + 2) % per_pair == 0) {   // pair complete
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-      ag += __shfl_xor_sync(0xffffffffu, ag, m);
-      au += __shfl_xor_sync(0xffffffffu, au, m);
+      for (int m = 16; m > 0; m >>= 1) {
+        ag += __shfl_xor_sync(0xffffffffu, ag, m);
+        au += __shfl_xor_sync(0xffffffffu, au, m);
+      }
+      if (lane == 0)
+        p.hf[slot * p.I + hb * 32 + 2 * warp + it / per_pair] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
+      ag = 0.f;
+      au = 0.f;
     }
-    if (lane == 0) p.hf[slot * p.I + hb * 32 + pr] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
   }
 }
 
-__global__ void __launch_bounds__(kDownThreads) down_bf16_kernel(DownParams p) {
+// Down task `task` of this block (slot r, local row jl): its weight row, or
+// null past the block's rows. The ids are final before the gate/up kernel
+// starts, so this may run before the wait on gate/up.
+SI_DEV const __nv_bfloat16 *down_row(const DownParams &p, int task, int n_slots, int nrows, int j0,
+                                     int &r, int &jl, int &width) {
+  r = task / p.J;
+  jl = task - r * p.J;
+  width = 0;
+  if (task >= n_slots * p.J || jl >= nrows) return nullptr;
+  if (p.Is > 0 && r == p.k) {
+    width = p.Is;
+    return reinterpret_cast<const __nv_bfloat16 *>(p.wsd) + static_cast<size_t>(j0 + jl) * p.Is;
+  }
+  width = p.I;
+  const int e = load_expert(p.ids, r, p.E, p.status);
+  return reinterpret_cast<const __nv_bfloat16 *>(p.wd) + (static_cast<size_t>(e) * p.H + j0 + jl) * p.I;
+}
+
+// A 512-wide chunk of a down row: lane l8 of the task's 8 lanes holds
+// columns cc + 8 l8 + 64 it .. + 7 (it < 8).
+SI_DEV void load_down8(const __nv_bfloat16 *row, int cc, int width, int l8, uint4 u[8]) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int c = cc + l8 * 8 + 64 * it;
+    if (row && c < width) u[it] = __ldcs(reinterpret_cast<const uint4 *>(row + c));
+  }
+}
+
+SI_DEV void dot_down8(const uint4 u[8], const float *hv, int cc, int width, int l8, float &acc) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int c = cc + l8 * 8 + 64 * it;
+    if (c < width) {
+      float wv[8];
+      Load8<__nv_bfloat16>::run(&u[it], wv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], hv[c + i], acc);
+    }
+  }
+}
+
+// Whole-row dot of one task whose first chunk is already in `u0`, reduced
+// over its 8 lanes.
+SI_DEV float down_task_dot(const __nv_bfloat16 *row, const uint4 u0[8], const float *hv, int width,
+                           int l8) {
+  float acc = 0.f;
+  if (row) {
+    dot_down8(u0, hv, 0, width, l8, acc);
+#pragma unroll 1
+    for (int cc = 512; cc < width; cc += 512) {
+      uint4 u[8];
+      load_down8(row, cc, width, l8, u);
+      dot_down8(u, hv, cc, width, l8, acc);
+    }
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  return acc;
+}
+
+// Down, bf16: one block per tile of J output rows, tasks (slot, row) of 8
+// lanes; the first round's rows are requested before the wait on gate/up
+// (they depend only on the expert ids).
+__global__ void __launch_bounds__(kDownThreads, 1) down_bf16_kernel(DownParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const bool has_shared = p.Is > 0;
   const int n_slots = p.k + (has_shared ? 1 : 0);
   const int nq = p.k * p.I + p.Is;
   float *wts = reinterpret_cast<float *>(smem);   // [8]
   float *red = wts + 8;                           // [kDownThreads / 32]
-  int *eid = reinterpret_cast<int *>(red + kDownThreads / 32);   // [8]
-  float *y = reinterpret_cast<float *>(eid + 8);  // [n_slots][J]
+  float *y = red + kDownThreads / 32;             // [n_slots][J]
   float *hs = reinterpret_cast<float *>(            // [nq], 16-byte aligned
       (reinterpret_cast<uintptr_t>(y + n_slots * p.J) + 15) & ~uintptr_t(15));
   const int j0 = blockIdx.x * p.J;
   const int nrows = min(p.J, p.H - j0);
-  if (threadIdx.x < p.k) {
-    eid[threadIdx.x] = load_expert(p.ids, threadIdx.x, p.E, p.status);
-    wts[threadIdx.x] = __ldcg(p.wts + threadIdx.x);
-  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane >> 3, l8 = lane & 7;   // 4 tasks per warp, 8 lanes each
+  const int ntask = n_slots * p.J, step = 4 * (kDownThreads / 32);
+  if (threadIdx.x < p.k) wts[threadIdx.x] = __ldcg(p.wts + threadIdx.x);
+  int t0 = 4 * warp;
+  int r, jl, wd;
+  const __nv_bfloat16 *row = down_row(p, t0 + sub, n_slots, nrows, j0, r, jl, wd);
+  uint4 u[8];
+  load_down8(row, 0, wd, l8, u);
   float sigma = 0.f;
   if (has_shared) {
     const float z = block_dot_bf16(p.w_sg, p.x, p.H, red);
@@ -520,47 +595,14 @@ __global__ void __launch_bounds__(kDownThreads) down_bf16_kernel(DownParams p) {
   for (int i = threadIdx.x; i < nq / 4; i += blockDim.x)
     reinterpret_cast<float4 *>(hs)[i] = __ldcg(reinterpret_cast<const float4 *>(p.hf) + i);
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane >> 3, l8 = lane & 7;   // 4 tasks per warp, 8 lanes each
-  for (int t0 = 4 * warp; t0 < n_slots * p.J; t0 += 4 * (kDownThreads / 32)) {
-    const int task = t0 + sub;
-    float acc = 0.f;
-    const int r = task / p.J, jl = task % p.J;
-    const bool live = task < n_slots * p.J && jl < nrows;
-    if (live) {
-      const bool sh = has_shared && r == p.k;
-      const int width = sh ? p.Is : p.I;
-      const __nv_bfloat16 *row =
-          sh ? reinterpret_cast<const __nv_bfloat16 *>(p.wsd) + static_cast<size_t>(j0 + jl) * p.Is
-             : reinterpret_cast<const __nv_bfloat16 *>(p.wd) +
-                   (static_cast<size_t>(eid[r]) * p.H + j0 + jl) * p.I;
-      const float *hv = hs + r * p.I;
-      // eight 16-byte loads per lane in flight (the rows were staged into L2
-      // by the gate/up units), then fmas in column order
 #pragma unroll 1
-      for (int cc = 0; cc < width; cc += 512) {
-        uint4 u[8];
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int c = cc + l8 * 8 + 64 * it;
-          if (c < width) u[it] = __ldcs(reinterpret_cast<const uint4 *>(row + c));
-        }
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int c = cc + l8 * 8 + 64 * it;
-          if (c < width) {
-            float wv[8];
-            Load8<__nv_bfloat16>::run(&u[it], wv);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], hv[c + i], acc);
-          }
-        }
-      }
-    }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    if (live && l8 == 0) y[r * p.J + jl] = acc;
+  for (;;) {
+    const float acc = down_task_dot(row, u, hs + r * p.I, wd, l8);
+    if (row && l8 == 0) y[r * p.J + jl] = acc;
+    t0 += step;
+    if (t0 >= ntask) break;
+    row = down_row(p, t0 + sub, n_slots, nrows, j0, r, jl, wd);
+    load_down8(row, 0, wd, l8, u);
   }
   __syncthreads();
   if (threadIdx.x < nrows) {
@@ -768,7 +810,7 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
   } else {
     const size_t gsm = static_cast<size_t>(L.hidden) * 2;
     const int nq = L.top_k * L.inter + gp.Is;
-    const size_t dsm = (16 + kDownThreads / 32) * sizeof(float) + (g.n_slots * dp.J + nq) * sizeof(float) + 16;
+    const size_t dsm = (8 + kDownThreads / 32) * sizeof(float) + (g.n_slots * dp.J + nq) * sizeof(float) + 16;
     e = allow_smem(gateup_bf16_kernel, gsm);
     if (e == cudaSuccess) e = allow_smem(down_bf16_kernel, dsm);
     if (e == cudaSuccess)

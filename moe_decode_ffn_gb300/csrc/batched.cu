@@ -15,11 +15,13 @@
 //  prep    block 0 groups the pairs by expert (counts, offsets, stable order
 //          by token, the list of active experts); the other blocks quantise
 //          every token's x once into a Q8_1 tile record.
-//  gate/up one block per (active expert, 32-row unit of h): 32 gate + 32 up
-//          rows by TMA bulk copy, the expert's token tiles by bulk copy, h of
-//          every token, then Q8_1 of each token's 32 values of h.
+//  gate/up one block per (active expert, 32-row unit of h), two per SM: 32
+//          gate + 32 up rows by TMA bulk copy, the expert's token tiles by
+//          bulk copy, each weight super-block unpacked once and dotted with
+//          every token of the chunk, then Q8_1 of each token's 32 values of h.
 //  down    one block per (active expert, 32 output rows): the rows once, then
-//          y = D_e h for each of the expert's pairs (fp32 per pair).
+//          y = D_e h for each of the expert's pairs (fp32 per pair), each
+//          weight piece unpacked once per chunk of pairs.
 //  combine routed[t][j] = sum_r w[t][r] * y[pair(t, r)][j] in rank order.
 #include "common.cuh"
 #include "host.hpp"
@@ -29,9 +31,10 @@ namespace si {
 
 constexpr int kBatchedMaxExperts = 256;
 constexpr int kPrepThreads = 512;
-constexpr int kGuBThreads = 512;
+constexpr int kGuBThreads = 256;     // two gate/up blocks per SM: one's copies overlap the other's dots
+constexpr int kGuTok = 8;            // token tiles resident per gate/up block at once
 constexpr int kDownBThreads = 256;
-constexpr int kTokChunk = 16;        // token tiles resident per gate/up block at once
+constexpr int kDnTok = 8;            // token tiles resident per down block at once
 constexpr int kDownRows = 32;        // output rows per down block
 
 // Size of one token's Q8_1 tile record: codes at the padded super-block
@@ -138,16 +141,78 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
 }
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kGuBThreads, 1) gateup_grouped_kernel(BatchedParams p) {
+// One Q4_K super-block `w` (144 bytes, shared memory) against super-block sb
+// of the first nt token tiles at xt (Q8_1 tile records of width H, xrb bytes
+// apart): for each token exactly the single-token super-block dot (integer
+// sub-block sums, the fmas in sub-block order, one rounding per product and
+// one for the difference); the weight words and scales are read and unpacked
+// once for all the tokens.
+SI_DEV void q4k_sb_dot_tokens(const uint8_t *w, const uint8_t *xt, int xrb, int H, int sb, int nt,
+                              float out[kGuTok]) {
+  const uint4 *wv = reinterpret_cast<const uint4 *>(w);
+  const uint4 hd = wv[0];
+  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
+  int sc[8], mn[8];
+  q4k_unpack_scales(sw, sc, mn);
+  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
+  uint32_t qw[32];
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const uint4 u = wv[1 + v];
+    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
+  }
+  const int nsb = H / kQKK;
+#pragma unroll
+  for (int i = 0; i < kGuTok; ++i) {
+    if (i < nt) {
+      const uint8_t *rec = xt + i * xrb;
+      const uint4 *a = reinterpret_cast<const uint4 *>(rec + sb * kActSbStride);
+      const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb;
+      const float *sa = da + H / 32;
+      int isum[8];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const uint4 al0 = a[4 * pp + 0], al1 = a[4 * pp + 1];   // sub-block 2pp
+        const uint4 ah0 = a[4 * pp + 2], ah1 = a[4 * pp + 3];   // sub-block 2pp+1
+        const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+        const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+        int lo = 0, hi = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t q = qw[8 * pp + c];
+          lo = __dp4a(static_cast<int>(q & 0x0F0F0F0Fu), static_cast<int>(aw_lo[c]), lo);
+          hi = __dp4a(static_cast<int>((q >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[c]), hi);
+        }
+        isum[2 * pp] = lo;
+        isum[2 * pp + 1] = hi;
+      }
+      float acc_d = 0.f, acc_m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc_d = fmaf(static_cast<float>(sc[j] * isum[j]), da[j], acc_d);
+        acc_m = fmaf(static_cast<float>(mn[j]), sa[j], acc_m);
+      }
+      out[i] = __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
+    }
+  }
+}
+
+// Gate/up, integer mode: one block per (active expert, 32-row unit of h).
+// Warp w issues one bulk copy of 8 gate (w < 4) or up rows and, per chunk of
+// up to kGuTok of the expert's tokens, the copy of token tile w. Thread
+// (row pair prq, gate/up m, lane8) owns super-blocks lane8, lane8 + 8, ... of
+// rows prq and prq + 16 and dots each against all the chunk's tokens.
+__global__ void __launch_bounds__(kGuBThreads, 2) gateup_grouped_kernel(BatchedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int units = p.I / 32;
   const int nsb = p.H / kQKK;
   const int xrb = tile_record_bytes(p.H);
   const int hrb = tile_record_bytes(p.I);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);        // 4 weight groups + 1 tokens
-  float *h_s = reinterpret_cast<float *>(smem + 64);          // [kTokChunk][32]
-  uint8_t *xt = smem + 64 + kTokChunk * 32 * 4;               // [kTokChunk][xrb]
-  uint8_t *wbuf = xt + kTokChunk * xrb;                       // gate [32][rb], up [32][rb]
+  float *h_s = reinterpret_cast<float *>(smem + 64);          // [kGuTok][32]
+  uint8_t *xt = smem + 64 + kGuTok * 32 * 4;                  // [kGuTok][xrb]
+  uint8_t *wbuf = xt + kGuTok * xrb;                          // gate [32][rb], up [32][rb]
   grid_dep_wait();
   grid_dep_launch();
   const int na = __ldcg(p.n_active);
@@ -157,56 +222,62 @@ __global__ void __launch_bounds__(kGuBThreads, 1) gateup_grouped_kernel(BatchedP
   const int n_e = __ldcg(p.count + e), p0 = __ldcg(p.offset + e);
   const int rb = p.rb_gu;
   uint8_t *gate_buf = wbuf, *up_buf = wbuf + 32 * rb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bytes = 8u * rb;
   if (threadIdx.x == 0) {
     for (int g = 0; g < 5; ++g) mbar_init(&bars[g], 1);
     fence_mbar_init();
+    for (int g = 0; g < 4; ++g) mbar_arrive_expect_tx(&bars[g], 2 * bytes);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     const uint64_t pol = policy_evict_first();
-    const size_t row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(unit) * 32;
-    const uint32_t bytes = 8u * rb;
-    for (int g = 0; g < 4; ++g) {
-      mbar_arrive_expect_tx(&bars[g], 2 * bytes);
-      bulk_g2s_evict_first(gate_buf + 8 * g * rb, p.wg + (row0 + 8 * g) * rb, bytes, &bars[g], pol);
-      bulk_g2s_evict_first(up_buf + 8 * g * rb, p.wu + (row0 + 8 * g) * rb, bytes, &bars[g], pol);
-    }
+    const size_t row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(unit) * 32 + 8 * (warp & 3);
+    bulk_g2s_evict_first((warp < 4 ? gate_buf : up_buf) + 8 * (warp & 3) * rb,
+                         (warp < 4 ? p.wg : p.wu) + row0 * rb, bytes, &bars[warp & 3], pol);
   }
-  const int pr = threadIdx.x >> 4, m = (threadIdx.x >> 3) & 1, lane8 = threadIdx.x & 7;
-  const uint8_t *row = (m ? up_buf : gate_buf) + pr * rb;
+  const int prq = threadIdx.x >> 4, m = (threadIdx.x >> 3) & 1, lane8 = threadIdx.x & 7;
   uint32_t phase = 0;
-  bool weights_ready = false;
-  for (int c0 = 0; c0 < n_e; c0 += kTokChunk) {
-    const int nc = min(kTokChunk, n_e - c0);
-    if (threadIdx.x == 0) {
-      mbar_arrive_expect_tx(&bars[4], nc * xrb);
-      for (int i = 0; i < nc; ++i) {
-        const int t = __ldcg(p.pair_token + p0 + c0 + i);
-        bulk_g2s(xt + i * xrb, p.xrec + static_cast<size_t>(t) * xrb, xrb, &bars[4]);
-      }
+  for (int c0 = 0; c0 < n_e; c0 += kGuTok) {
+    const int nc = min(kGuTok, n_e - c0);
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&bars[4], nc * xrb);
+    __syncthreads();   // armed before any of the chunk's copies is issued
+    if (lane == 0 && warp < nc) {
+      const int t = __ldcg(p.pair_token + p0 + c0 + warp);
+      bulk_g2s(xt + warp * xrb, p.xrec + static_cast<size_t>(t) * xrb, xrb, &bars[4]);
     }
     mbar_wait_bounded(&bars[4], phase, p.status);
     phase ^= 1u;
-    if (!weights_ready) {
-      mbar_wait_bounded(&bars[pr >> 3], 0, p.status);
-      weights_ready = true;
-    }
-    for (int i = 0; i < nc; ++i) {
-      const ActTile a = tile_at(xt + i * xrb, p.H);
-      float acc = 0.f;
-      for (int sb = lane8; sb < nsb; sb += 8)
-        acc += q4k_sb_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes),
-                          reinterpret_cast<const uint4 *>(a.qs + sb * kActSbStride), a.d + 8 * sb,
-                          a.s + 8 * sb);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      const float u = __shfl_xor_sync(0xffffffffu, acc, 8);
-      if ((threadIdx.x & 15) == 0) h_s[i * 32 + pr] = __fdiv_rn(acc, 1.f + expf(-acc)) * u;
+#pragma unroll 1
+    for (int rr = 0; rr < 2; ++rr) {
+      const int pr = prq + 16 * rr;
+      if (c0 == 0) mbar_wait_bounded(&bars[pr >> 3], 0, p.status);
+      const uint8_t *row = (m ? up_buf : gate_buf) + pr * rb;
+      float acc[kGuTok];
+#pragma unroll
+      for (int i = 0; i < kGuTok; ++i) acc[i] = 0.f;
+#pragma unroll 1
+      for (int sb = lane8; sb < nsb; sb += 8) {
+        float dv[kGuTok];
+        q4k_sb_dot_tokens(row + sb * kQ4KBytes, xt, xrb, p.H, sb, nc, dv);
+#pragma unroll
+        for (int i = 0; i < kGuTok; ++i)
+          if (i < nc) acc[i] += dv[i];
+      }
+#pragma unroll
+      for (int i = 0; i < kGuTok; ++i) {
+        if (i < nc) {   // nc is uniform over the block
+          float v = acc[i];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          const float u = __shfl_xor_sync(0xffffffffu, v, 8);
+          if ((threadIdx.x & 15) == 0) h_s[i * 32 + pr] = __fdiv_rn(v, 1.f + expf(-v)) * u;
+        }
+      }
     }
     __syncthreads();
-    // Q8_1 of each token's 32 values of h: warp w encodes tokens w, w+16, ...
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Q8_1 of each token's 32 values of h: warp w encodes token w of the chunk
     for (int i = warp; i < nc; i += kGuBThreads / 32) {
       uint16_t d16, s16;
       const int q = q8_1_encode_warp(h_s[i * 32 + lane], d16, s16);
@@ -223,6 +294,69 @@ __global__ void __launch_bounds__(kGuBThreads, 1) gateup_grouped_kernel(BatchedP
 }
 
 // ---------------------------------------------------------------------------
+// Half h (sub-blocks 4h..4h+3) of one Q4_K super-block `w` against
+// super-block sb of the first nt Q8_1 tiles at ht (width I, hrb bytes apart):
+// per token exactly the single-token half dot (the same integer sums, fmas in
+// sub-block order and roundings); the weight words and scales are read and
+// unpacked once for all the tokens.
+SI_DEV void q4k_half_dot_tokens(const uint8_t *w, const uint8_t *ht, int hrb, int I, int sb, int h,
+                                int nt, float out[kDnTok]) {
+  const uint4 *wv = reinterpret_cast<const uint4 *>(w);
+  const uint4 hd = wv[0];
+  int sc8[8], mn8[8];
+  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
+  q4k_unpack_scales(sw, sc8, mn8);
+  int sc[4], mn[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    sc[i] = h ? sc8[4 + i] : sc8[i];
+    mn[i] = h ? mn8[4 + i] : mn8[i];
+  }
+  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
+  uint32_t qw[16];   // the half's 64 code bytes
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 u = wv[1 + 4 * h + v];
+    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
+  }
+  const int nsb = I / kQKK;
+#pragma unroll
+  for (int i = 0; i < kDnTok; ++i) {
+    if (i < nt) {
+      const uint8_t *rec = ht + i * hrb;
+      const uint4 *a = reinterpret_cast<const uint4 *>(rec + sb * kActSbStride);
+      const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb;
+      const float *sa = da + I / 32;
+      float acc_d = 0.f, acc_m = 0.f;
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const int pa = 2 * h + pp;
+        const uint4 al0 = a[4 * pa + 0], al1 = a[4 * pa + 1];
+        const uint4 ah0 = a[4 * pa + 2], ah1 = a[4 * pa + 3];
+        const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+        const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+        int lo = 0, hi = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t q = qw[8 * pp + c];
+          lo = __dp4a(static_cast<int>(q & 0x0F0F0F0Fu), static_cast<int>(aw_lo[c]), lo);
+          hi = __dp4a(static_cast<int>((q >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[c]), hi);
+        }
+        acc_d = fmaf(static_cast<float>(sc[2 * pp] * lo), da[2 * pa], acc_d);
+        acc_d = fmaf(static_cast<float>(sc[2 * pp + 1] * hi), da[2 * pa + 1], acc_d);
+        acc_m = fmaf(static_cast<float>(mn[2 * pp]), sa[2 * pa], acc_m);
+        acc_m = fmaf(static_cast<float>(mn[2 * pp + 1]), sa[2 * pa + 1], acc_m);
+      }
+      out[i] = __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
+    }
+  }
+}
+
+// Down, integer mode: one block per (active expert, 32 output rows). The
+// rows arrive once by bulk copy; per chunk of up to kDnTok of the expert's
+// pairs, each (row, half super-block) piece is dotted with every pair's h,
+// then each (pair, row) sums its pieces in order.
 __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tiles = p.H / kDownRows;
@@ -230,9 +364,9 @@ __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedPara
   const int P = 2 * nsb;                 // half super-block pieces per row
   const int hrb = tile_record_bytes(p.I);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);           // weights, tokens
-  float *part = reinterpret_cast<float *>(smem + 64);            // [kDownRows][P <= 32]
-  uint8_t *ht = smem + 64 + kDownRows * 32 * 4;                  // [kTokChunk][hrb]
-  uint8_t *wbuf = ht + kTokChunk * hrb;                          // [kDownRows][rb_d]
+  float *part = reinterpret_cast<float *>(smem + 64);            // [kDnTok][kDownRows][P]
+  uint8_t *ht = smem + 64 + kDnTok * kDownRows * P * 4;          // [kDnTok][hrb]
+  uint8_t *wbuf = ht + kDnTok * hrb;                             // [kDownRows][rb_d]
   grid_dep_wait();
   grid_dep_launch();
   const int na = __ldcg(p.n_active);
@@ -253,36 +387,31 @@ __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedPara
                          policy_evict_first());
   }
   uint32_t phase = 0;
-  bool weights_ready = false;
-  for (int c0 = 0; c0 < n_e; c0 += kTokChunk) {
-    const int nc = min(kTokChunk, n_e - c0);
+  for (int c0 = 0; c0 < n_e; c0 += kDnTok) {
+    const int nc = min(kDnTok, n_e - c0);
     if (threadIdx.x == 0) {
       mbar_arrive_expect_tx(&bars[1], nc * hrb);
       bulk_g2s(ht, p.hrec + static_cast<size_t>(p0 + c0) * hrb, nc * hrb, &bars[1]);
     }
     mbar_wait_bounded(&bars[1], phase, p.status);
     phase ^= 1u;
-    if (!weights_ready) {
-      mbar_wait_bounded(&bars[0], 0, p.status);
-      weights_ready = true;
+    if (c0 == 0) mbar_wait_bounded(&bars[0], 0, p.status);
+    for (int u = threadIdx.x; u < kDownRows * P; u += blockDim.x) {
+      const int jl = u / P, q = u % P, sb = q >> 1;
+      float dv[kDnTok];
+      q4k_half_dot_tokens(wbuf + jl * p.rb_d + sb * kQ4KBytes, ht, hrb, p.I, sb, q & 1, nc, dv);
+#pragma unroll
+      for (int i = 0; i < kDnTok; ++i)
+        if (i < nc) part[(i * kDownRows + jl) * P + q] = dv[i];
     }
-    for (int i = 0; i < nc; ++i) {
-      const ActTile h = tile_at(ht + i * hrb, p.I);
-      for (int u = threadIdx.x; u < kDownRows * P; u += blockDim.x) {
-        const int jl = u / P, q = u % P, sb = q >> 1;
-        part[jl * P + q] = q4k_half_dot(
-            reinterpret_cast<const uint4 *>(wbuf + jl * p.rb_d + sb * kQ4KBytes),
-            reinterpret_cast<const uint4 *>(h.qs + sb * kActSbStride), h.d + 8 * sb, h.s + 8 * sb,
-            q & 1);
-      }
-      __syncthreads();
-      if (threadIdx.x < kDownRows) {
-        float y = 0.f;
-        for (int q = 0; q < P; ++q) y += part[threadIdx.x * P + q];
-        p.y[static_cast<size_t>(p0 + c0 + i) * p.H + j0 + threadIdx.x] = y;
-      }
-      __syncthreads();
+    __syncthreads();
+    for (int v = threadIdx.x; v < nc * kDownRows; v += blockDim.x) {
+      const int i = v / kDownRows, jl = v % kDownRows;
+      float y = 0.f;
+      for (int q = 0; q < P; ++q) y += part[(i * kDownRows + jl) * P + q];
+      p.y[static_cast<size_t>(p0 + c0 + i) * p.H + j0 + jl] = y;
     }
+    __syncthreads();   // part and the h tiles are reused by the next chunk
   }
 }
 
@@ -644,11 +773,13 @@ static si_status batched_check(const si_moe_layer &L, int T) {
 }
 
 static size_t gateup_grouped_smem(const si_moe_layer &L) {
-  return 64 + kTokChunk * 32 * 4 + static_cast<size_t>(kTokChunk) * tile_record_bytes(L.hidden) +
+  return 64 + kGuTok * 32 * 4 + static_cast<size_t>(kGuTok) * tile_record_bytes(L.hidden) +
          64u * (L.hidden / 256 * kQ4KBytes);
 }
 static size_t down_grouped_smem(const si_moe_layer &L) {
-  return 64 + kDownRows * 32 * 4 + static_cast<size_t>(kTokChunk) * tile_record_bytes(L.inter) +
+  const int P = 2 * (L.inter / 256);
+  return 64 + static_cast<size_t>(kDnTok) * kDownRows * P * 4 +
+         static_cast<size_t>(kDnTok) * tile_record_bytes(L.inter) +
          static_cast<size_t>(kDownRows) * (L.inter / 256 * kQ4KBytes);
 }
 

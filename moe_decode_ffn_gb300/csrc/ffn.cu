@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kDownQThreads, 2) down_q_kernel(DownParams p) 
   const int n_slots = p.k + (kShared ? 1 : 0);
   const int nsb_r = p.I / kQKK, nsb_s = kShared ? p.Is / kQKK : 0;
   const int P_r = down_pieces<SFMT>(false, p.I);
-  const int P_s = kShared ? down_pieces<SFMT>(true, p.Is) : 0;
+  const int P_s = kShared ? down_pieces<SFMT>(true, p.Is) : 1;   // 1: never divides (no shared items)
   const int P_max = max(P_r, P_s);
   const int nq = p.k * p.I + (kShared ? p.Is : 0);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);

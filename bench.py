@@ -509,6 +509,109 @@ def run_configs(args):
     return 0
 
 
+def run_kernels(args):
+    """Each kernel of the four-kernel layer on its own: 8 distinct Q4_K layers
+    (Q4_K shared expert) x 16 tokens per graph, so every call reads its
+    weights from HBM; one JSON line per kernel with its algorithmic bytes and
+    fraction of the measured HBM peak. The down kernel is timed as gate/up +
+    down minus gate/up."""
+    import torch
+
+    import gen
+    import moe_decode_ffn_gb300 as m
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    m.build()
+    lib = m.library()
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.Stream(device=dev)
+    NL, NT = 8, 16
+    spec = gen.Q4K_LAYER_SHARED_Q4_K
+    H, E, k = spec.hidden, spec.n_experts, spec.top_k
+    layers = [m.device_layer(spec, SEED + 100, l, device=dev) for l in range(NL)]
+    x = gen.make_tokens(SEED + 7, NT, device=dev)
+    ids = torch.empty(NL, NT, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(NL, NT, k, dtype=torch.float32, device=dev)
+    rws = m.workspace(m.router_workspace_bytes(E, H, 1), dev)
+    fws = m.workspace(m.ffn_workspace_bytes(layers[0]), dev)
+    routed = torch.empty(H, dtype=torch.bfloat16, device=dev)
+    shared = torch.empty(H, dtype=torch.bfloat16, device=dev)
+    s_out = torch.empty(H, dtype=torch.bfloat16, device=dev)
+    y_out = torch.empty(H, dtype=torch.bfloat16, device=dev)
+    q_out = torch.empty(H // 32 * 36, dtype=torch.uint8, device=dev)
+    cs = stream.cuda_stream
+
+    def router(L, l, t):
+        return lib.si_moe_router_topk(x[t].data_ptr(), m.SI_BF16, L.t["w_router"].data_ptr(), m.SI_BF16,
+                                      H, E, k, 1, ids[l, t].data_ptr(), wts[l, t].data_ptr(), None,
+                                      rws.data_ptr(), rws.numel(), cs)
+
+    def gateup(L, l, t):
+        return lib.si_moe_ffn_gateup(L.ref, 1, x[t].data_ptr(), None, ids[l, t].data_ptr(),
+                                     fws.data_ptr(), fws.numel(), cs)
+
+    def ffn(L, l, t):
+        return lib.si_moe_ffn_decode(L.ref, 1, x[t].data_ptr(), None, ids[l, t].data_ptr(),
+                                     wts[l, t].data_ptr(), routed.data_ptr(), shared.data_ptr(),
+                                     fws.data_ptr(), fws.numel(), cs)
+
+    def norm(L, l, t):
+        return lib.si_add_rmsnorm3(routed.data_ptr(), shared.data_ptr(), x[t].data_ptr(),
+                                   L.t["w_norm"].data_ptr(), H, 1, spec.eps, s_out.data_ptr(),
+                                   y_out.data_ptr(), None, cs)
+
+    def quant(L, l, t):
+        return lib.si_quantize_q8_1(x[t].data_ptr(), m.SI_BF16, H, q_out.data_ptr(), cs)
+
+    def timed(fn):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for t in range(NT):
+                for l, L in enumerate(layers):
+                    assert fn(L, l, t) == 0
+        us = _time_replays(graph.replay, stream) / (NL * NT)
+        del graph
+        return us
+
+    def emit(kernel, row, us, nbytes, **extra):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        line = {"kernel": kernel, "row": row, "value": round(us, 3), "unit": "us/call",
+                "bytes": nbytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                "peak_gbs": peak, "peak_kind": peak_kind}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    q4k = 512 * 2048 // 256 * 144
+    b_router = E * H * 2 + H * 2
+    b_gateup = (k + 1) * 2 * q4k
+    b_down = (k + 1) * q4k + H * 2
+    us_router = timed(router)   # also leaves the ids the experts below read
+    emit("router_topk_kernel", "A1-A3", us_router, b_router, note="bf16 router, E=256, T=1")
+    us_gu = timed(gateup)
+    emit("gateup_q_kernel", "A4-A5, A7", us_gu, b_gateup,
+         note="8 routed + shared 32-row units, Q4_K, x quantised to Q8_1 inside")
+    us_ffn = timed(ffn)
+    emit("gateup_q_kernel + down_q_kernel", "A4-A7", us_ffn, b_gateup + b_down)
+    emit("down_q_kernel (by difference)", "A6-A7", us_ffn - us_gu, b_down,
+         note="gate/up + down minus gate/up; includes the sigmoid-gate dot")
+    emit("add_rmsnorm_kernel", "A8", timed(norm), 5 * H * 2, bound="latency")
+    emit("quantize_q8_1_kernel", "A4", timed(quant), H * 2 + H // 32 * 36, bound="latency")
+    # Q8_1 of a large vector: the same kernel HBM-bound
+    n = 1 << 26
+    big = torch.randn(n, device=dev).to(torch.bfloat16)
+    qb = torch.empty(n // 32 * 36, dtype=torch.uint8, device=dev)
+
+    def quant_big():
+        assert lib.si_quantize_q8_1(big.data_ptr(), m.SI_BF16, n, qb.data_ptr(), cs) == 0
+
+    us = _time_replays(quant_big, stream)
+    emit("quantize_q8_1_kernel", "A4", us, n * 2 + n // 32 * 36, note=f"n = {n} bf16 values")
+    st = max(m.si_workspace_status(w, stream) for w in (rws, fws))
+    print(json.dumps({"device_status": m.status_string(st)}), flush=True)
+    return 0 if st == m.SI_OK else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,6 +624,8 @@ def main():
                     help="skip timing the four-kernels-per-layer path")
     ap.add_argument("--configs", action="store_true",
                     help="instead of the headline line, one line per workload configuration")
+    ap.add_argument("--kernels", action="store_true",
+                    help="instead of the headline line, one line per kernel of the four-kernel layer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -528,6 +633,8 @@ def main():
         return run_reference(args)
     if args.configs:
         return run_configs(args)
+    if args.kernels:
+        return run_kernels(args)
     return run_gpu(args)
 
 

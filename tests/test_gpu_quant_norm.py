@@ -39,6 +39,44 @@ def test_quantize_q8_1_bit_exact(n, dtype):
     assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
 
 
+def _near_half_quotients(n_blocks, seed):
+    """Blocks whose quotients x / d sit on, or within a few 1e-5 of, the
+    half-integer rounding boundaries (and others well inside), for scales d
+    that are not powers of two, plus blocks of subnormal and tiny amax."""
+    rng = np.random.default_rng(seed)
+    out = np.zeros((n_blocks, 32), dtype=np.float32)
+    offsets = np.array([0.0, 1e-7, -1e-7, 1e-6, -1e-6, 1e-5, -1e-5, 2.2e-5, -2.2e-5, 2.9e-5,
+                        -2.9e-5, 3.1e-5, -3.1e-5, 5e-5, -5e-5, 0.25])
+    for b in range(n_blocks):
+        amax = np.float32(rng.uniform(0.01, 100.0) * 10.0 ** rng.integers(-30, 30))
+        if b % 17 == 0:
+            amax = np.float32(rng.uniform(1.0, 1000.0) * 1e-42)   # subnormal scale
+        d = np.float32(amax / np.float32(127.0))
+        out[b, 0] = amax if b % 2 else -amax
+        for i in range(1, 32):
+            k = rng.integers(-127, 127)
+            t = k + 0.5 + offsets[rng.integers(len(offsets))]
+            v = np.float32(np.float64(t) * np.float64(d))
+            if abs(v) > amax:
+                v = np.float32(np.sign(v) * amax)
+            if rng.integers(4) == 0:   # the neighbours of the product
+                v = np.nextafter(v, np.float32(np.inf) if rng.integers(2) else np.float32(-np.inf))
+                if abs(v) > amax:
+                    v = np.float32(np.sign(v) * amax)
+            out[b, i] = v
+    return out.reshape(-1)
+
+
+def test_quantize_q8_1_codes_at_rounding_boundaries():
+    """Codes decided by quotients on or next to a half-integer: bit-exact
+    against the oracle's IEEE fp32 division (also through the norm's fused
+    Q8_1 output path's encoder, which is the same)."""
+    x = torch.from_numpy(_near_half_quotients(4096, 11))
+    got = m.si_quantize_q8_1(x.cuda()).cpu().numpy().reshape(-1, 36)
+    ref = F.q8_1_to_bytes(F.q8_1_quantize(x.numpy()))
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+
+
 def _norm_inputs(rows, n, seed, scales=(0.1, 0.2, 1.0)):
     keys = [gen.stream_key(seed, i, rows, n) for i in range(4)]
     vs = [gen.to_bf16(gen.normal([keys[i]], rows * n, 0.0, s)[0].reshape(rows, n))

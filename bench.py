@@ -154,11 +154,11 @@ def oracle_jobs(n_layer_tokens: int, device="cpu"):
     import gen
     from oracle import moe as M
     spec = gen.Q4K_LAYER_SHARED_Q4_K
-    x = gen.make_tokens(SEED, 2)
+    x = gen.make_tokens(SEED, (n_layer_tokens + N_LAYERS - 1) // N_LAYERS)
     jobs = []
-    for i in range(n_layer_tokens):
+    for i in range(n_layer_tokens):   # distinct (layer, token) pairs
         layer = i % N_LAYERS
-        xt = x[i % 2]
+        xt = x[i // N_LAYERS]
         w_router = gen.to_bf16(gen.normal([gen.stream_key(SEED, layer, gen.ROLE_ROUTER, 0)],
                                           spec.n_experts * spec.hidden, 0.0, gen.WEIGHT_STD,
                                           device)).reshape(spec.n_experts, spec.hidden).cpu()
@@ -618,7 +618,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-layer-tokens", type=int, default=30)
+    ap.add_argument("--cpu-layer-tokens", type=int, default=120,
+                    help="layer-tokens the CPU oracle baseline times (about 10 s on one core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-layer-path", action="store_true",
                     help="skip timing the four-kernels-per-layer path")

@@ -124,6 +124,25 @@ def _opt(t, name):
     return None if t is None else _cuda(t, name)
 
 
+def _shaped(t, name: str, numel: int, dtypes) -> int:
+    """Device pointer of ``t`` after checking that it holds exactly ``numel``
+    elements of one of ``dtypes``: the C ABI takes raw pointers and cannot
+    tell a short buffer from a long one."""
+    p = _cuda(t, name)
+    if t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {' or '.join(map(str, dtypes))}")
+    return p
+
+
+_BF16 = (torch.bfloat16,)
+_FLOATS = (torch.bfloat16, torch.float32)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+_U8 = (torch.uint8,)
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -153,8 +172,9 @@ def si_quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None, stream=No
     n = x.numel()
     if out is None:
         out = torch.empty(n // 32 * 36, dtype=torch.uint8, device=x.device)
-    _check(library().si_quantize_q8_1(_cuda(x, "x"), _xtype(x), n, _cuda(out, "out"),
-                                      _stream(stream)), "si_quantize_q8_1")
+    _check(library().si_quantize_q8_1(_cuda(x, "x"), _xtype(x), n,
+                                      _shaped(out, "out", n // 32 * 36, _U8), _stream(stream)),
+           "si_quantize_q8_1")
     return out
 
 
@@ -167,6 +187,8 @@ def si_moe_router_topk(x: torch.Tensor, w_router: torch.Tensor, top_k: int = 8,
     """x [T, H], w_router [E, H] (bf16 or fp32) -> (ids int32 [T, k], w fp32 [T, k], logits|None)."""
     T, H = x.shape
     E = w_router.shape[0]
+    if tuple(w_router.shape) != (E, H):
+        raise ValueError(f"w_router has shape {tuple(w_router.shape)}, expected ({E}, {H})")
     dev = x.device
     ids = torch.empty(T, top_k, dtype=torch.int32, device=dev)
     wts = torch.empty(T, top_k, dtype=torch.float32, device=dev)
@@ -187,6 +209,8 @@ def si_moe_router_topk_noalloc(x: torch.Tensor, w_router: torch.Tensor, top_k: i
     here are the caller's; the call itself needs no workspace."""
     T, H = x.shape
     E = w_router.shape[0]
+    if tuple(w_router.shape) != (E, H):
+        raise ValueError(f"w_router has shape {tuple(w_router.shape)}, expected ({E}, {H})")
     dev = x.device
     ids = torch.empty(T, top_k, dtype=torch.int32, device=dev)
     wts = torch.empty(T, top_k, dtype=torch.float32, device=dev)
@@ -243,8 +267,11 @@ def si_moe_ffn_decode(layer: Layer, x: torch.Tensor, ids: torch.Tensor, w: torch
     shared = torch.empty(H, dtype=torch.bfloat16, device=x.device) if layer.spec.shared_inter else None
     if ws is None:
         ws = workspace(ffn_workspace_bytes(layer), x.device)
+    k = layer.spec.top_k
     _check(library().si_moe_ffn_decode(
-        layer.ref, 1, _cuda(x, "x"), _opt(x_q8_1, "x_q8_1"), _cuda(ids, "ids"), _cuda(w, "w"),
+        layer.ref, 1, _shaped(x, "x", H, _BF16),
+        None if x_q8_1 is None else _shaped(x_q8_1, "x_q8_1", H // 32 * 36, _U8),
+        _shaped(ids, "ids", k, _I32), _shaped(w, "w", k, _F32),
         _cuda(routed, "routed"), _opt(shared, "shared"), _cuda(ws, "ws"), ws.numel(),
         _stream(stream)), "si_moe_ffn_decode")
     return routed, shared
@@ -261,12 +288,14 @@ def si_moe_ffn_batched(layer: Layer, x: torch.Tensor, ids: torch.Tensor, w: torc
                        mode: int = SI_FFN_AUTO, ws: torch.Tensor | None = None, stream=None):
     """T tokens with per-token routing: x bf16 [T, H], ids int32 [T, k], w fp32 [T, k]
     -> routed bf16 [T, H]."""
-    T, H = x.shape
+    T = x.shape[0]
+    H, k = layer.spec.hidden, layer.spec.top_k
     routed = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
     if ws is None:
         ws = workspace(ffn_batched_workspace_bytes(layer, T), x.device)
     _check(library().si_moe_ffn_batched(
-        layer.ref, T, mode, _cuda(x, "x"), _cuda(ids, "ids"), _cuda(w, "w"),
+        layer.ref, T, mode, _shaped(x, "x", T * H, _BF16), _shaped(ids, "ids", T * k, _I32),
+        _shaped(w, "w", T * k, _F32),
         _cuda(routed, "routed"), _cuda(ws, "ws"), ws.numel(), _stream(stream)),
         "si_moe_ffn_batched")
     return routed
@@ -279,8 +308,9 @@ def si_add_rmsnorm3(a, b, c, w_norm, eps: float = 1e-6, want_q8: bool = False, s
     s = torch.empty_like(a)
     y = torch.empty_like(a)
     q8 = torch.empty(rows * (n // 32) * 36, dtype=torch.uint8, device=a.device) if want_q8 else None
-    _check(library().si_add_rmsnorm3(_cuda(a, "a"), _cuda(b, "b"), _opt(c, "c"),
-                                     _cuda(w_norm, "w_norm"), n, rows, eps, _cuda(s, "sum"),
+    _check(library().si_add_rmsnorm3(_shaped(a, "a", rows * n, _BF16), _shaped(b, "b", rows * n, _BF16),
+                                     None if c is None else _shaped(c, "c", rows * n, _BF16),
+                                     _shaped(w_norm, "w_norm", n, _BF16), n, rows, eps, _cuda(s, "sum"),
                                      _cuda(y, "norm"), _opt(q8, "q8"), _stream(stream)),
            "si_add_rmsnorm3")
     return s, y, q8
@@ -301,7 +331,8 @@ def si_moe_layer_decode(layer: Layer, x, residual=None, ws=None, stream=None) ->
         ws = workspace(layer_workspace_bytes(layer), dev)
     res = x if residual is None else residual
     _check(library().si_moe_layer_decode(
-        layer.ref, _cuda(x, "x"), _cuda(res, "residual"), _cuda(out["sum"], "sum"),
+        layer.ref, _shaped(x, "x", H, _BF16), _shaped(res, "residual", H, _BF16),
+        _cuda(out["sum"], "sum"),
         _cuda(out["y"], "y"), _cuda(out["ids"], "ids"), _cuda(out["w"], "w"),
         _cuda(out["routed"], "routed"), _cuda(out["shared"], "shared"), _cuda(ws, "ws"),
         ws.numel(), _stream(stream)), "si_moe_layer_decode")
@@ -323,6 +354,9 @@ class StackGraph:
         arr = (SiMoeLayer * len(self.layers))(*[l.c for l in self.layers])
         self._arr = arr
         T, H = x_in.shape
+        if H != self.layers[0].spec.hidden or x_in.dtype != torch.bfloat16:
+            raise ValueError(f"x_in must be bf16 [T, {self.layers[0].spec.hidden}], got "
+                             f"{x_in.dtype} {tuple(x_in.shape)}")
         k = self.layers[0].spec.top_k
         dev = x_in.device
         self.x_in = x_in
@@ -364,8 +398,10 @@ def si_requant_q4_k(src: torch.Tensor, src_type: str, rows: int, cols: int,
     rows (uint8 [rows, cols / 256 * 144])."""
     if out is None:
         out = torch.empty(rows, cols // 256 * 144, dtype=torch.uint8, device=src.device)
-    _check(library().si_requant_q4_k(_cuda(src, "src"), DTYPES[src_type], rows, cols,
-                                     _cuda(out, "out"), _stream(stream)), "si_requant_q4_k")
+    src_rb = int(library().si_row_bytes(DTYPES[src_type], cols))
+    _check(library().si_requant_q4_k(_shaped(src, "src", rows * src_rb, _U8), DTYPES[src_type],
+                                     rows, cols, _shaped(out, "out", rows * (cols // 256 * 144), _U8),
+                                     _stream(stream)), "si_requant_q4_k")
     return out
 
 
@@ -378,7 +414,8 @@ def si_workspace_status(ws: torch.Tensor, stream=None) -> int:
 
 def si_test_q4k_block_dots(w: torch.Tensor, rows: int, k: int, a_q8_1: torch.Tensor, stream=None):
     out = torch.empty(rows, k // 32, dtype=torch.int32, device=w.device)
-    _check(library().si_test_q4k_block_dots(_cuda(w, "w"), rows, k, _cuda(a_q8_1, "a"),
+    _check(library().si_test_q4k_block_dots(_shaped(w, "w", rows * (k // 256 * 144), _U8), rows, k,
+                                            _shaped(a_q8_1, "a", k // 32 * 36, _U8),
                                             _cuda(out, "out"), _stream(stream)),
            "si_test_q4k_block_dots")
     return out

@@ -44,6 +44,17 @@ SPECS = {
     "q4k_shared_q4k": gen.Q4K_LAYER_SHARED_Q4_K,
     "bf16": gen.BF16_LAYER,
     "q4k_128e_i768": gen.Q4K_LAYER_128E,
+    # bf16 shapes that take the other branches of the bf16 kernels: two
+    # 2048-wide chunks per gate/up row and two 512-wide chunks per down row
+    # (H=4096, I=1024) with a shared width that ends mid-chunk (768); a
+    # hidden size that ends mid-chunk (2304); down rows narrower than one
+    # chunk and no shared expert (I=256)
+    "bf16_h4096_i1024": gen.LayerSpec(hidden=4096, n_experts=16, top_k=4, inter=1024,
+                                      expert_type="bf16", shared_inter=768, shared_type="bf16"),
+    "bf16_h2304_i512": gen.LayerSpec(hidden=2304, n_experts=8, top_k=2, inter=512,
+                                     expert_type="bf16", shared_inter=256, shared_type="bf16"),
+    "bf16_no_shared_i256": gen.LayerSpec(hidden=2048, n_experts=8, top_k=2, inter=256,
+                                         expert_type="bf16", shared_inter=0, shared_type="bf16"),
 }
 
 
@@ -53,7 +64,7 @@ def test_ffn_decode_against_oracle(name, seed):
     spec = SPECS[name]
     dev = device_layer(spec, 100, 0)
     ids, w = _routing(seed, spec)
-    x = gen.make_tokens(500 + seed, 1)[0]
+    x = gen.make_tokens(500 + seed, 1, hidden=spec.hidden)[0]
     ws = m.workspace(m.ffn_workspace_bytes(dev))
     routed, shared = m.si_moe_ffn_decode(dev, x.cuda(), ids.cuda(), w.cuda(), ws=ws)
     assert m.si_workspace_status(ws) == m.SI_OK
@@ -107,6 +118,23 @@ def test_ffn_rejects_bad_arguments():
     with pytest.raises(m.SiError) as e:
         m.si_moe_ffn_decode(dev, x, ids.cuda(), w.cuda(), ws=small)
     assert e.value.status == m.SI_ERR_WORKSPACE
+
+
+def test_binding_rejects_buffers_of_the_wrong_size():
+    """The C ABI takes raw pointers; the binding checks element counts and
+    dtypes so that a short buffer never reaches a kernel."""
+    spec = gen.Q4K_LAYER_SHARED_Q8_0
+    dev = device_layer(spec, 100, 0)
+    ids, w = _routing(0, spec)
+    x = gen.make_tokens(1, 1)[0].cuda()
+    with pytest.raises(ValueError):
+        m.si_moe_ffn_decode(dev, x[:1024], ids.cuda(), w.cuda())
+    with pytest.raises(ValueError):
+        m.si_moe_ffn_decode(dev, x, ids[:4].cuda(), w.cuda())
+    with pytest.raises(ValueError):
+        m.si_moe_ffn_decode(dev, x.float(), ids.cuda(), w.cuda())
+    with pytest.raises(ValueError):
+        m.si_moe_layer_decode(dev, x, x[:2047])
 
 
 def test_ffn_out_of_range_expert_is_reported_not_faulted():

@@ -96,6 +96,26 @@ def test_batched_deterministic_and_status_clean():
     assert m.si_workspace_status(ws) == m.SI_OK
 
 
+# A wider layer: two super-blocks of each gate/up row per lane (H=4096) and
+# eight half-super-block pieces per down row (I=1024).
+WIDE = gen.LayerSpec(hidden=4096, n_experts=16, top_k=4, inter=1024, shared_inter=0,
+                     expert_type="q4_k", shared_type="q4_k")
+
+
+@pytest.mark.parametrize("T", [3, 12])
+def test_batched_int8_wide_layer_against_oracle(T):
+    dev = device_layer(WIDE, SEED, 0)
+    ids, w = routing(40 + T, T, spec=WIDE)
+    x = gen.make_tokens(950 + T, T, hidden=WIDE.hidden)
+    routed = m.si_moe_ffn_batched(dev, x.cuda(), ids.cuda(), w.cuda(), m.SI_FFN_INT8)
+    torch.cuda.synchronize()
+    host = host_layer_all(WIDE, SEED, 0)
+    for t in range(T):
+        f = M.moe_ffn(host, M.as_f64(x[t]), ids[t].tolist(), w[t].double().numpy())
+        ok, rep = P.float_parity(bf16_np(routed.cpu()[t]), F.bf16(f["routed"]))
+        assert ok, f"token {t}: {rep}"
+
+
 def test_batched_rejects_unsupported():
     dev = device_layer(SPEC, SEED, 0)
     ids, w = routing(1, 2)

@@ -125,6 +125,24 @@ def _dist():
     return world, rank, local
 
 
+def job_max(value: float, pg) -> float:
+    """The largest per-rank value over all ranks (the slowest replica bounds
+    the job); `pg` is torch.distributed when there are several ranks, else
+    None."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_layer_token(ms_step: float, world: int) -> float:
+    """Whole-job µs per layer-token: in one step each of `world` replicas runs
+    all N_LAYERS x N_TOKENS layer-tokens."""
+    return ms_step * 1e3 / (N_LAYERS * N_TOKENS) / world
+
+
 def _traffic_record(kernel_sources):
     """DRAM bytes per layer-token of the persistent stack kernel from the
     committed ncu record, valid only while the kernel sources match the
@@ -253,13 +271,9 @@ def run_gpu(args):
     ms = e0.elapsed_time(e1)
     status = m.si_workspace_status(graph.ws, stream)
     ids_ok = bool((graph.ids >= 0).all().item() and (graph.ids < 256).all().item())
-    if pg is not None:
-        t = torch.tensor([ms], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = job_max(ms, pg)
     ms_step = ms / args.steps
-    # whole job: world x 40 x 128 layer-tokens per step
-    value_job = ms_step * 1e3 / (N_LAYERS * N_TOKENS) / world
+    value_job = job_us_per_layer_token(ms_step, world)
     peak, peak_kind = _peaks()
     gbs_stage = BYTES_LAYER_TOKEN / (ms_step * 1e3 / (N_LAYERS * N_TOKENS)) / 1e3
 
@@ -280,11 +294,8 @@ def run_gpu(args):
             h_out.copy_(graph.y, non_blocking=True)
     barrier()
     e2e_ms = (time.perf_counter() - t_e2e) * 1e3 / args.steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = e2e_ms * 1e3 / (N_LAYERS * N_TOKENS) / world
+    e2e_ms = job_max(e2e_ms, pg)
+    e2e_value = job_us_per_layer_token(e2e_ms, world)
 
     # --- the same stack through four kernels per layer (context) --------------
     per_layer_us = None

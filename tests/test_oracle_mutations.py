@@ -119,3 +119,34 @@ def test_missing_first_rounding_breaks_fused_equals_unfused(monkeypatch):
     monkeypatch.setattr(M, "add_rmsnorm3", fused_no_t_round)
     with pytest.raises(AssertionError):
         P.test_add_rmsnorm3_equals_unfused_chain_bit_exact()
+
+
+def test_h_rounded_to_bf16_breaks_the_fp16_mode_bound(monkeypatch):
+    from tests import test_oracle_float_pins as FP
+
+    def wrong(fmt, gate, up, down, x):
+        G, U, D = (F.fp16(F.fp32(M.dequant_rows(fmt, m))) for m in (gate, up, down))
+        x16 = F.fp16(np.asarray(x, dtype=np.float64))
+        g, u = G @ x16, U @ x16
+        h = M.silu(g) * u
+        return {"g": g, "u": u, "h": h, "y": D @ F.bf16(h)}   # bf16 where fp16 is meant
+
+    monkeypatch.setattr(M, "expert_ffn_fp16", wrong)
+    with pytest.raises(AssertionError):
+        FP.test_fp16_mode_is_the_float_mode_up_to_the_rounding_of_h()
+
+
+def test_gate_and_up_swapped_break_the_float_mode_brute_force(monkeypatch):
+    from tests import test_oracle_float_pins as FP
+
+    def wrong(fmt, gate, up, down, x, down_fmt=None):
+        G, U = (M.dequant_rows(fmt, m) for m in (up, gate))   # swapped
+        D = M.dequant_rows(down_fmt or fmt, down)
+        xx = np.asarray(x, dtype=np.float64)
+        g, u = G @ xx, U @ xx
+        h = M.silu(g) * u
+        return {"g": g, "u": u, "h": h, "y": D @ h}
+
+    monkeypatch.setattr(M, "expert_ffn_float", wrong)
+    with pytest.raises(AssertionError):
+        FP.test_float_mode_equals_integer_brute_force()

@@ -222,7 +222,8 @@ si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, const void *x,
  *   x          device bf16 [n_tokens][H]
  *   topk_ids   device int32 [n_tokens][k]; topk_w device fp32 [n_tokens][k]
  *   routed_out device bf16 [n_tokens][H]
- * Supported: Q4_K experts, no shared expert, n_tokens * k <= 1024, H <= 8192.
+ * Supported: Q4_K experts, no shared expert, 1 <= n_tokens, n_tokens * k <= 1024,
+ * H <= 8192 (n_tokens = 0 returns SI_ERR_INVALID_ARG and enqueues nothing).
  */
 enum { SI_FFN_AUTO = 0, SI_FFN_INT8 = 1, SI_FFN_TENSOR = 2 };
 size_t si_moe_ffn_batched_workspace_bytes(const si_moe_layer *L, int n_tokens);
@@ -243,6 +244,7 @@ si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int mode, cons
  *   src       device, rows x si_row_bytes(src_type, cols) bytes, rows contiguous
  *   src_type  SI_Q8_0 or SI_Q5_K (176 bytes per 256 weights: fp16 d, fp16 dmin,
  *             12 scale bytes as Q4_K, 32 bytes of fifth bits, 128 code bytes)
+ *   rows      >= 0; 0 returns SI_OK and enqueues nothing
  *   cols      weights per row, a multiple of 256
  *   dst       device, rows x (cols / 256 * 144) bytes
  * Not in place (src and dst must not overlap). Enqueues one kernel.
@@ -288,6 +290,7 @@ si_status si_moe_layer_decode(const si_moe_layer *L, const void *x, const void *
  * n_layers layers in order; layer l takes (norm_out, sum_out) of layer l-1 as
  * (x, residual); layer 0 takes (x_in[t], x_in[t]). Tokens run one after the
  * other.
+ *   n_layers, n_tokens  >= 1 (0 returns SI_ERR_INVALID_ARG)
  *   x_in     device bf16 [n_tokens][H]; y_out device bf16 [n_tokens][H] (last norm)
  *   sum_out  device bf16 [n_tokens][H] (last residual) or NULL
  *   ids_out  device int32 [n_tokens][n_layers][k] or NULL

@@ -81,6 +81,29 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
                                               1 << 20, 7, None, ctypes.byref(h)) == m.SI_ERR_INVALID_ARG
 
 
+def test_empty_inputs_are_rejected_or_are_no_ops(lib):
+    """Zero tokens, rows or values: every call answers before touching the
+    device (an error, or for the load-time requant a no-op)."""
+    assert lib.si_quantize_q8_1(16, m.SI_F32, 0, 16, None) == m.SI_ERR_INVALID_ARG
+    r = lib.si_moe_router_topk(16, m.SI_BF16, 16, m.SI_BF16, 2048, 256, 8, 0, 16, 16, None, 256,
+                               1 << 20, None)
+    assert r == m.SI_ERR_INVALID_ARG
+    assert lib.si_add_rmsnorm3(16, 16, None, 16, 2048, 0, 1e-6, 16, 16, None, None) == m.SI_ERR_INVALID_ARG
+    assert lib.si_requant_q4_k(16, m.SI_Q8_0, 0, 2048, 16, None) == m.SI_OK
+    L = m.SiMoeLayer()
+    L.hidden, L.n_experts, L.top_k, L.inter = 2048, 128, 8, 768
+    L.expert_type = m.SI_Q4_K
+    L.w_gate = L.w_up = L.w_down = 256
+    assert lib.si_moe_ffn_batched_workspace_bytes(ctypes.byref(L), 0) == 0
+    assert lib.si_moe_ffn_batched(ctypes.byref(L), 0, 1, 16, 16, 16, 16, 256, 1 << 20,
+                                  None) == m.SI_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    assert lib.si_moe_stack_graph_create_mode(ctypes.byref(L), 1, 0, 16, 16, None, None, 256,
+                                              1 << 20, 0, None, ctypes.byref(h)) == m.SI_ERR_INVALID_ARG
+    assert lib.si_moe_stack_graph_create_mode(ctypes.byref(L), 0, 1, 16, 16, None, None, 256,
+                                              1 << 20, 0, None, ctypes.byref(h)) == m.SI_ERR_INVALID_ARG
+
+
 def test_layer_descriptor_validation(lib):
     L = m.SiMoeLayer()
     L.hidden, L.n_experts, L.top_k, L.inter = 2048, 256, 8, 512

@@ -610,7 +610,7 @@ def run_kernels(args):
     emit("quantize_q8_1_kernel", "A4", timed(quant), H * 2 + H // 32 * 36, bound="latency")
     # Q8_1 of a large vector: the same kernel HBM-bound
     n = 1 << 26
-    big = torch.randn(n, device=dev).to(torch.bfloat16)
+    big = gen.to_bf16(gen.normal([gen.stream_key(SEED, 77, n)], n, 0.0, 1.0, dev)[0])   # seeded
     qb = torch.empty(n // 32 * 36, dtype=torch.uint8, device=dev)
 
     def quant_big():

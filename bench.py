@@ -381,8 +381,11 @@ Q4K_EXPERT_128E = 3 * (768 * 2048 // 256 * 144)                                 
 
 
 def _time_replays(fn, stream, warm=3, reps=10):
-    """Device time per call of fn() (which enqueues on `stream`), by CUDA events."""
+    """Device time per call of fn() (which enqueues on `stream`), by CUDA events.
+    The device is synchronised first: inputs made on another stream (e.g. by the
+    generator on the default stream) must be complete before the timed work."""
     import torch
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):

@@ -19,9 +19,12 @@ TIE_REL = 1e-5
 
 
 def ulp_bf16(v) -> np.ndarray:
+    """Spacing of the bf16 values around |v|: 2**(e - 7) for |v| in
+    [2**e, 2**(e + 1)), and 2**-133 below the smallest normal 2**-126 (bf16
+    keeps fp32's exponent range; its subnormals are evenly spaced)."""
     v = np.abs(np.asarray(v, dtype=np.float64))
     _, e = np.frexp(np.where(v > 0, v, 1.0))
-    return np.where(v > 0, np.ldexp(1.0, e - 8), np.ldexp(1.0, -133))
+    return np.where(v > 0, np.ldexp(1.0, np.maximum(e - 8, -133)), np.ldexp(1.0, -133))
 
 
 def float_parity(got, ref, rel_l2: float = REL_L2, ulps: float = ULPS):

@@ -150,3 +150,109 @@ def test_gate_and_up_swapped_break_the_float_mode_brute_force(monkeypatch):
     monkeypatch.setattr(M, "expert_ffn_float", wrong)
     with pytest.raises(AssertionError):
         FP.test_float_mode_equals_integer_brute_force()
+
+
+# ----------------------------------------------------------------------------
+# Slips in the parity criteria: caught by tests/test_oracle_parity_pins.py
+# ----------------------------------------------------------------------------
+
+def test_ulp_exponent_off_by_one_breaks_the_spacing_pin(monkeypatch):
+    from oracle import parity as PP
+    from tests import test_oracle_parity_pins as PR
+
+    def wrong(v):
+        v = np.abs(np.asarray(v, dtype=np.float64))
+        _, e = np.frexp(np.where(v > 0, v, 1.0))
+        return np.where(v > 0, np.ldexp(1.0, np.maximum(e - 7, -133)), np.ldexp(1.0, -133))
+
+    monkeypatch.setattr(PP, "ulp_bf16", wrong)
+    with pytest.raises(AssertionError):
+        PR.test_ulp_bf16_is_the_spacing_of_adjacent_bf16_values()
+
+
+def test_ids_check_without_the_gap_rule_breaks_the_near_tie_pin(monkeypatch):
+    from oracle import parity as PP
+    from tests import test_oracle_parity_pins as PR
+    good = PP.ids_valid
+    monkeypatch.setattr(PP, "ids_valid", lambda g, r, l, tie_rel=PP.TIE_REL: good(g, r, l, 1.0))
+    with pytest.raises(AssertionError):
+        PR.test_ids_valid_near_tie_rule()
+
+
+def test_parity_without_the_l2_bound_breaks_its_pin(monkeypatch):
+    from oracle import parity as PP
+    from tests import test_oracle_parity_pins as PR
+    good = PP.float_parity
+    monkeypatch.setattr(PP, "float_parity",
+                        lambda g, o, rel_l2=PP.REL_L2, ulps=PP.ULPS: good(g, o, 1.0, ulps))
+    with pytest.raises(AssertionError):
+        PR.test_float_parity_relative_l2_boundary()
+
+
+# ----------------------------------------------------------------------------
+# Slips in the whole layer: caught by tests/test_oracle_layer_pins.py
+# ----------------------------------------------------------------------------
+
+def _slipped_layer_forward(slip):
+    """oracle.moe.layer_forward with one planted mistake."""
+    def lf(L, x, residual=None, ids=None, mode="int"):
+        spec = L["spec"]
+        xx = M.as_f64(x)
+        res = xx if (residual is None or slip == "residual_is_x") else M.as_f64(residual)
+        logits = M.router_logits(xx, L["w_router"])
+        if ids is None:
+            ids = M.topk_sort(logits, spec.top_k)
+        if slip == "order_reversed":
+            ids = list(reversed(ids))
+        if slip == "softmax_over_all":
+            full = np.exp(logits - logits.max())
+            w = full[list(ids)] / full.sum()
+        else:
+            w = M.softmax_selected(logits, ids)
+        f = M.moe_ffn(L, xx, ids, w, mode)
+        shared = f["shared"]
+        if spec.shared_inter > 0 and slip in ("gate_on_input", "gate_from_residual"):
+            z = M.as_f64(L["w_sg"]) @ (res if slip == "gate_from_residual" else xx)
+            gs = M.sigmoid(float(z))
+            inp = gs * xx if slip == "gate_on_input" else xx
+            ys = M.expert_ffn("bf16", L["sh_gate"], L["sh_up"], L["sh_down"], inp)["y"]
+            shared = ys if slip == "gate_on_input" else gs * ys
+        routed16 = f["routed"] if slip == "routed_unrounded" else F.bf16(f["routed"])
+        shared16 = F.bf16(shared)
+        if spec.shared_inter > 0 and slip != "shared_dropped":
+            s, y = M.add_rmsnorm3(routed16, shared16, res, M.as_f64(L["w_norm"]), spec.eps)
+        else:
+            s, y = M.add_rmsnorm2(routed16, res, M.as_f64(L["w_norm"]), spec.eps)
+        return {"logits": logits, "ids": list(ids), "w": w, "routed": f["routed"],
+                "routed_bf16": routed16, "shared": shared, "shared_bf16": shared16, "sum": s,
+                "y": y}
+    return lf
+
+
+@pytest.mark.parametrize("slip", ["residual_is_x", "order_reversed", "softmax_over_all",
+                                  "gate_on_input", "gate_from_residual", "routed_unrounded",
+                                  "shared_dropped"])
+def test_layer_slips_break_the_worked_example(monkeypatch, slip):
+    from tests import test_oracle_layer_pins as LP
+    monkeypatch.setattr(M, "layer_forward", _slipped_layer_forward(slip))
+    with pytest.raises(AssertionError):
+        LP.test_layer_worked_example()
+
+
+def test_unslipped_copy_passes_the_worked_example(monkeypatch):
+    """The copy used for the slips is faithful when no slip is planted."""
+    from tests import test_oracle_layer_pins as LP
+    monkeypatch.setattr(M, "layer_forward", _slipped_layer_forward(None))
+    LP.test_layer_worked_example()
+    LP.test_layer_worked_example_without_shared_expert()
+
+
+def test_unrounded_routed_changes_the_folded_sum_itself():
+    """The worked example's residual makes the bf16 rounding of routed before
+    the fold visible in `sum`, not only in the stored routed output."""
+    from tests import test_oracle_layer_pins as LP
+    x, r = LP.hand_inputs()
+    for with_shared in (True, False):
+        good = M.layer_forward(LP.hand_layer(with_shared), x, r)
+        bad = _slipped_layer_forward("routed_unrounded")(LP.hand_layer(with_shared), x, r)
+        assert not np.array_equal(good["sum"], bad["sum"]), with_shared

@@ -626,6 +626,49 @@ def run_kernels(args):
     return 0 if st == m.SI_OK else 1
 
 
+def run_profile_case(args):
+    """A bounded run for profilers (ncu), not a measurement: seeded layers,
+    n_tokens tokens through n_layers layers captured as one CUDA graph and
+    replayed `launches` times (or the batched routed FFN of one 128-expert
+    layer for `batched` tokens); exits non-zero if the device recorded an
+    error, so a profiler only ever runs a command that has just exited 0."""
+    import torch
+
+    import gen
+    import moe_decode_ffn_gb300 as m
+
+    m.build()
+    if args.batched:
+        T = args.batched
+        L = m.device_layer(gen.Q4K_LAYER_128E, args.seed, 0)
+        x = gen.make_tokens(args.seed + 1, T, device="cuda")
+        keys = gen.raw64([gen.stream_key(args.seed, t, 901) for t in range(T)], 128)
+        ids = torch.argsort(keys, dim=1)[:, :8].to(torch.int32).cuda()
+        w = torch.full((T, 8), 0.125, dtype=torch.float32, device="cuda")
+        mode = m.SI_FFN_TENSOR if args.mode == "tensor" else m.SI_FFN_INT8
+        ws = m.workspace(m.ffn_batched_workspace_bytes(L, T))
+        for _ in range(args.launches):
+            m.si_moe_ffn_batched(L, x, ids, w, mode, ws=ws)
+        torch.cuda.synchronize()
+        st = m.si_workspace_status(ws)
+        print(f"batched T={T} mode={args.mode} launches={args.launches} status={m.status_string(st)}")
+        return 0 if st == m.SI_OK else 1
+    spec = {"q4k": gen.Q4K_LAYER_SHARED_Q4_K, "q4k_q8_0": gen.Q4K_LAYER_SHARED_Q8_0,
+            "bf16": gen.BF16_LAYER}[args.spec]
+    layers = [m.device_layer(spec, args.seed, l) for l in range(args.layers)]
+    x = gen.make_tokens(args.seed + 1, args.tokens, device="cuda")
+    mode = m.SI_STACK_PER_LAYER if args.per_layer else m.SI_STACK_AUTO
+    g = m.StackGraph(layers, x, mode=mode)
+    for _ in range(args.launches):
+        g.launch()
+    torch.cuda.synchronize()
+    st = m.si_workspace_status(g.ws)
+    print(f"layers={args.layers} tokens={args.tokens} launches={args.launches} "
+          f"persistent={g.persistent} status={m.status_string(st)}")
+    g.close()
+    return 0 if st == m.SI_OK else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -641,7 +684,20 @@ def main():
                     help="instead of the headline line, one line per workload configuration")
     ap.add_argument("--kernels", action="store_true",
                     help="instead of the headline line, one line per kernel of the four-kernel layer")
+    pc = ap.add_argument_group("--profile-case", "a bounded run for profilers (not a measurement)")
+    pc.add_argument("--profile-case", action="store_true")
+    pc.add_argument("--layers", type=int, default=4)
+    pc.add_argument("--tokens", type=int, default=8)
+    pc.add_argument("--launches", type=int, default=3)
+    pc.add_argument("--seed", type=int, default=21)
+    pc.add_argument("--per-layer", action="store_true",
+                    help="four kernels per layer instead of the persistent kernel")
+    pc.add_argument("--spec", default="q4k", choices=["q4k", "q4k_q8_0", "bf16"])
+    pc.add_argument("--batched", type=int, default=0, help="T: the batched FFN of T tokens instead")
+    pc.add_argument("--mode", default="tensor", choices=["tensor", "int8"])
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -131,22 +131,33 @@ si_status si_moe_router_topk(const void *x, si_dtype x_type, const void *w_route
  * synchronise the whole device and stall other streams), or a plug-in running
  * inside a host whose allocator owns all device memory. Same arguments and
  * results as si_moe_router_topk, minus the workspace. It allocates nothing:
- * its scratch is a fixed array compiled into the library (about 132 KB on
+ * its scratch is a fixed array compiled into the library (133,376 bytes on
  * every GPU that loads it, held until the process exits).
- *   - Limit: n_tokens * n_experts <= 16384 (e.g. 64 tokens of 256 experts);
- *     larger calls return SI_ERR_UNSUPPORTED and enqueue nothing.
+ *   - Limit: n_tokens * n_experts <= 16384 (e.g. 64 tokens of 256 experts,
+ *     2048 tokens of 8); every such shape fits the array. Larger calls return
+ *     SI_ERR_UNSUPPORTED and enqueue nothing.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.
  *   - All calls share the one array: calls that may overlap on the GPU (two
  *     streams, two threads) race and must be serialised by the caller. Each
- *     call clears the status word and completion counters before its kernel
- *     (an asynchronous memset on `stream`).
+ *     call clears the completion counters before its kernel (an asynchronous
+ *     memset on `stream`).
+ *   - Device-side errors of these calls (a completion count that does not add
+ *     up, e.g. from two calls that overlapped: ids -1 and weights 0) are kept
+ *     in the array's status word, the first one only, until
+ *     si_moe_router_noalloc_status reads them.
  */
 si_status si_moe_router_topk_noalloc(const void *x, si_dtype x_type, const void *w_router,
                                      si_dtype w_type, int hidden, int n_experts, int top_k,
                                      int n_tokens, int32_t *topk_ids, float *topk_w,
                                      float *logits_out, void *stream);
+
+/* Synchronises `stream`, then reads the status word of the no-alloc router's
+ * built-in scratch on the current device (SI_OK if no call recorded a
+ * device-side error since the last read) and clears it. Like the router
+ * call, it allocates nothing. */
+si_status si_moe_router_noalloc_status(void *stream, int *status_out);
 
 /* One MoE FFN layer: shapes, formats and device weight pointers. */
 typedef struct si_moe_layer {
@@ -345,6 +356,31 @@ si_status si_workspace_status(const void *workspace, void *stream, int *status_o
  * [rows][k] against Q8_1 activations [k/32]; out int32 [rows][k/32]. */
 si_status si_test_q4k_block_dots(const void *w, int rows, int k, const void *a_q8_1,
                                  int32_t *out, void *stream);
+
+/* Exact int32 sums sum_i q_w,i * q_a,i of every (vector, row, 32-block), taken
+ * by the integer helper that each GEMV of the library uses ("Q4_K
+ * shared-expert FFN kernels + Q8_0/Q5_K->Q4_K requant of the MoE FFN stage",
+ * Summary: int8 dot products of Q8_1 activations with the weight codes):
+ *   SI_TEST_DOTS_Q4K_SB          whole Q4_K super-blocks (gate/up GEMVs)
+ *   SI_TEST_DOTS_Q4K_HALF        Q4_K halves of 128 weights (down GEMVs, and
+ *                                the persistent stack's down step)
+ *   SI_TEST_DOTS_Q5K_HALF        Q5_K halves (the Q5_K routed down)
+ *   SI_TEST_DOTS_Q4K_SB_TOKENS   whole super-blocks, code words loaded once for
+ *                                every vector (batched gate/up), n_vec <= 8
+ *   SI_TEST_DOTS_Q4K_HALF_TOKENS halves, the same (batched down), n_vec <= 8
+ *   w      device, rows x (k/256) super-blocks (144 bytes Q4_K, 176 Q5_K)
+ *   k      multiple of 256, <= 16384; rows 1..65535
+ *   a_q8_1 device, n_vec vectors of k/32 Q8_1 blocks (36 bytes), back to back
+ *   out    device int32 [n_vec][rows][k/32] */
+enum {
+  SI_TEST_DOTS_Q4K_SB = 0,
+  SI_TEST_DOTS_Q4K_HALF = 1,
+  SI_TEST_DOTS_Q5K_HALF = 2,
+  SI_TEST_DOTS_Q4K_SB_TOKENS = 3,
+  SI_TEST_DOTS_Q4K_HALF_TOKENS = 4
+};
+si_status si_test_block_dots(int kind, const void *w, int rows, int k, const void *a_q8_1,
+                             int n_vec, int32_t *out, void *stream);
 
 /* Only the gate/up kernel of si_moe_ffn_decode (same arguments; h is left in
  * the workspace). For timing that kernel in isolation. */

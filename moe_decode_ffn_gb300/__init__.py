@@ -55,6 +55,7 @@ SIGNATURES = {
                                   _vp, _sz, _vp]),
     "si_moe_router_topk_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
                                           _vp, _vp]),
+    "si_moe_router_noalloc_status": (_i32, [_vp, ctypes.POINTER(_i32)]),
     "si_moe_ffn_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
     "si_moe_ffn_decode": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _vp, _sz, _vp]),
@@ -78,6 +79,7 @@ SIGNATURES = {
     "si_workspace_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "si_moe_ffn_gateup": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "si_test_q4k_block_dots": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp]),
+    "si_test_block_dots": (_i32, [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp]),
     "si_test_wait_timeout": (_i32, [ctypes.c_uint64, _vp, _vp]),
     "si_test_poll_timeout": (_i32, [ctypes.c_uint64, _vp, _vp]),
     "si_test_umma_f16": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp]),
@@ -220,6 +222,14 @@ def si_moe_router_topk_noalloc(x: torch.Tensor, w_router: torch.Tensor, top_k: i
         _cuda(ids, "ids"), _cuda(wts, "w"), _opt(logits, "logits"), _stream(stream)),
         "si_moe_router_topk_noalloc")
     return ids, wts, logits
+
+
+def si_moe_router_noalloc_status(stream=None) -> int:
+    """Reads and clears the device status of the no-alloc router's scratch."""
+    v = _i32(0)
+    _check(library().si_moe_router_noalloc_status(_stream(stream), ctypes.byref(v)),
+           "si_moe_router_noalloc_status")
+    return v.value
 
 
 class Layer:
@@ -418,6 +428,23 @@ def si_test_q4k_block_dots(w: torch.Tensor, rows: int, k: int, a_q8_1: torch.Ten
                                             _shaped(a_q8_1, "a", k // 32 * 36, _U8),
                                             _cuda(out, "out"), _stream(stream)),
            "si_test_q4k_block_dots")
+    return out
+
+
+SI_TEST_DOTS_Q4K_SB, SI_TEST_DOTS_Q4K_HALF, SI_TEST_DOTS_Q5K_HALF = 0, 1, 2
+SI_TEST_DOTS_Q4K_SB_TOKENS, SI_TEST_DOTS_Q4K_HALF_TOKENS = 3, 4
+
+
+def si_test_block_dots(kind: int, w: torch.Tensor, rows: int, k: int, a_q8_1: torch.Tensor,
+                       n_vec: int = 1, stream=None):
+    """Exact int32 block sums of the library's integer dot helper `kind` ->
+    int32 [n_vec, rows, k / 32]."""
+    sbb = 176 if kind == SI_TEST_DOTS_Q5K_HALF else 144
+    out = torch.empty(n_vec, rows, k // 32, dtype=torch.int32, device=w.device)
+    _check(library().si_test_block_dots(kind, _shaped(w, "w", rows * (k // 256 * sbb), _U8), rows, k,
+                                        _shaped(a_q8_1, "a", n_vec * (k // 32 * 36), _U8), n_vec,
+                                        _cuda(out, "out"), _stream(stream)),
+           "si_test_block_dots")
     return out
 
 

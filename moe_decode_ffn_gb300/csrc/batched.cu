@@ -147,6 +147,21 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
 // sub-block sums, the fmas in sub-block order, one rounding per product and
 // one for the difference); the weight words and scales are read and unpacked
 // once for all the tokens.
+// The 32 code words of a Q4_K super-block (all 8 sub-blocks), loaded once
+// for every token; and the exact int32 sums of its 8 sub-blocks with one
+// token's 256 activation codes (a: that super-block of the token's tile).
+SI_DEV void q4k_sb_words(const uint4 *wv, uint32_t qw[32]) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const uint4 u = wv[1 + v];
+    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
+  }
+}
+SI_DEV void q4k_sb_token_isums(const uint32_t qw[32], const uint4 *a, int isum[8]) {
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) q4k_pair_isums(qw + 8 * pp, a + 4 * pp, isum[2 * pp], isum[2 * pp + 1]);
+}
+
 SI_DEV void q4k_sb_dot_tokens(const uint8_t *w, const uint8_t *xt, int xrb, int H, int sb, int nt,
                               float out[kGuTok]) {
   const uint4 *wv = reinterpret_cast<const uint4 *>(w);
@@ -157,11 +172,7 @@ SI_DEV void q4k_sb_dot_tokens(const uint8_t *w, const uint8_t *xt, int xrb, int 
   const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
   const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
   uint32_t qw[32];
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const uint4 u = wv[1 + v];
-    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
-  }
+  q4k_sb_words(wv, qw);
   const int nsb = H / kQKK;
 #pragma unroll
   for (int i = 0; i < kGuTok; ++i) {
@@ -171,22 +182,7 @@ SI_DEV void q4k_sb_dot_tokens(const uint8_t *w, const uint8_t *xt, int xrb, int 
       const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb;
       const float *sa = da + H / 32;
       int isum[8];
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        const uint4 al0 = a[4 * pp + 0], al1 = a[4 * pp + 1];   // sub-block 2pp
-        const uint4 ah0 = a[4 * pp + 2], ah1 = a[4 * pp + 3];   // sub-block 2pp+1
-        const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
-        const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
-        int lo = 0, hi = 0;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t q = qw[8 * pp + c];
-          lo = __dp4a(static_cast<int>(q & 0x0F0F0F0Fu), static_cast<int>(aw_lo[c]), lo);
-          hi = __dp4a(static_cast<int>((q >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[c]), hi);
-        }
-        isum[2 * pp] = lo;
-        isum[2 * pp + 1] = hi;
-      }
+      q4k_sb_token_isums(qw, a, isum);
       float acc_d = 0.f, acc_m = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -299,6 +295,23 @@ __global__ void __launch_bounds__(kGuBThreads, 2) gateup_grouped_kernel(BatchedP
 // per token exactly the single-token half dot (the same integer sums, fmas in
 // sub-block order and roundings); the weight words and scales are read and
 // unpacked once for all the tokens.
+// The 16 code words of half h of a Q4_K super-block (sub-blocks 4h .. 4h +
+// 3), loaded once for every token; and the exact int32 sums of those 4
+// sub-blocks with one token's activation codes (a: the super-block of the
+// token's tile).
+SI_DEV void q4k_half_words(const uint4 *wv, int h, uint32_t qw[16]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 u = wv[1 + 4 * h + v];
+    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
+  }
+}
+SI_DEV void q4k_half_token_isums(const uint32_t qw[16], const uint4 *a, int h, int isum[4]) {
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp)
+    q4k_pair_isums(qw + 8 * pp, a + 4 * (2 * h + pp), isum[2 * pp], isum[2 * pp + 1]);
+}
+
 SI_DEV void q4k_half_dot_tokens(const uint8_t *w, const uint8_t *ht, int hrb, int I, int sb, int h,
                                 int nt, float out[kDnTok]) {
   const uint4 *wv = reinterpret_cast<const uint4 *>(w);
@@ -315,11 +328,7 @@ SI_DEV void q4k_half_dot_tokens(const uint8_t *w, const uint8_t *ht, int hrb, in
   const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
   const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
   uint32_t qw[16];   // the half's 64 code bytes
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 u = wv[1 + 4 * h + v];
-    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
-  }
+  q4k_half_words(wv, h, qw);
   const int nsb = I / kQKK;
 #pragma unroll
   for (int i = 0; i < kDnTok; ++i) {
@@ -328,25 +337,13 @@ SI_DEV void q4k_half_dot_tokens(const uint8_t *w, const uint8_t *ht, int hrb, in
       const uint4 *a = reinterpret_cast<const uint4 *>(rec + sb * kActSbStride);
       const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb;
       const float *sa = da + I / 32;
+      int isum[4];
+      q4k_half_token_isums(qw, a, h, isum);
       float acc_d = 0.f, acc_m = 0.f;
 #pragma unroll
-      for (int pp = 0; pp < 2; ++pp) {
-        const int pa = 2 * h + pp;
-        const uint4 al0 = a[4 * pa + 0], al1 = a[4 * pa + 1];
-        const uint4 ah0 = a[4 * pa + 2], ah1 = a[4 * pa + 3];
-        const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
-        const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
-        int lo = 0, hi = 0;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t q = qw[8 * pp + c];
-          lo = __dp4a(static_cast<int>(q & 0x0F0F0F0Fu), static_cast<int>(aw_lo[c]), lo);
-          hi = __dp4a(static_cast<int>((q >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[c]), hi);
-        }
-        acc_d = fmaf(static_cast<float>(sc[2 * pp] * lo), da[2 * pa], acc_d);
-        acc_d = fmaf(static_cast<float>(sc[2 * pp + 1] * hi), da[2 * pa + 1], acc_d);
-        acc_m = fmaf(static_cast<float>(mn[2 * pp]), sa[2 * pa], acc_m);
-        acc_m = fmaf(static_cast<float>(mn[2 * pp + 1]), sa[2 * pa + 1], acc_m);
+      for (int q = 0; q < 4; ++q) {
+        acc_d = fmaf(static_cast<float>(sc[q] * isum[q]), da[4 * h + q], acc_d);
+        acc_m = fmaf(static_cast<float>(mn[q]), sa[4 * h + q], acc_m);
       }
       out[i] = __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
     }
@@ -506,10 +503,12 @@ SI_DEV bool tc_product(RowPtr a_row_ptr, const __half *bsrc, const int *brows, i
     const int b = c & 1;
     uint8_t *A = smem + b * kTcABytes;
     uint8_t *B = smem + 2 * kTcABytes + b * kTcBBytes;
-    if (pending[b]) {
+    if (pending[b]) {   // uniform over the block
       ok &= mbar_wait_bounded(&bars[b], phase[b], status);
       phase[b] ^= 1u;
       pending[b] = 0;
+      // a commit that never arrived: no more tiles, no more MMAs
+      if (__syncthreads_or(!ok)) break;
     }
     {
       const int row = threadIdx.x >> 1, hf = threadIdx.x & 1;   // 256 threads: 128 rows x 2 halves
@@ -529,6 +528,8 @@ SI_DEV bool tc_product(RowPtr a_row_ptr, const __half *bsrc, const int *brows, i
     }
     pending[b] = 1;
   }
+  // every commit still outstanding (also after a failed wait: the MMAs
+  // already issued must finish before tensor memory is read or released)
   for (int b = 0; b < 2; ++b) {
     if (pending[b]) {
       ok &= mbar_wait_bounded(&bars[b], phase[b], status);
@@ -537,7 +538,7 @@ SI_DEV bool tc_product(RowPtr a_row_ptr, const __half *bsrc, const int *brows, i
     }
   }
   tc_fence_after();
-  return ok;
+  return !__syncthreads_or(!ok);
 }
 
 SI_DEV void tc_setup(uint8_t *smem, uint64_t *bars, uint32_t *s_taddr) {
@@ -588,8 +589,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gateup_kernel(BatchedParams 
   float *U = reinterpret_cast<float *>(smem);     // [64][kTcMaxN], reuses tile A0 after the MMAs
   for (int nc0 = 0; nc0 < n_e; nc0 += kTcMaxN) {
     const int nv = min(kTcMaxN, n_e - nc0), npad = (nv + 15) & ~15;
-    tc_product(a_row, p.xh, p.pair_token + p0 + nc0, 0, nv, npad, p.H, p.H / kTcK, smem, bars,
-               phase, pending, taddr, p.status);
+    // a timed-out commit (recorded in the status word): leave the
+    // accumulators unread and the outputs unwritten
+    if (!tc_product(a_row, p.xh, p.pair_token + p0 + nc0, 0, nv, npad, p.H, p.H / kTcK, smem, bars,
+                    phase, pending, taddr, p.status))
+      break;
     // Accumulator rows 64..127 (up) to shared memory, then rows 0..63 (gate) combine.
     if (warp >= 2 && warp < 4) {
       const int r = 32 * warp + lane - 64;
@@ -647,8 +651,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(BatchedParams p)
   for (int nc0 = 0; nc0 < n_e; nc0 += kTcMaxN) {
     const int nv = min(kTcMaxN, n_e - nc0), npad = (nv + 15) & ~15;
     // h rows of this expert's pairs are contiguous: p0 + nc0 + n.
-    tc_product(a_row, p.hh, nullptr, p0 + nc0, nv, npad, p.I, p.I / kTcK, smem, bars, phase,
-               pending, taddr, p.status);
+    if (!tc_product(a_row, p.hh, nullptr, p0 + nc0, nv, npad, p.I, p.I / kTcK, smem, bars, phase,
+                    pending, taddr, p.status))
+      break;
     if (warp < 4) {
       const int r = 32 * warp + lane;
       for (int c8 = 0; c8 < npad; c8 += 8) {
@@ -698,10 +703,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_test_kernel(const __half *a,
                ks > 0 ? 1u : 0u);
     umma_commit(&bars[0]);
   }
-  mbar_wait_bounded(&bars[0], 0, status);
+  const bool ok = !__syncthreads_or(!mbar_wait_bounded(&bars[0], 0, status));
   tc_fence_after();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 4) {
+  if (ok && warp < 4) {   // a timed-out commit leaves the accumulator unread
     for (int c8 = 0; c8 < n; c8 += 8) {
       float v[8];
       tmem_ld8(taddr + (static_cast<uint32_t>(32 * warp) << 16) + c8, v);
@@ -725,6 +730,57 @@ __global__ void __launch_bounds__(256) combine_kernel(BatchedParams p) {
     acc = fmaf(__ldcg(p.wts + t * p.k + r), __ldcg(p.y + static_cast<size_t>(q) * p.H + j), acc);
   }
   p.routed[static_cast<size_t>(t) * p.H + j] = __float2bfloat16_rn(acc);
+}
+
+// Test export: the exact integer block sums of the batched helpers for
+// n_vec activation vectors (the "tokens"), each super-block's code words
+// loaded once for all of them, as the grouped kernels do: whole super-blocks
+// (gate/up) or halves (down). out int32 [n_vec][rows][k / 32].
+__global__ void tokens_block_dots_kernel(const uint8_t *w, int rows, int k, const uint8_t *a,
+                                         int n_vec, int halves, int32_t *out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nsb = k / kQKK, nb = k / 32, rec = tile_record_bytes(k);
+  for (int t = 0; t < n_vec; ++t)
+    tile_from_q8_1(a + static_cast<size_t>(t) * nb * kQ81Bytes, k, tile_at(smem + t * rec, k));
+  const int r = blockIdx.x;
+  for (int sb = threadIdx.x; sb < nsb; sb += blockDim.x) {
+    const uint4 *wv = reinterpret_cast<const uint4 *>(w + (static_cast<size_t>(r) * nsb + sb) * kQ4KBytes);
+    int32_t *o = out + static_cast<size_t>(r) * nb + 8 * sb;
+    if (!halves) {
+      uint32_t qw[32];
+      q4k_sb_words(wv, qw);
+      for (int t = 0; t < n_vec; ++t) {
+        int isum[8];
+        q4k_sb_token_isums(qw, reinterpret_cast<const uint4 *>(smem + t * rec + sb * kActSbStride), isum);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[static_cast<size_t>(t) * rows * nb + j] = isum[j];
+      }
+    } else {
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t qw[16];
+        q4k_half_words(wv, h, qw);
+        for (int t = 0; t < n_vec; ++t) {
+          int isum[4];
+          q4k_half_token_isums(qw, reinterpret_cast<const uint4 *>(smem + t * rec + sb * kActSbStride), h,
+                               isum);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[static_cast<size_t>(t) * rows * nb + 4 * h + j] = isum[j];
+        }
+      }
+    }
+  }
+}
+
+si_status batched_test_dots(const void *w, int rows, int k, const void *a, int n_vec, int halves,
+                            int32_t *out, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(n_vec) * tile_record_bytes(k);
+  cudaError_t e = allow_smem(tokens_block_dots_kernel, smem);
+  if (e == cudaSuccess)
+    e = launch_pdl(tokens_block_dots_kernel, dim3(rows), dim3(128), smem, s,
+                   static_cast<const uint8_t *>(w), rows, k, static_cast<const uint8_t *>(a), n_vec,
+                   halves, out);
+  return cuda_status(e);
 }
 
 // ---------------------------------------------------------------------------

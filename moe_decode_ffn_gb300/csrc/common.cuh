@@ -299,6 +299,23 @@ SI_DEV void quantize_to_tile(const T *x, int n, ActTile t) {
   __syncthreads();
 }
 
+// Fill an ActTile from Q8_1 blocks in global memory (36-byte blocks), all
+// threads of the block cooperating. Ends with __syncthreads().
+SI_DEV void tile_from_q8_1(const uint8_t *src, int n, ActTile t) {
+  const int words = n / 32 * 9;
+  for (int i = threadIdx.x; i < words; i += blockDim.x) {
+    const int blk = i / 9, w = i % 9;
+    const uint32_t v = __ldcg(reinterpret_cast<const uint32_t *>(src + blk * kQ81Bytes) + w);
+    if (w == 0) {
+      t.d[blk] = half_bits_to_float(static_cast<uint16_t>(v & 0xFFFF));
+      t.s[blk] = half_bits_to_float(static_cast<uint16_t>(v >> 16));
+    } else {
+      *reinterpret_cast<uint32_t *>(t.qs + (blk >> 3) * kActSbStride + (blk & 7) * 32 + 4 * (w - 1)) = v;
+    }
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // Q4_K super-block x Q8_1 activations.
 // w: the 144-byte super-block (16-byte aligned, shared memory);
@@ -317,6 +334,31 @@ SI_DEV void q4k_unpack_scales(const uint32_t sw[3], int sc[8], int mn[8]) {
   }
 }
 
+// Exact int32 sums of one pair of Q4_K sub-blocks with their activation
+// codes: sub-block 2p is the low nibbles, 2p + 1 the high nibbles of the
+// pair's 32 code bytes (qw, 8 little-endian words); a points at the pair's 64
+// activation codes (sub-block 2p, then 2p + 1). Every Q4_K dot of the library
+// reduces its codes through this one function.
+SI_DEV void q4k_pair_isums(const uint32_t *qw, const uint4 *a, int &lo, int &hi) {
+  const uint4 al0 = a[0], al1 = a[1], ah0 = a[2], ah1 = a[3];
+  const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
+  const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
+  lo = 0;
+  hi = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    lo = __dp4a(static_cast<int>(qw[i] & 0x0F0F0F0Fu), static_cast<int>(aw_lo[i]), lo);
+    hi = __dp4a(static_cast<int>((qw[i] >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[i]), hi);
+  }
+}
+
+// The 8 code words of pair p of a Q4_K super-block w (16-byte aligned).
+SI_DEV void q4k_pair_words(const uint4 *w, int p, uint32_t qw[8]) {
+  const uint4 q0 = w[1 + 2 * p], q1 = w[2 + 2 * p];
+  qw[0] = q0.x; qw[1] = q0.y; qw[2] = q0.z; qw[3] = q0.w;
+  qw[4] = q1.x; qw[5] = q1.y; qw[6] = q1.z; qw[7] = q1.w;
+}
+
 SI_DEV void q4k_isums(const uint4 *w, const uint4 *a, int isum[8], uint32_t &dd,
                       uint32_t sw[3]) {
   uint4 h = w[0];  // d, dmin, scale bytes 0..11
@@ -324,20 +366,21 @@ SI_DEV void q4k_isums(const uint4 *w, const uint4 *a, int isum[8], uint32_t &dd,
   sw[0] = h.y; sw[1] = h.z; sw[2] = h.w;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    const uint4 q0 = w[1 + 2 * p], q1 = w[2 + 2 * p];     // 32 code bytes of pair p
-    const uint4 al0 = a[4 * p + 0], al1 = a[4 * p + 1];   // sub-block 2p
-    const uint4 ah0 = a[4 * p + 2], ah1 = a[4 * p + 3];   // sub-block 2p+1
-    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
-    const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
-    int lo = 0, hi = 0;
+    uint32_t qw[8];
+    q4k_pair_words(w, p, qw);
+    q4k_pair_isums(qw, a + 4 * p, isum[2 * p], isum[2 * p + 1]);
+  }
+}
+
+// Half h of a Q4_K super-block (sub-blocks 4h .. 4h + 3, 128 weights):
+// isum[i] = exact sum over sub-block 4h + i of q_w * q_a.
+SI_DEV void q4k_half_isums(const uint4 *w, const uint4 *a, int h, int isum[4]) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      lo = __dp4a(static_cast<int>(qw[i] & 0x0F0F0F0Fu), static_cast<int>(aw_lo[i]), lo);
-      hi = __dp4a(static_cast<int>((qw[i] >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[i]), hi);
-    }
-    isum[2 * p] = lo;
-    isum[2 * p + 1] = hi;
+  for (int pp = 0; pp < 2; ++pp) {
+    const int p = 2 * h + pp;
+    uint32_t qw[8];
+    q4k_pair_words(w, p, qw);
+    q4k_pair_isums(qw, a + 4 * p, isum[2 * pp], isum[2 * pp + 1]);
   }
 }
 
@@ -355,19 +398,10 @@ static __device__ __noinline__ float q4k_dot_pairs(const uint8_t *w, const uint8
   const uint8_t *sb = w + 4;   // the 12 scale bytes
 #pragma unroll 1
   for (int p = p0; p < p0 + np; ++p) {
-    const uint4 q0 = *reinterpret_cast<const uint4 *>(w + 16 + 32 * p);
-    const uint4 q1 = *reinterpret_cast<const uint4 *>(w + 32 + 32 * p);
-    const uint4 *ap = reinterpret_cast<const uint4 *>(a + 64 * p);
-    const uint4 al0 = ap[0], al1 = ap[1], ah0 = ap[2], ah1 = ap[3];
-    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
-    const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
-    int lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      lo = __dp4a(static_cast<int>(qw[i] & 0x0F0F0F0Fu), static_cast<int>(aw_lo[i]), lo);
-      hi = __dp4a(static_cast<int>((qw[i] >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[i]), hi);
-    }
+    uint32_t qw[8];
+    q4k_pair_words(reinterpret_cast<const uint4 *>(w), p, qw);
+    int lo, hi;
+    q4k_pair_isums(qw, reinterpret_cast<const uint4 *>(a) + 4 * p, lo, hi);
     // 6-bit scale and min of sub-blocks j = 2p, 2p + 1 (j < 4: low 6 bits of
     // bytes j, j + 4; j >= 4: nibbles of byte j + 4 plus the top 2 bits of
     // bytes j - 4, j)
@@ -410,26 +444,13 @@ SI_DEV float q4k_half_dot(const uint4 *w, const uint4 *a, const float *da, const
     sc[i] = h ? sc8[4 + i] : sc8[i];
     mn[i] = h ? mn8[4 + i] : mn8[i];
   }
+  int isum[4];
+  q4k_half_isums(w, a, h, isum);
   float acc_d = 0.f, acc_m = 0.f;
 #pragma unroll
-  for (int pp = 0; pp < 2; ++pp) {
-    const int p = 2 * h + pp;
-    const uint4 q0 = w[1 + 2 * p], q1 = w[2 + 2 * p];
-    const uint4 al0 = a[4 * p + 0], al1 = a[4 * p + 1];
-    const uint4 ah0 = a[4 * p + 2], ah1 = a[4 * p + 3];
-    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const uint32_t aw_lo[8] = {al0.x, al0.y, al0.z, al0.w, al1.x, al1.y, al1.z, al1.w};
-    const uint32_t aw_hi[8] = {ah0.x, ah0.y, ah0.z, ah0.w, ah1.x, ah1.y, ah1.z, ah1.w};
-    int lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      lo = __dp4a(static_cast<int>(qw[i] & 0x0F0F0F0Fu), static_cast<int>(aw_lo[i]), lo);
-      hi = __dp4a(static_cast<int>((qw[i] >> 4) & 0x0F0F0F0Fu), static_cast<int>(aw_hi[i]), hi);
-    }
-    acc_d = fmaf(static_cast<float>(sc[2 * pp] * lo), da[2 * p], acc_d);
-    acc_d = fmaf(static_cast<float>(sc[2 * pp + 1] * hi), da[2 * p + 1], acc_d);
-    acc_m = fmaf(static_cast<float>(mn[2 * pp]), sa[2 * p], acc_m);
-    acc_m = fmaf(static_cast<float>(mn[2 * pp + 1]), sa[2 * p + 1], acc_m);
+  for (int i = 0; i < 4; ++i) {
+    acc_d = fmaf(static_cast<float>(sc[i] * isum[i]), da[4 * h + i], acc_d);
+    acc_m = fmaf(static_cast<float>(mn[i]), sa[4 * h + i], acc_m);
   }
   const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
   const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
@@ -457,21 +478,11 @@ SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const f
 // (sub-blocks 4h..4h+3): the Q4_K half dot with each code's fifth bit (bit j
 // of qh[i] for element i of sub-block j) OR-ed in as 16 before the dp4a.
 constexpr int kQ5KBytes = 176;
-SI_DEV float q5k_half_dot(const uint8_t *w, const uint4 *a, const float *da, const float *sa, int h) {
-  const uint4 hd = *reinterpret_cast<const uint4 *>(w);
-  int sc8[8], mn8[8];
-  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
-  q4k_unpack_scales(sw, sc8, mn8);
-  int sc[4], mn[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    sc[i] = h ? sc8[4 + i] : sc8[i];
-    mn[i] = h ? mn8[4 + i] : mn8[i];
-  }
+// isum[i] = exact sum over sub-block 4h + i of q_w * q_a (q_w in 0..31).
+SI_DEV void q5k_half_isums(const uint8_t *w, const uint4 *a, int h, int isum[4]) {
   const uint4 qh0 = *reinterpret_cast<const uint4 *>(w + 16);
   const uint4 qh1 = *reinterpret_cast<const uint4 *>(w + 32);
   const uint32_t qhw[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
-  float acc_d = 0.f, acc_m = 0.f;
 #pragma unroll
   for (int pp = 0; pp < 2; ++pp) {
     const int p = 2 * h + pp;
@@ -490,10 +501,29 @@ SI_DEV float q5k_half_dot(const uint8_t *w, const uint4 *a, const float *da, con
       lo = __dp4a(static_cast<int>((qw[i] & 0x0F0F0F0Fu) | b_lo), static_cast<int>(aw_lo[i]), lo);
       hi = __dp4a(static_cast<int>(((qw[i] >> 4) & 0x0F0F0F0Fu) | b_hi), static_cast<int>(aw_hi[i]), hi);
     }
-    acc_d = fmaf(static_cast<float>(sc[2 * pp] * lo), da[2 * p], acc_d);
-    acc_d = fmaf(static_cast<float>(sc[2 * pp + 1] * hi), da[2 * p + 1], acc_d);
-    acc_m = fmaf(static_cast<float>(mn[2 * pp]), sa[2 * p], acc_m);
-    acc_m = fmaf(static_cast<float>(mn[2 * pp + 1]), sa[2 * p + 1], acc_m);
+    isum[2 * pp] = lo;
+    isum[2 * pp + 1] = hi;
+  }
+}
+
+SI_DEV float q5k_half_dot(const uint8_t *w, const uint4 *a, const float *da, const float *sa, int h) {
+  const uint4 hd = *reinterpret_cast<const uint4 *>(w);
+  int sc8[8], mn8[8];
+  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
+  q4k_unpack_scales(sw, sc8, mn8);
+  int sc[4], mn[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    sc[i] = h ? sc8[4 + i] : sc8[i];
+    mn[i] = h ? mn8[4 + i] : mn8[i];
+  }
+  int isum[4];
+  q5k_half_isums(w, a, h, isum);
+  float acc_d = 0.f, acc_m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc_d = fmaf(static_cast<float>(sc[i] * isum[i]), da[4 * h + i], acc_d);
+    acc_m = fmaf(static_cast<float>(mn[i]), sa[4 * h + i], acc_m);
   }
   const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
   const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));

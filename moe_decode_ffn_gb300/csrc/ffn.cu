@@ -85,22 +85,6 @@ SI_DEV int load_expert(const int32_t *ids, int r, int E, uint32_t *status) {
   return e;
 }
 
-// Fill an ActTile from Q8_1 blocks in global memory (36-byte blocks).
-SI_DEV void tile_from_q8_1(const uint8_t *src, int n, ActTile t) {
-  const int words = n / 32 * 9;
-  for (int i = threadIdx.x; i < words; i += blockDim.x) {
-    const int blk = i / 9, w = i % 9;
-    const uint32_t v = __ldcg(reinterpret_cast<const uint32_t *>(src + blk * kQ81Bytes) + w);
-    if (w == 0) {
-      t.d[blk] = half_bits_to_float(static_cast<uint16_t>(v & 0xFFFF));
-      t.s[blk] = half_bits_to_float(static_cast<uint16_t>(v >> 16));
-    } else {
-      *reinterpret_cast<uint32_t *>(t.qs + (blk >> 3) * kActSbStride + (blk & 7) * 32 + 4 * (w - 1)) = v;
-    }
-  }
-  __syncthreads();
-}
-
 template <int SFMT>
 SI_DEV float row_dot_q(const uint8_t *row, bool shared, int nsb, int lane8, const ActTile &a) {
   float acc = 0.f;
@@ -636,6 +620,43 @@ __global__ void q4k_block_dots_kernel(const uint8_t *w, int rows, int k, const u
   }
 }
 
+// Test export: exact per-(vector, row, 32-block) integer sums of the
+// single-token helpers: whole Q4_K super-blocks (gate/up), Q4_K halves
+// (routed and shared down) or Q5_K halves (the Q5_K routed down).
+__global__ void block_dots_kernel(int kind, const uint8_t *w, int rows, int k, const uint8_t *a,
+                                  int32_t *out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nsb = k / kQKK, nb = k / 32;
+  ActTile t;
+  t.qs = smem;
+  t.d = reinterpret_cast<float *>(smem + nsb * kActSbStride);
+  t.s = t.d + nb;
+  tile_from_q8_1(a + static_cast<size_t>(blockIdx.y) * nb * kQ81Bytes, k, t);
+  const int r = blockIdx.x;
+  const int sbb = kind == SI_TEST_DOTS_Q5K_HALF ? kQ5KBytes : kQ4KBytes;
+  int32_t *o = out + (static_cast<size_t>(blockIdx.y) * rows + r) * nb;
+  for (int sb = threadIdx.x; sb < nsb; sb += blockDim.x) {
+    const uint8_t *wb = w + (static_cast<size_t>(r) * nsb + sb) * sbb;
+    const uint4 *av = reinterpret_cast<const uint4 *>(t.qs + sb * kActSbStride);
+    if (kind == SI_TEST_DOTS_Q4K_SB) {
+      int isum[8];
+      uint32_t dd, sw[3];
+      q4k_isums(reinterpret_cast<const uint4 *>(wb), av, isum, dd, sw);
+      for (int j = 0; j < 8; ++j) o[8 * sb + j] = isum[j];
+    } else {
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        int isum[4];
+        if (kind == SI_TEST_DOTS_Q4K_HALF)
+          q4k_half_isums(reinterpret_cast<const uint4 *>(wb), av, h, isum);
+        else
+          q5k_half_isums(wb, av, h, isum);
+        for (int j = 0; j < 4; ++j) o[8 * sb + 4 * h + j] = isum[j];
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -876,6 +897,29 @@ extern "C" si_status si_test_q4k_block_dots(const void *w, int rows, int k, cons
     e = launch_pdl(q4k_block_dots_kernel, dim3(rows), dim3(128), smem,
                    static_cast<cudaStream_t>(stream), static_cast<const uint8_t *>(w), rows, k,
                    static_cast<const uint8_t *>(a_q8_1), out);
+  return cuda_status(e);
+}
+
+extern "C" si_status si_test_block_dots(int kind, const void *w, int rows, int k, const void *a_q8_1,
+                                        int n_vec, int32_t *out, void *stream) {
+  if (kind < SI_TEST_DOTS_Q4K_SB || kind > SI_TEST_DOTS_Q4K_HALF_TOKENS) return SI_ERR_INVALID_ARG;
+  if (!w || !a_q8_1 || !out || rows < 1 || rows > 65535 || k < 256 || k % 256 || k > 16384 ||
+      n_vec < 1)
+    return SI_ERR_INVALID_ARG;
+  if (!aligned16(w) || (reinterpret_cast<uintptr_t>(a_q8_1) & 3u) ||
+      (reinterpret_cast<uintptr_t>(out) & 3u))
+    return SI_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kind >= SI_TEST_DOTS_Q4K_SB_TOKENS) {
+    if (n_vec > 8) return SI_ERR_INVALID_ARG;
+    return batched_test_dots(w, rows, k, a_q8_1, n_vec, kind == SI_TEST_DOTS_Q4K_HALF_TOKENS, out, s);
+  }
+  if (n_vec > 65535) return SI_ERR_INVALID_ARG;
+  const size_t smem = (k / 256) * (kActSbStride + 64);
+  cudaError_t e = allow_smem(block_dots_kernel, smem);
+  if (e == cudaSuccess)
+    e = launch_pdl(block_dots_kernel, dim3(rows, n_vec), dim3(128), smem, s, kind,
+                   static_cast<const uint8_t *>(w), rows, k, static_cast<const uint8_t *>(a_q8_1), out);
   return cuda_status(e);
 }
 

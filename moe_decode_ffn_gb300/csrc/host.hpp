@@ -99,6 +99,10 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
                      const float *wts, void *routed, void *shared, void *ws, uint32_t *status,
                      cudaStream_t s, bool gateup_only = false);
 
+// ---- test export of the batched helpers' integer block sums (batched.cu)
+si_status batched_test_dots(const void *w, int rows, int k, const void *a, int n_vec, int halves,
+                            int32_t *out, cudaStream_t s);
+
 // ---- residual norm
 si_status norm_launch(const void *a, const void *b, const void *c, const void *w, int n, int rows,
                       float eps, void *sum_out, void *norm_out, void *q8_out, cudaStream_t s);

@@ -375,11 +375,17 @@ extern "C" int si_trace_reset_router(void) {
 // memory. The scratch (status word, completion counters, epochs and the
 // tagged logits) lives in this file-scope device array instead of a caller
 // workspace; every GPU that loads the library holds it until the process
-// exits. It is sized for n_tokens * n_experts <= kNoAllocMaxEntries.
+// exits. It is sized for every accepted shape: n_tokens * n_experts <=
+// kNoAllocMaxEntries, with n_experts >= 8, so at most 2048 tokens and 256
+// token chunks (status header, counters and epochs of 256 chunks, tagged
+// logits of 16384 entries: 133,376 bytes).
 // ---------------------------------------------------------------------------
 namespace si {
 constexpr int kNoAllocMaxEntries = 64 * 256;
-constexpr size_t kNoAllocScratchBytes = 3 * 256 + sizeof(uint2) * kNoAllocMaxEntries;
+constexpr int kNoAllocMaxChunks = kNoAllocMaxEntries / 8 / kMaxChunkTokens;
+constexpr size_t kNoAllocScratchBytes = sizeof(WsHeader) + 2 * ((4 * kNoAllocMaxChunks + 255) / 256 * 256) +
+                                        sizeof(uint2) * kNoAllocMaxEntries;
+static_assert(kNoAllocScratchBytes == 133376, "no-alloc scratch size");
 static __device__ __align__(256) uint8_t g_router_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array for the current device. The first call
@@ -424,9 +430,28 @@ extern "C" si_status si_moe_router_topk_noalloc(const void *x, si_dtype x_type, 
   si_status st = noalloc_scratch(&scratch);
   if (st != SI_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents: the status word and the
-  // completion counters must start at zero (the epochs may keep counting).
-  if (cudaMemsetAsync(scratch, 0, g.off_flags, s) != cudaSuccess) return SI_ERR_CUDA;
+  // The array keeps the previous call's contents: the completion counters
+  // must start at zero (the epochs may keep counting, and the status word
+  // keeps the first device-side error until si_moe_router_noalloc_status
+  // reads it).
+  if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + g.off_counters, 0,
+                      g.off_flags - g.off_counters, s) != cudaSuccess)
+    return SI_ERR_CUDA;
   return router_launch(x, x_type, w_router, w_type, hidden, n_experts, top_k, n_tokens, topk_ids,
                        topk_w, logits_out, scratch, static_cast<uint32_t *>(scratch), s);
+}
+
+extern "C" si_status si_moe_router_noalloc_status(void *stream, int *status_out) {
+  if (!status_out) return SI_ERR_INVALID_ARG;
+  void *scratch = nullptr;
+  si_status st = noalloc_scratch(&scratch);
+  if (st != SI_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && v != 0) e = cudaMemset(scratch, 0, sizeof(v));
+  if (e != cudaSuccess) return SI_ERR_CUDA;
+  *status_out = static_cast<int>(v);
+  return SI_OK;
 }

@@ -109,6 +109,15 @@ def q4_k_block_dots(w_rows, a: dict) -> np.ndarray:
     return np.einsum("rsji,sji->rsj", q, qa).reshape(rows, nsb * 8)
 
 
+def q5_k_block_dots(w_rows, a: dict) -> np.ndarray:
+    """The same for Q5_K rows (5-bit codes 0..31): uint8 [rows, K/256*176] ->
+    int64 [rows, K/32]."""
+    _, _, _, _, q = F.q5_k_fields(F.q5_k_rows(w_rows))          # [rows, nsb, 8, 32]
+    rows, nsb = q.shape[0], q.shape[1]
+    qa = a["q"].reshape(nsb, 8, 32)
+    return np.einsum("rsji,sji->rsj", q, qa).reshape(rows, nsb * 8)
+
+
 def matvec_q4_k(w_rows, a: dict) -> np.ndarray:
     """Q4_K weights x Q8_1 activations, integer mode. For row r and 32-block b
     (sub-block j of super-block s): acc += d*sc_j*d_a(b)*sum_i q_w q_a

@@ -30,6 +30,39 @@ def test_q4k_block_dots_bit_exact(rows, k):
     assert np.array_equal(got, M.q4_k_block_dots(w.numpy(), a))
 
 
+# (kind, format, rows, k, vectors): the full gate/up (H = 2048) and down
+# (I = 512 and 768) shapes of the studied layers, for every integer helper.
+BLOCK_DOT_CASES = [
+    (m.SI_TEST_DOTS_Q4K_SB, "q4_k", 512, 2048, 2),
+    (m.SI_TEST_DOTS_Q4K_SB, "q4_k", 768, 2048, 1),
+    (m.SI_TEST_DOTS_Q4K_HALF, "q4_k", 2048, 512, 2),
+    (m.SI_TEST_DOTS_Q4K_HALF, "q4_k", 2048, 768, 1),
+    (m.SI_TEST_DOTS_Q5K_HALF, "q5_k", 2048, 512, 2),
+    (m.SI_TEST_DOTS_Q5K_HALF, "q5_k", 2048, 768, 1),
+    (m.SI_TEST_DOTS_Q4K_SB_TOKENS, "q4_k", 768, 2048, 8),
+    (m.SI_TEST_DOTS_Q4K_SB_TOKENS, "q4_k", 512, 2048, 3),
+    (m.SI_TEST_DOTS_Q4K_HALF_TOKENS, "q4_k", 2048, 768, 8),
+    (m.SI_TEST_DOTS_Q4K_HALF_TOKENS, "q4_k", 2048, 512, 5),
+]
+
+
+@pytest.mark.parametrize("kind,fmt,rows,k,nv", BLOCK_DOT_CASES)
+def test_integer_block_dots_of_every_helper_bit_exact(kind, fmt, rows, k, nv):
+    """Every integer dot helper (gate/up super-blocks, down halves, Q5_K
+    halves, the batched forms that reuse a super-block's code words for
+    several tokens) gives the oracle's exact int32 block sums."""
+    w = gen.encode(gen.float_weights(17, kind, gen.ROLE_DOWN, rows, rows, k), fmt)
+    # activations of both signs with a few blocks at full scale and one all-zero block
+    x = gen.normal([gen.stream_key(18, kind, k, v) for v in range(nv)], k, 0.0, 1.0)
+    x[:, 32:64] = 0.0
+    acts = [F.q8_1_quantize(x[v].numpy()) for v in range(nv)]
+    a_bytes = torch.from_numpy(np.concatenate([F.q8_1_to_bytes(a).reshape(-1) for a in acts]))
+    got = m.si_test_block_dots(kind, w.cuda(), rows, k, a_bytes.cuda(), nv).cpu().numpy()
+    dots = M.q5_k_block_dots if fmt == "q5_k" else M.q4_k_block_dots
+    for v in range(nv):
+        assert np.array_equal(got[v], dots(w.numpy(), acts[v])), v
+
+
 def _routing(seed, spec):
     """Seeded distinct expert ids and softmax weights (inputs of the FFN call)."""
     keys = gen.raw64([gen.stream_key(seed, 999)], spec.n_experts)[0]

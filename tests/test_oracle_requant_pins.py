@@ -169,3 +169,23 @@ def test_requant_of_q8_0_and_q5_k_stays_within_the_q4_k_bound():
     x4 = F.fp32(M.dequant_rows("q4_k", q4)).astype(np.float32)
     assert np.array_equal(F.q4_k_quantize(x4), F.q4_k_quantize(F.fp32(
         M.dequant_rows("q4_k", F.q4_k_quantize(x4))).astype(np.float32)))
+
+
+def test_q5_k_block_dots_brute_force():
+    """Integer block sums of Q5_K rows, element by element from the bytes:
+    code = low or high nibble (sub-block parity) + 16 * bit j of qh[i]."""
+    rng = np.random.default_rng(31)
+    w = gen.encode_q5_k(gen.float_weights(6, 0, gen.ROLE_DOWN, 1, 3, 512)).numpy()
+    a = F.q8_1_quantize(rng.standard_normal(512).astype(np.float32))
+    got = M.q5_k_block_dots(w, a)
+    for r in range(3):
+        for b in range(16):
+            sb, j = divmod(b, 8)
+            base = sb * 176
+            tot = 0
+            for i in range(32):
+                byte = int(w[r, base + 48 + 32 * (j // 2) + i])
+                code = (byte & 15) if j % 2 == 0 else (byte >> 4)
+                code += 16 * ((int(w[r, base + 16 + i]) >> j) & 1)
+                tot += code * int(a["q"][b, i])
+            assert got[r, b] == tot

@@ -113,15 +113,25 @@ SI_DEV uint64_t now_ns() {
   return t;
 }
 
-// Wait for phase `parity` of `bar` for at most `budget_ns`. Returns false on
-// timeout (after recording SI_ERR_TIMEOUT). The spin loop is out of line so
-// that every call site stays one try_wait long.
+// Reading %globaltimer stalls the reading thread for about half a
+// microsecond on GB300, longer than most of the waits below: every bounded
+// wait therefore spins a fixed number of times before it first reads the
+// clock, and then reads it only between long runs of attempts.
+constexpr int kSpinBeforeClock = 4096;
+
+// Wait for phase `parity` of `bar` for at most about `budget_ns` (plus the
+// initial spin). Returns false on timeout (after recording SI_ERR_TIMEOUT).
+// The spin loop is out of line so that every call site stays one try_wait
+// long.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
                                                    uint32_t *status, uint64_t budget_ns) {
+#pragma unroll 1
+  for (int i = 0; i < kSpinBeforeClock; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = now_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (now_ns() - t0 > budget_ns) break;
   }
@@ -237,16 +247,14 @@ SI_DEV void q8_1_encode_4lanes(const float v[8], uint32_t &q_lo, uint32_t &q_hi,
 // block (lane i = value i). One division per lane keeps the dependent chain
 // short. Returns this lane's code; d16 / s16 identical on every lane.
 SI_DEV int q8_1_encode_warp(float v, uint16_t &d16, uint16_t &s16) {
-  float amax = fabsf(v);
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  // |v| as bits orders like the values (non-negative floats), so one warp
+  // reduction gives amax; a second gives the exact integer sum of the codes
+  const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
   const float d = __fdiv_rn(amax, 127.0f);
   const bool live = d > 0.f;
   const float r = fminf(fmaxf(roundf(__fdiv_rn(v, live ? d : 1.0f)), -127.f), 127.f);
   const int q = live ? static_cast<int>(r) : 0;
-  int sum = q;
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+  const int sum = __reduce_add_sync(0xffffffffu, q);
   d16 = float_to_half_bits(d);
   s16 = float_to_half_bits(__fmul_rn(d, static_cast<float>(sum)));
   return q;
@@ -432,29 +440,51 @@ static __device__ __noinline__ float q4k_dot_pairs(const uint8_t *w, const uint8
 // once per launch (their code is fetched once): half of a super-block
 // (sub-blocks 4h..4h+3, 128 weights) and the whole super-block. Same order of
 // accumulation and rounding as q4k_dot_pairs, so the same bits.
-SI_DEV float q4k_half_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa,
-                          int h) {
+//
+// A half taken apart ahead of its dot product: the 16 code words of its two
+// pairs, the 6-bit scales and mins of its four sub-blocks (packed one per
+// byte), d and dmin. The scales of sub-blocks 4..7 are their low nibble in
+// bytes 8..11 plus the top two bits of bytes 0..3 (mins: high nibble, bytes
+// 4..7), so all four come out of three words with a few masks.
+struct Q4KHalf {
+  uint32_t qw[16];
+  uint32_t scw, mnw;
+  float d, dmin;
+};
+SI_DEV void q4k_half_load(const uint4 *w, int h, Q4KHalf &q) {
   const uint4 hd = w[0];
-  int sc8[8], mn8[8];
-  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
-  q4k_unpack_scales(sw, sc8, mn8);
-  int sc[4], mn[4];   // this half's four sub-blocks (selects, no runtime indexing)
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    sc[i] = h ? sc8[4 + i] : sc8[i];
-    mn[i] = h ? mn8[4 + i] : mn8[i];
+  if (h) {
+    q.scw = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+    q.mnw = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+  } else {
+    q.scw = hd.y & 0x3F3F3F3Fu;
+    q.mnw = hd.z & 0x3F3F3F3Fu;
   }
+  q4k_pair_words(w, 2 * h, q.qw);
+  q4k_pair_words(w, 2 * h + 1, q.qw + 8);
+  q.d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+  q.dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
+}
+SI_DEV float q4k_half_dot_loaded(const Q4KHalf &q, const uint4 *a, const float *da, const float *sa,
+                                 int h) {
   int isum[4];
-  q4k_half_isums(w, a, h, isum);
+  q4k_pair_isums(q.qw, a + 4 * (2 * h), isum[0], isum[1]);
+  q4k_pair_isums(q.qw + 8, a + 4 * (2 * h + 1), isum[2], isum[3]);
   float acc_d = 0.f, acc_m = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    acc_d = fmaf(static_cast<float>(sc[i] * isum[i]), da[4 * h + i], acc_d);
-    acc_m = fmaf(static_cast<float>(mn[i]), sa[4 * h + i], acc_m);
+    const int sc = static_cast<int>((q.scw >> (8 * i)) & 0xFFu);
+    const int mn = static_cast<int>((q.mnw >> (8 * i)) & 0xFFu);
+    acc_d = fmaf(static_cast<float>(sc * isum[i]), da[4 * h + i], acc_d);
+    acc_m = fmaf(static_cast<float>(mn), sa[4 * h + i], acc_m);
   }
-  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
-  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
-  return __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
+  return __fsub_rn(__fmul_rn(q.d, acc_d), __fmul_rn(q.dmin, acc_m));
+}
+SI_DEV float q4k_half_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa,
+                          int h) {
+  Q4KHalf q;
+  q4k_half_load(w, h, q);
+  return q4k_half_dot_loaded(q, a, da, sa, h);
 }
 
 SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa) {

@@ -230,14 +230,15 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
   SI_TRACE_MARK(0, 6);
 }
 
-// Rows per block R and warps per row W (R * W = 8): R large enough that the
-// chunk has at most ~160 blocks (one wave on a 152-SM GB300), W such that
-// every warp holds whole 16-byte vectors of the row.
+// Rows per block R and warps per row W (R * W = 8): one row per block with
+// its 16-byte vectors dealt to the 256 lanes of all 8 warps (vector
+// c * 256 + 32 w + lane to lane `lane` of warp w), the order in which the
+// persistent stack kernel forms the same dot products, so both give the same
+// bits; fewer warps per row only when the row has fewer than 256 vectors.
 static void router_shape(int n_experts, int hidden, int vec, int &R, int &W, int &nch) {
-  int rmin = 1;
-  while ((n_experts + rmin - 1) / rmin > 160 && rmin < 8) rmin *= 2;
+  (void)n_experts;
   const int nv = hidden / vec;
-  W = 8 / rmin;
+  W = 8;
   while (W > 1 && nv % (32 * W) != 0) W /= 2;
   R = 8 / W;
   nch = nv / (32 * W);

@@ -49,7 +49,22 @@ SI_TRACE_BUFFER
 constexpr int kStkThreads = 512;
 constexpr int kSlot = 16;           // u64 elements per 128-byte slot
 constexpr int kStkFixedBytes = 2048;
-constexpr int kArmT = 480;          // the thread that arms every barrier (warp 15, lane 0)
+constexpr int kArmT = 480;          // the thread that arms the prefetch barriers (warp 15, lane 0)
+// Every exchange slot is written kXRep times, and block b reads copy b % kXRep:
+// a line polled by every block delays the store that the readers wait for
+// (the polls queue ahead of it at the line's L2 slice), so each copy has only
+// G / kXRep readers. The copies cost one warp-wide store instead of one.
+constexpr int kXRep = 8;
+
+// The 64 rows of a gate/up unit arrive in kGuGroups groups of 32 / kGuGroups
+// gate rows and as many up rows, one bulk copy per matrix and group.
+constexpr int kGuGroups = 2;
+constexpr int kGuRows = 32 / kGuGroups;
+// mbarriers of a stack block: 0, 1 the routing-independent prefetch (router
+// rows, shared-gate vector, norm weights) by iteration parity; then one per
+// gate/up group of the block's unit; then the routed down rows; then the
+// shared down rows.
+enum { kBarPre = 0, kBarGu = 2, kBarDn = 2 + kGuGroups, kBarSd = 3 + kGuGroups, kNumBars = 4 + kGuGroups };
 
 struct StackLayerPtrs {             // 80 bytes
   const __nv_bfloat16 *w_router, *w_sg, *w_norm;
@@ -70,8 +85,6 @@ struct StackParams {
   int H, E, k, I, Is;         // Is == 0: no shared expert
   int rb, rbd, rbsd;          // row bytes: gate/up rows (H), routed down rows (I), shared down rows
   int J;                      // down output rows per block (even)
-  int W;                      // router: warps per expert row
-  int nch;                    // router: 16-byte vectors per lane
   int np3;                    // X3: pairs of elements per block slot (ceil(J / 4))
   float eps;
   StackSmem sm;
@@ -80,9 +93,9 @@ struct StackParams {
   int32_t *ids_out;           // [T][L][k] or null
   uint32_t *status;
   uint32_t *epoch;            // tag base
-  uint64_t *lg;               // X1 [2][G][kSlot]: {logit row c, logit row c + G}
-  uint64_t *hl;               // X2 [2][units][kSlot]: 8 code words, {d16 | s16 << 16}, pad
-  uint64_t *ol;               // X3 [2][G][kSlot]: bf16 pairs of this block's rows
+  uint64_t *lg;               // X1 [2][kXRep][G][kSlot]: {logit row c, logit row c + G}
+  uint64_t *hl;               // X2 [2][kXRep][units][kSlot]: 8 code words, {d16 | s16 << 16}, pad
+  uint64_t *ol;               // X3 [2][kXRep][G][kSlot]: bf16 pairs of this block's rows
 };
 
 // ---- tagged lines ----------------------------------------------------------
@@ -90,9 +103,6 @@ SI_DEV uint64_t tagged(uint32_t tag, uint32_t payload) {
   return (static_cast<uint64_t>(tag) << 32) | payload;
 }
 SI_DEV bool tag_ok(uint64_t v, uint32_t tag) { return static_cast<uint32_t>(v >> 32) == tag; }
-SI_DEV void st_tag1(uint64_t *p, uint64_t v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 SI_DEV void st_tag2(uint64_t *p, uint64_t a, uint64_t b) {
   asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
@@ -103,15 +113,21 @@ SI_DEV void ld_tag2(const uint64_t *p, uint64_t &a, uint64_t &b) {
 }
 SI_DEV bool pair_ok(uint64_t a, uint64_t b, uint32_t tag) { return tag_ok(a, tag) && tag_ok(b, tag); }
 
-// Re-read the pair at p until both elements carry `tag`, at most
-// kWaitBudgetNs; records SI_ERR_TIMEOUT and returns false if they never do.
-static __device__ __noinline__ bool poll_pair(const uint64_t *p, uint32_t tag, uint64_t &a,
-                                              uint64_t &b, uint32_t *status,
-                                              uint64_t budget_ns = kWaitBudgetNs) {
+// Re-read the pair at p until both elements carry `tag`, for at most about
+// budget_ns after an initial run of kSpinBeforeClock reads (no clock read on
+// the fast path: it would stall the poller longer than a round trip);
+// records SI_ERR_TIMEOUT and returns false if they never do.
+SI_DEV bool poll_pair(const uint64_t *p, uint32_t tag, uint64_t &a, uint64_t &b, uint32_t *status,
+                     uint64_t budget_ns = kWaitBudgetNs) {
+#pragma unroll 1
+  for (int i = 0; i < kSpinBeforeClock; ++i) {
+    ld_tag2(p, a, b);
+    if (pair_ok(a, b, tag)) return true;
+  }
   const uint64_t t0 = now_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 64; ++i) {
       ld_tag2(p, a, b);
       if (pair_ok(a, b, tag)) return true;
     }
@@ -197,27 +213,30 @@ SI_DEV float sigma_dot(const __nv_bfloat16 *w, const float *y, int n, float *red
 
 // ---- copies ---------------------------------------------------------------------
 // Issuing one bulk copy occupies the issuing thread for a few hundred cycles
-// whatever its size, so copies are few and large, and are issued one per
-// warp (lane 0) by warps that have nothing else to do at that moment. One
-// thread (kArmT) arms every barrier (arrive + expected bytes) before a
-// __syncthreads that precedes the copies.
-SI_DEV void arm(uint64_t *bars, int b, uint32_t bytes, uint32_t &armed, uint32_t &used) {
+// whatever its size, and many small copies ramp up more slowly than a few
+// large ones, so copies are few and large and issued one per warp (lane 0)
+// by warps that have nothing else to do at that moment. A barrier is armed
+// (arrive + expected bytes) before any copy completing on it is issued; every
+// arming flips the barrier's bit in `s_arm` (parity of the phases armed so
+// far) and sets its "used" bit, so that an error exit can wait for the last
+// armed phase of each barrier and leave no copy in flight.
+SI_DEV void arm(uint64_t *bars, uint32_t *s_arm, int b, uint32_t bytes) {
   mbar_arrive_expect_tx(&bars[b], bytes);
-  armed ^= 1u << b;
-  used |= 1u << b;
+  atomicXor(s_arm, 1u << b);
+  atomicOr(s_arm, 1u << (16 + b));
 }
 
-// Gather X3 (t = bf16(routed + shared) per row) into `tbuf`, then fold it
-// into the residual: s = bf16(t + resid), y = bf16((s * rsqrt(mean(s^2) +
-// eps)) * w), the norm kernel's arithmetic and order (the first 256 threads
-// own rows 8i..8i+7 of every 2048-row slice). Thread i reads pairs i and
-// i + 512 of the slots: f_src = element offset, f_row = first row, f_n = rows
-// of this block in the pair (0 for a pair that only proves presence).
-// `resid` holds the residual on entry and s on exit. Returns false (in every
-// thread) if a slot did not arrive in time.
-SI_DEV bool fold_norm(const StackParams &p, const uint64_t *ol, uint32_t tag, float *resid,
-                      const __nv_bfloat16 *w, float *y, float *tbuf, float *red,
-                      const int f_src[2], const int f_row[2], const int f_n[2]) {
+// Gather X3 (t = bf16(routed + shared) per row) into `tbuf` and fold it into
+// the residual: s = bf16(t + resid) with the sum of squares in the norm
+// kernel's order (the first 256 threads own rows 8i..8i+7 of every
+// 2048-row slice); returns r = rsqrt(mean(s^2) + eps) in `r` (every thread).
+// Thread i reads pairs i and i + 512 of the slots: f_src = element offset,
+// f_row = first row, f_n = rows of this block in the pair (0 for a pair that
+// only proves presence). `resid` holds the residual on entry and s on exit.
+// Returns false (in every thread) if a slot did not arrive in time.
+SI_DEV bool fold_sum(const StackParams &p, const uint64_t *ol, uint32_t tag, float *resid,
+                     float *tbuf, float *red, const int f_src[2], const int f_row[2], const int f_n[2],
+                     float &r) {
   const int H = p.H;
   bool ok = true;
   uint64_t v[2][2];
@@ -228,7 +247,6 @@ SI_DEV bool fold_norm(const StackParams &p, const uint64_t *ol, uint32_t tag, fl
   for (int s = 0; s < 2; ++s) {
     if (f_src[s] < 0) continue;
     ok &= get_pair(ol + f_src[s], tag, v[s][0], v[s][1], p.status);
-    SI_TRACE_LATEST(0, 13);
     const uint32_t w0 = static_cast<uint32_t>(v[s][0]), w1 = static_cast<uint32_t>(v[s][1]);
     const float tv[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
 #pragma unroll
@@ -258,13 +276,36 @@ SI_DEV bool fold_norm(const StackParams &p, const uint64_t *ol, uint32_t tag, fl
   float tot = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) tot += red[i];
-  const float r = rsqrtf(__fdiv_rn(tot, static_cast<float>(H)) + p.eps);
-#pragma unroll 1
-  for (int i = threadIdx.x; i < H; i += blockDim.x)
-    y[i] = bf16_round(__fmul_rn(__fmul_rn(resid[i], r), __bfloat162float(w[i])));
-  __syncthreads();
+  r = rsqrtf(__fdiv_rn(tot, static_cast<float>(H)) + p.eps);
   return true;
 }
+
+// Phase timing of profiling builds (-DSI_TRACE). A %globaltimer read stalls
+// its thread for about half a microsecond, so a launch stamps only two points
+// of its last iteration (thread 0 of every block): the iteration start
+// (phase 0) and the phase selected with si_trace_stack_phase; phase 14 sits
+// right after phase 0 and measures the stall of a stamp itself. A profiling
+// run takes many launches per phase.
+#ifdef SI_TRACE
+static __device__ int g_stk_trace_phase;
+#define STK_TRACE_START()   \
+  do {                      \
+    STK_TRACE(0);           \
+    STK_TRACE(14);          \
+  } while (0)
+#define STK_TRACE(ph)                                                                     \
+  do {                                                                                    \
+    if (threadIdx.x == 0 && it + 1 == n_iters && ((ph) == 0 || (ph) == tr_sel) && c < kTraceBlocks) \
+      g_si_trace[0][c][(ph)] = now_ns();                                                  \
+  } while (0)
+#else
+#define STK_TRACE_START() \
+  do {                    \
+  } while (0)
+#define STK_TRACE(ph) \
+  do {                \
+  } while (0)
+#endif
 
 template <int SFMT>
 __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
@@ -273,23 +314,26 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   const int G = gridDim.x, c = blockIdx.x;
   const int H = p.H, I = p.I, Is = kShared ? p.Is : 0, k = p.k, E = p.E;
   const int nsb = H / kQKK;
-  const int n_slots = k + (kShared ? 1 : 0);
   const int units_r = k * I / 32, units = units_r + Is / 32;
   const int nsb_r = I / kQKK, nsb_s = Is / kQKK;
   const int P_r = 2 * nsb_r, P_s = kShared ? 2 * nsb_s : 1, P_max = P_r > P_s ? P_r : P_s;
   const int n_iters = p.n_tokens * p.n_layers;
   const int J = p.J;
+  const int nvec = H / 2048;   // router: 16-byte vectors of a row per thread of the first 256
 
+#ifdef SI_TRACE
+  const int tr_sel = g_stk_trace_phase;
+#endif
   // ---- shared memory --------------------------------------------------------
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);   // 0,1 prefetch groups; 2..5 gate/up groups; 6 routed down; 7 shared down
-  uint32_t *s_base = reinterpret_cast<uint32_t *>(smem + 128);
-  float *red = reinterpret_cast<float *>(smem + 144);
-  float *s_part = reinterpret_cast<float *>(smem + 208);
-  float *s_wts = reinterpret_cast<float *>(smem + 240);
-  uint64_t *s_sel = reinterpret_cast<uint64_t *>(smem + 304);
-  uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + 368);
-  float *h_s = reinterpret_cast<float *>(smem + 880);
-  float *s_logit = reinterpret_cast<float *>(smem + 1024);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);     // kNumBars
+  uint32_t *s_arm = reinterpret_cast<uint32_t *>(smem + 64);
+  uint32_t *s_base = reinterpret_cast<uint32_t *>(smem + 68);
+  float *red = reinterpret_cast<float *>(smem + 128);      // [16]
+  float *s_part = reinterpret_cast<float *>(smem + 192);   // [2][8] router partials per warp
+  float *s_wts = reinterpret_cast<float *>(smem + 256);    // [8]
+  uint64_t *s_sel = reinterpret_cast<uint64_t *>(smem + 320);
+  uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + 384);   // [64]
+  float *h_s = reinterpret_cast<float *>(smem + 896);      // [32]
   StackLayerPtrs *s_layers = reinterpret_cast<StackLayerPtrs *>(smem + p.sm.layers);
   float *resid = reinterpret_cast<float *>(smem + p.sm.resid);
   float *y = reinterpret_cast<float *>(smem + p.sm.y);
@@ -311,9 +355,9 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   const int j0 = c * J;
   const int nrows = j0 < H ? min(J, H - j0) : 0;
   const int row_a = c, row_b = c + G;   // router rows of this block
-  const int nrr = (row_a < E ? 1 : 0) + (p.W == 4 && row_b < E ? 1 : 0);
+  const int rep = c % kXRep;            // the copy of every exchange slot this block reads
+  const int nrr = (row_a < E ? 1 : 0) + (row_b < E ? 1 : 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rs = warp / p.W, wpart = warp % p.W;               // router: row, K part
   const int pr = threadIdx.x >> 4, gm = (threadIdx.x >> 3) & 1, lane8 = threadIdx.x & 7;   // gate/up
   const uint64_t pol = policy_evict_first();
   // X2 gather: pair q (5 per unit slot: 4 code pairs, 1 scale pair) ->
@@ -330,11 +374,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     g_dst[s] = sub < 4 ? static_cast<int>(p.sm.ht_qs) + (base_sb + hb / 8) * kActSbStride + (hb % 8) * 32 + 8 * sub
                        : -(u + 1);
   }
-  // down: item (slot r, row jl, half-super-block qq) of this thread
-  int d_row[2], d_act[2], d_blk[2], d_h[2], d_part[2];
+  // down: item (slot r, row jl, half-super-block qq) of this thread in pass s;
+  // the P pieces of a (slot, row) lie in consecutive lanes of one warp, the
+  // first of them (qq == 0) sums them in order
+  int d_row[2], d_act[2], d_blk[2], d_h[2], d_dst[2], d_P[2];
+  bool d_live[2], d_first[2];
+  const int items_r = k * J * P_r;
+  const int items = items_r + (kShared ? J * P_s : 0);
   {
-    const int items_r = k * J * P_r;
-    const int items = items_r + (kShared ? J * P_s : 0);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int u = static_cast<int>(threadIdx.x) + s * kStkThreads;
@@ -351,7 +398,10 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       }
       const bool sh = kShared && r == k;
       const int sb = qq >> 1;
-      d_part[s] = (u < items && jl < nrows) ? (r * J + jl) * P_max + qq : -1;
+      d_live[s] = u < items && jl < nrows;
+      d_first[s] = qq == 0;
+      d_P[s] = sh ? P_s : P_r;
+      d_dst[s] = r * J + jl;
       d_row[s] = (sh ? static_cast<int>(p.sm.sd) + jl * p.rbsd
                      : static_cast<int>(p.sm.dn) + (r * J + jl) * p.rbd) + sb * kQ4KBytes;
       d_act[s] = static_cast<int>(p.sm.ht_qs) + (r * nsb_r + sb) * kActSbStride;
@@ -370,15 +420,12 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     f_row[s] = r0;
     f_n[s] = max(0, min(min(4, J - 4 * m), H - r0));
   }
-  // combine: slot tr, row tj
-  const int tr = static_cast<int>(threadIdx.x) / J, tj = static_cast<int>(threadIdx.x) - tr * J;
-  const bool tlive = static_cast<int>(threadIdx.x) < n_slots * J && tj < nrows;
-  const int tPP = (kShared && tr == k) ? P_s : P_r;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
     *s_base = __ldcg(p.epoch);
+    *s_arm = 0u;
   }
   {
     const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p.layers);
@@ -389,141 +436,168 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   __syncthreads();
   const uint32_t base = *s_base;
 
-  // Thread kArmT: `armed` holds, per barrier, the parity of the number of
-  // phases armed so far, `used` which barriers were ever armed. On an error
-  // exit it waits for the last armed phase of each, so no copy is left in
-  // flight.
-  uint32_t armed = 0u, used = 0u;
   int t = 0, l = 0;   // token and layer of iteration it
   const uint32_t gbytes = static_cast<uint32_t>((nrr + (kShared ? 1 : 0) + 1) * H * 2);
-  const uint32_t gubytes = 8u * p.rb;    // one group: 8 gate (or up) rows
+  const uint32_t cbytes = static_cast<uint32_t>(kGuRows) * p.rb;   // one copy: a group's gate (or up) rows
   if (threadIdx.x == kArmT && n_iters > 0) {
     // iteration 0's routing-independent bytes and shared gate/up unit
     const StackLayerPtrs &L0 = s_layers[0];
-    arm(bars, 0, gbytes, armed, used);
-    if (nrr > 0) bulk_g2s(pbuf, L0.w_router + static_cast<size_t>(row_a) * H, H * 2, &bars[0]);
-    if (nrr > 1) bulk_g2s(pbuf + 2 * H, L0.w_router + static_cast<size_t>(row_b) * H, H * 2, &bars[0]);
-    if (kShared) bulk_g2s(pbuf + 4 * H, L0.w_sg, H * 2, &bars[0]);
-    bulk_g2s(pbuf + 6 * H, L0.w_norm, H * 2, &bars[0]);
+    arm(bars, s_arm, kBarPre, gbytes);
+    if (nrr > 0) bulk_g2s(pbuf, L0.w_router + static_cast<size_t>(row_a) * H, H * 2, &bars[kBarPre]);
+    if (nrr > 1) bulk_g2s(pbuf + 2 * H, L0.w_router + static_cast<size_t>(row_b) * H, H * 2, &bars[kBarPre]);
+    if (kShared) bulk_g2s(pbuf + 4 * H, L0.w_sg, H * 2, &bars[kBarPre]);
+    bulk_g2s(pbuf + 6 * H, L0.w_norm, H * 2, &bars[kBarPre]);
     if (shared_unit) {
       const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32;
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        arm(bars, 2 + g, 2 * gubytes, armed, used);
-        bulk_g2s_evict_first(gu_buf + g * gubytes, L0.wsg + (row0 + 8 * g) * p.rb, gubytes, &bars[2 + g], pol);
-        bulk_g2s_evict_first(gu_buf + (4 + g) * gubytes, L0.wsu + (row0 + 8 * g) * p.rb, gubytes,
-                             &bars[2 + g], pol);
+      for (int g = 0; g < kGuGroups; ++g) {
+        arm(bars, s_arm, kBarGu + g, 2 * cbytes);
+        bulk_g2s_evict_first(gu_buf + kGuRows * g * p.rb, L0.wsg + (row0 + kGuRows * g) * p.rb, cbytes,
+                             &bars[kBarGu + g], pol);
+        bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rb, L0.wsu + (row0 + kGuRows * g) * p.rb,
+                             cbytes, &bars[kBarGu + g], pol);
       }
     }
   }
 
+  float r_norm = 0.f;   // rsqrt(mean(s^2) + eps) of the latest fold
   for (int it = 0;; ++it) {
     const uint32_t tag = base + static_cast<uint32_t>(it) + 1u, par = it & 1u;
-    SI_TRACE_MARK(0, 0);
+    STK_TRACE_START();
     if (threadIdx.x == kArmT && it < n_iters) {   // copies issued during this iteration's logit gather
-      if (it + 1 < n_iters) arm(bars, (it + 1) & 1, gbytes, armed, used);
-      if (kShared && nrows > 0) arm(bars, 7, static_cast<uint32_t>(nrows) * p.rbsd, armed, used);
+      if (it + 1 < n_iters) arm(bars, s_arm, kBarPre + (par ^ 1u), gbytes);
+      if (kShared && nrows > 0) arm(bars, s_arm, kBarSd, static_cast<uint32_t>(nrows) * p.rbsd);
     }
-    // [N] FFN input: the fold of the previous iteration's outputs (at a
-    // token's first layer, those are the previous token's results), or x_in.
+    // [N] the fold of the previous iteration's outputs (at a token's first
+    // layer, those are the previous token's results): resid := s, r_norm
     if (it > 0) {
-      const uint8_t *pb = pbuf + ((it - 1) & 1) * pstr;
-      if (!fold_norm(p, p.ol + static_cast<size_t>((it - 1) & 1) * G * kSlot, tag - 1u, resid,
-                     reinterpret_cast<const __nv_bfloat16 *>(pb + 6 * H), y, tbuf, red, f_src, f_row,
-                     f_n))
+      if (!fold_sum(p, p.ol + (static_cast<size_t>((it - 1) & 1) * kXRep + rep) * G * kSlot, tag - 1u, resid, tbuf, red,
+                    f_src, f_row, f_n, r_norm))
         goto fail;
-      if (l == 0) {
+      if (l == 0) {   // token t - 1 is done: its last norm output and residual
+        const __nv_bfloat16 *wn =
+            reinterpret_cast<const __nv_bfloat16 *>(pbuf + ((it - 1) & 1) * pstr + 6 * H);
 #pragma unroll 1
         for (int i = threadIdx.x; i < nrows; i += blockDim.x) {
-          p.y_out[static_cast<size_t>(t - 1) * H + j0 + i] = __float2bfloat16_rn(y[j0 + i]);
+          const float yv = bf16_round(__fmul_rn(__fmul_rn(resid[j0 + i], r_norm), __bfloat162float(wn[j0 + i])));
+          p.y_out[static_cast<size_t>(t - 1) * H + j0 + i] = __float2bfloat16_rn(yv);
           if (p.sum_out)
             p.sum_out[static_cast<size_t>(t - 1) * H + j0 + i] = __float2bfloat16_rn(resid[j0 + i]);
         }
-        __syncthreads();   // y and resid are overwritten below
+        __syncthreads();   // resid is overwritten below
       }
     }
+#ifdef SI_TRACE
+    if (it == n_iters && threadIdx.x == 0 && tr_sel == 13 && c < kTraceBlocks) g_si_trace[0][c][13] = now_ns();
+#endif
     if (it == n_iters) break;
-    if (l == 0) {
-#pragma unroll 1
-      for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        const float v = __bfloat162float(p.x_in[static_cast<size_t>(t) * H + i]);
-        resid[i] = v;
-        y[i] = v;
-      }
-      __syncthreads();
-    }
-    SI_TRACE_MARK(0, 1);
+    STK_TRACE(1);
 
-    // [R] router rows: W warps per row, vector (i * W + wpart) * 32 + lane
+    // [R] y = this iteration's FFN input (x_in at a token's first layer, else
+    // bf16(s * r * w_norm) with the previous layer's norm weights) and the
+    // router rows' dot products in the same pass: thread i < 256 owns 16-byte
+    // vectors i, i + 256, ... of a row (8 values each)
     {
-      const bool ok = mbar_wait_bounded(&bars[par], (it >> 1) & 1, p.status);
-      if (ok && rs < nrr) {
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(pbuf + par * pstr + rs * 2 * H);
-        float acc = 0.f;
+      bool ok = true;
+      if (threadIdx.x < 256) {
+        ok = mbar_wait_bounded(&bars[kBarPre + par], (it >> 1) & 1, p.status);
+        const uint8_t *pb = pbuf + par * pstr;
+        const __nv_bfloat16 *wn =
+            reinterpret_cast<const __nv_bfloat16 *>(pbuf + (par ^ 1u) * pstr + 6 * H);
+        float acc_a = 0.f, acc_b = 0.f;
 #pragma unroll 1
-        for (int i = 0; i < p.nch; ++i) {
-          const int v = (i * p.W + wpart) * 32 + lane;
-          const uint4 u = wrow[v];
-          float wv[8];
-          Load8<__nv_bfloat16>::run(&u, wv);
-          const float4 y0 = *reinterpret_cast<const float4 *>(y + 8 * v);
-          const float4 y1 = *reinterpret_cast<const float4 *>(y + 8 * v + 4);
-          acc = fmaf(wv[0], y0.x, acc);
-          acc = fmaf(wv[1], y0.y, acc);
-          acc = fmaf(wv[2], y0.z, acc);
-          acc = fmaf(wv[3], y0.w, acc);
-          acc = fmaf(wv[4], y1.x, acc);
-          acc = fmaf(wv[5], y1.y, acc);
-          acc = fmaf(wv[6], y1.z, acc);
-          acc = fmaf(wv[7], y1.w, acc);
+        for (int i = 0; i < nvec; ++i) {
+          const int v = static_cast<int>(threadIdx.x) + 256 * i;
+          float yv[8];
+          if (l == 0) {
+            Load8<__nv_bfloat16>::run(p.x_in + static_cast<size_t>(t) * H + 8 * v, yv);
+            *reinterpret_cast<float4 *>(resid + 8 * v) = make_float4(yv[0], yv[1], yv[2], yv[3]);
+            *reinterpret_cast<float4 *>(resid + 8 * v + 4) = make_float4(yv[4], yv[5], yv[6], yv[7]);
+          } else {
+            float wv[8];
+            Load8<__nv_bfloat16>::run(wn + 8 * v, wv);
+            const float4 s0 = *reinterpret_cast<const float4 *>(resid + 8 * v);
+            const float4 s1 = *reinterpret_cast<const float4 *>(resid + 8 * v + 4);
+            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) yv[e] = bf16_round(__fmul_rn(__fmul_rn(sv[e], r_norm), wv[e]));
+          }
+          *reinterpret_cast<float4 *>(y + 8 * v) = make_float4(yv[0], yv[1], yv[2], yv[3]);
+          *reinterpret_cast<float4 *>(y + 8 * v + 4) = make_float4(yv[4], yv[5], yv[6], yv[7]);
+          if (ok && nrr > 0) {
+            float wa[8];
+            Load8<__nv_bfloat16>::run(pb + 16 * v, wa);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc_a = fmaf(wa[e], yv[e], acc_a);
+            if (nrr > 1) {
+              float wb[8];
+              Load8<__nv_bfloat16>::run(pb + 2 * H + 16 * v, wb);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc_b = fmaf(wb[e], yv[e], acc_b);
+            }
+          }
         }
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (lane == 0) s_part[rs * p.W + wpart] = acc;
+        for (int m = 16; m > 0; m >>= 1) {
+          acc_a += __shfl_xor_sync(0xffffffffu, acc_a, m);
+          acc_b += __shfl_xor_sync(0xffffffffu, acc_b, m);
+        }
+        if (lane == 0) {
+          s_part[warp] = acc_a;
+          s_part[8 + warp] = acc_b;
+        }
       }
       if (__syncthreads_or(!ok)) goto fail;
-      if (threadIdx.x == 0) {
+      if (warp == 0) {
         float lg[2] = {0.f, 0.f};
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr)
           if (rr < nrr) {
-            lg[rr] = s_part[rr * p.W];
-#pragma unroll 1
-            for (int w = 1; w < p.W; ++w) lg[rr] += s_part[rr * p.W + w];
+            lg[rr] = s_part[8 * rr];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) lg[rr] += s_part[8 * rr + w];
           }
-        st_tag2(p.lg + (static_cast<size_t>(par) * G + c) * kSlot, tagged(tag, __float_as_uint(lg[0])),
-                tagged(tag, __float_as_uint(lg[1])));
+        // lane r < kXRep writes copy r
+        if (lane < kXRep)
+          st_tag2(p.lg + ((static_cast<size_t>(par) * kXRep + lane) * G + c) * kSlot,
+                  tagged(tag, __float_as_uint(lg[0])), tagged(tag, __float_as_uint(lg[1])));
       }
     }
+    STK_TRACE(2);
     // the gate/up activations, while the logits travel
     quantize_y(y, H, xt);   // ends with __syncthreads
-    SI_TRACE_MARK(0, 2);
+    STK_TRACE(3);
 
-    // [S] gather every logit; top-k + softmax in every block
+    // [S] warps 0..7 gather the logits of experts 32w .. 32w + 31 (expert e
+    // is row e of block e, or row e - G of block e - G) and sort them; the
+    // first 8 of every warp are the candidates. Meanwhile the other warps
+    // request the next iteration's router rows, shared-gate vector and norm
+    // weights and this iteration's shared down rows.
     {
       bool ok = true;
-      if (static_cast<int>(threadIdx.x) < G && static_cast<int>(threadIdx.x) < E) {
-        const uint64_t *q = p.lg + (static_cast<size_t>(par) * G + threadIdx.x) * kSlot;
-        uint64_t a, b;
-        ld_tag2(q, a, b);
-        ok = get_pair(q, tag, a, b, p.status);
-        SI_TRACE_LATEST(0, 8);
-        s_logit[threadIdx.x] = __uint_as_float(static_cast<uint32_t>(a));
-        if (static_cast<int>(threadIdx.x) + G < E)
-          s_logit[threadIdx.x + G] = __uint_as_float(static_cast<uint32_t>(b));
+      if (warp < 8) {
+        const int ex = 32 * warp + lane;
+        uint64_t key = 0ull;   // below every real key
+        if (ex < E) {
+          const int slot = ex < G ? ex : ex - G;
+          const uint64_t *q = p.lg + ((static_cast<size_t>(par) * kXRep + rep) * G + slot) * kSlot;
+          uint64_t a, b;
+          ld_tag2(q, a, b);
+          ok = get_pair(q, tag, a, b, p.status);
+          key = make_key(__uint_as_float(static_cast<uint32_t>(ex < G ? a : b)), ex);
+        }
+        key = warp_sort32(key, lane);
+        if (lane < 8) s_cand[warp * 8 + lane] = key;
       } else if (lane == 0) {
-        // warps without a slot to poll: the next iteration's router rows,
-        // shared-gate vector and norm weights; this iteration's shared down
-        // rows; and the arming of this iteration's routed copies
         if (threadIdx.x == kArmT) {
           if (my_unit >= 0 && !shared_unit)
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) arm(bars, 2 + g, 2 * gubytes, armed, used);
-          if (nrows > 0) arm(bars, 6, static_cast<uint32_t>(k * nrows * p.rbd), armed, used);
+            for (int g = 0; g < kGuGroups; ++g) arm(bars, s_arm, kBarGu + g, 2 * cbytes);
+          if (nrows > 0) arm(bars, s_arm, kBarDn, static_cast<uint32_t>(k * nrows * p.rbd));
         }
         const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];
-        uint8_t *dst = pbuf + ((it + 1) & 1) * pstr;
-        uint64_t *bar = &bars[(it + 1) & 1];
+        uint8_t *dst = pbuf + (par ^ 1u) * pstr;
+        uint64_t *bar = &bars[kBarPre + (par ^ 1u)];
         const bool next = it + 1 < n_iters;
         if (warp == 12 && next && nrr > 0)
           bulk_g2s(dst, Ln.w_router + static_cast<size_t>(row_a) * H, H * 2, bar);
@@ -533,18 +607,11 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         if (warp == 15 && next) bulk_g2s(dst + 6 * H, Ln.w_norm, H * 2, bar);
         if (warp == 11 && kShared && nrows > 0)
           bulk_g2s_evict_first(sd_buf, s_layers[l].wsd + static_cast<size_t>(j0) * p.rbsd,
-                               static_cast<uint32_t>(nrows) * p.rbsd, &bars[7], pol);
+                               static_cast<uint32_t>(nrows) * p.rbsd, &bars[kBarSd], pol);
       }
       if (__syncthreads_or(!ok)) goto fail;
     }
-    SI_TRACE_MARK(0, 3);
-    if (warp < 8) {
-      const int ex = threadIdx.x;
-      const uint64_t key = warp_sort32(ex < E ? make_key(s_logit[ex], ex) : 0ull, lane);
-      if (lane < 8) s_cand[warp * 8 + lane] = key;
-    }
-    SI_TRACE_MARK(0, 9);
-    __syncthreads();
+    STK_TRACE(4);
     {
       // rank of candidate tid / 8 among the 64: 8 threads compare 8 each
       const uint64_t me = s_cand[threadIdx.x >> 3];
@@ -558,36 +625,54 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       if ((threadIdx.x & 7) == 0 && rank < k && me != 0ull) s_sel[rank] = me;
     }
     __syncthreads();
-    SI_TRACE_MARK(0, 10);
-    // routed bytes, one copy per warp: warps 0..7 this block's gate/up unit
-    // (warp w: group w & 3 of the gate (w < 4) or up rows, 8 rows each),
-    // warps 8 .. 8 + k - 1 its down rows of each selected expert; a block with
-    // a gate/up unit issues the down rows only once it has consumed its own
-    // gate/up rows, so that they do not compete with the more urgent bytes
+    STK_TRACE(5);
+    // routed bytes, one copy per warp: warps 0 .. 2 kGuGroups - 1 this block's
+    // gate/up unit (warp w: group w % kGuGroups of the gate (w < kGuGroups) or
+    // up rows), warps 8 .. 8 + k - 1
+    // its down rows of each selected expert if it has no gate/up unit (a block
+    // with a unit requests them once its gate/up rows have landed)
     if (lane == 0) {
       const StackLayerPtrs &Lp = s_layers[l];
-      if (warp < 8 && my_unit >= 0 && !shared_unit) {
+      if (warp < 2 * kGuGroups && my_unit >= 0 && !shared_unit) {
         const int slot = my_unit / (I / 32), hb = my_unit - slot * (I / 32);
         int e = key_index(s_sel[slot]);
         if (e < 0 || e >= E) e = 0;
-        const size_t row0 = static_cast<size_t>(e) * I + static_cast<size_t>(hb) * 32 + 8 * (warp & 3);
-        bulk_g2s_evict_first(gu_buf + warp * gubytes, (warp < 4 ? Lp.wg : Lp.wu) + row0 * p.rb,
-                             gubytes, &bars[2 + (warp & 3)], pol);
+        const int g = warp % kGuGroups;
+        const bool up = warp >= kGuGroups;
+        const size_t row0 = static_cast<size_t>(e) * I + static_cast<size_t>(hb) * 32 + kGuRows * g;
+        bulk_g2s_evict_first(gu_buf + ((up ? 32 : 0) + kGuRows * g) * p.rb, (up ? Lp.wu : Lp.wg) + row0 * p.rb,
+                             cbytes, &bars[kBarGu + g], pol);
       }
       if (warp >= 8 && warp < 8 + k && nrows > 0 && my_unit < 0) {
         int e = key_index(s_sel[warp - 8]);
         if (e < 0 || e >= E) e = 0;
         bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
                              Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
-                             static_cast<uint32_t>(nrows) * p.rbd, &bars[6], pol);
+                             static_cast<uint32_t>(nrows) * p.rbd, &bars[kBarDn], pol);
       }
     }
-    SI_TRACE_MARK(0, 4);
+    // while the routed bytes travel: softmax over the selected logits (rank
+    // order) and the ids
+    if (warp == 4) {
+      const int r = lane < k ? lane : 0;
+      const float ex = expf(key_value(s_sel[r]) - key_value(s_sel[0]));
+      float sum = 0.f;
+#pragma unroll 1
+      for (int q = 0; q < k; ++q) sum += __shfl_sync(0xffffffffu, ex, q);
+      if (lane < k) {
+        s_wts[lane] = ex * __frcp_rn(sum);
+        if (c == 0 && p.ids_out) {
+          const int e = key_index(s_sel[lane]);
+          p.ids_out[static_cast<size_t>(it) * k + lane] = (e < 0 || e >= E) ? 0 : e;
+        }
+      }
+    }
+    STK_TRACE(6);
 
     // [G] gate/up of this block's unit -> h line
     if (my_unit >= 0) {
       float acc = 0.f;
-      const bool ok = mbar_wait_bounded(&bars[2 + (pr >> 3)], par, p.status);
+      const bool ok = mbar_wait_bounded(&bars[kBarGu + pr / kGuRows], par, p.status);
       if (ok) {
         const uint8_t *row = gu_buf + (gm * 32 + pr) * p.rb;
         for (int sb = lane8; sb < nsb; sb += 8)
@@ -600,10 +685,9 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
       const float other = __shfl_xor_sync(0xffffffffu, acc, 8);
       if ((threadIdx.x & 15) == 0) h_s[pr] = __fdiv_rn(acc, 1.f + expf(-acc)) * other;
-      if (threadIdx.x == kArmT && shared_unit && it + 1 < n_iters)
-#pragma unroll 1
-        for (int g = 0; g < 4; ++g) arm(bars, 2 + g, 2 * gubytes, armed, used);
       if (__syncthreads_or(!ok)) goto fail;
+      STK_TRACE(7);
+      // every wait on this iteration's gate/up phases is over
       if (lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {
         // the down rows, now that this block's gate/up rows are in: they are
         // needed only after the h exchange
@@ -612,15 +696,18 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         if (e < 0 || e >= E) e = 0;
         bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
                              Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
-                             static_cast<uint32_t>(nrows) * p.rbd, &bars[6], pol);
+                             static_cast<uint32_t>(nrows) * p.rbd, &bars[kBarDn], pol);
       }
-      if (lane == 0 && warp >= 8 && shared_unit && it + 1 < n_iters) {
-        // the next iteration's shared gate/up unit (warps 8..15, one group each)
+      if (lane == 0 && warp >= 2 && warp < 2 + kGuGroups && shared_unit && it + 1 < n_iters) {
+        // the next iteration's shared gate/up group warp - 2, armed and
+        // requested by one thread
         const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];
-        const int w = warp - 8;
-        const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32 + 8 * (w & 3);
-        bulk_g2s_evict_first(gu_buf + w * gubytes, (w < 4 ? Ln.wsg : Ln.wsu) + row0 * p.rb, gubytes,
-                             &bars[2 + (w & 3)], pol);
+        const int g = warp - 2;
+        const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32 + kGuRows * g;
+        arm(bars, s_arm, kBarGu + g, 2 * cbytes);
+        bulk_g2s_evict_first(gu_buf + kGuRows * g * p.rb, Ln.wsg + row0 * p.rb, cbytes, &bars[kBarGu + g], pol);
+        bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rb, Ln.wsu + row0 * p.rb, cbytes,
+                             &bars[kBarGu + g], pol);
       }
       if (warp == 0) {
         uint16_t d16, s16;
@@ -628,105 +715,128 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         const uint32_t w = q | (__shfl_down_sync(0xffffffffu, q, 1) << 8) |
                            (__shfl_down_sync(0xffffffffu, q, 2) << 16) |
                            (__shfl_down_sync(0xffffffffu, q, 3) << 24);   // lane 4j: code word j
-        // lane j < 4: words 2j, 2j + 1; lane 4: scales; one coalesced store
-        const uint32_t wa = __shfl_sync(0xffffffffu, w, (8 * lane) & 31);
-        const uint32_t wb = __shfl_sync(0xffffffffu, w, (8 * lane + 4) & 31);
-        uint64_t *line = p.hl + (static_cast<size_t>(par) * units + my_unit) * kSlot;
-        if (lane < 4)
-          st_tag2(line + 2 * lane, tagged(tag, wa), tagged(tag, wb));
-        else if (lane == 4)
-          st_tag2(line + 8, tagged(tag, static_cast<uint32_t>(d16) | (static_cast<uint32_t>(s16) << 16)),
-                  tagged(tag, 0u));
-      }
-    }
-    if (warp == 1) {   // softmax over the selected logits, summed in rank order
-      const int r = lane < k ? lane : 0;
-      const float ex = expf(key_value(s_sel[r]) - key_value(s_sel[0]));
-      float sum = 0.f;
-#pragma unroll 1
-      for (int q = 0; q < k; ++q) sum += __shfl_sync(0xffffffffu, ex, q);
-      if (lane < k) {
-        s_wts[lane] = ex * __frcp_rn(sum);
-        if (c == 0 && p.ids_out) {
-          int e = key_index(s_sel[lane]);
-          p.ids_out[static_cast<size_t>(it) * k + lane] = (e < 0 || e >= E) ? 0 : e;
+        // item i = 5 r + j of copy r: pair j < 4 = code words 2j, 2j + 1,
+        // pair 4 = the scales; lane L writes items L, L + 32, ...
+#pragma unroll
+        for (int i0 = 0; i0 < 5 * kXRep; i0 += 32) {
+          const int i = i0 + lane, r = i / 5, j = i - 5 * r;
+          const uint32_t wa = __shfl_sync(0xffffffffu, w, (8 * j) & 31);
+          const uint32_t wb = __shfl_sync(0xffffffffu, w, (8 * j + 4) & 31);
+          uint64_t *line = p.hl + ((static_cast<size_t>(par) * kXRep + r) * units + my_unit) * kSlot;
+          if (i < 5 * kXRep) {
+            if (j < 4)
+              st_tag2(line + 2 * j, tagged(tag, wa), tagged(tag, wb));
+            else
+              st_tag2(line + 8, tagged(tag, static_cast<uint32_t>(d16) | (static_cast<uint32_t>(s16) << 16)),
+                      tagged(tag, 0u));
+          }
         }
       }
     }
-    SI_TRACE_MARK(0, 5);
+    STK_TRACE(8);
+    // the shared expert's gate sigma(w_sg . y), while the h lines travel
     float sigma = 0.f;
     if (kShared && nrows > 0) {
       const __nv_bfloat16 *wsg = reinterpret_cast<const __nv_bfloat16 *>(pbuf + par * pstr + 4 * H);
       sigma = __fdiv_rn(1.f, 1.f + expf(-sigma_dot(wsg, y, H, red)));
     }
 
-    // [D] gather h, down for this block's rows -> X3 line
+    // [D] gather h, down for this block's rows -> X3 line. The first reads of
+    // the h lines go out, then the down rows of this pass are taken apart
+    // into registers (they usually land before the last h line), then the h
+    // lines are polled.
     if (nrows > 0) {
       bool ok = true;
-      {
-        const uint64_t *hl = p.hl + static_cast<size_t>(par) * units * kSlot;
-        uint64_t v[2][2];
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-          if (g_q[s] >= 0) ld_tag2(hl + g_q[s], v[s][0], v[s][1]);
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (g_q[s] < 0) continue;
-          ok &= get_pair(hl + g_q[s], tag, v[s][0], v[s][1], p.status);
-          SI_TRACE_LATEST(0, 14);
-          if (g_dst[s] >= 0) {
-            *reinterpret_cast<uint2 *>(smem + g_dst[s]) =
-                make_uint2(static_cast<uint32_t>(v[s][0]), static_cast<uint32_t>(v[s][1]));
-          } else {
-            const uint32_t w = static_cast<uint32_t>(v[s][0]);
-            ht.d[-g_dst[s] - 1] = half_bits_to_float(static_cast<uint16_t>(w & 0xFFFFu));
-            ht.s[-g_dst[s] - 1] = half_bits_to_float(static_cast<uint16_t>(w >> 16));
-          }
-        }
-      }
-      if (__syncthreads_or(!ok)) goto fail;
-      SI_TRACE_MARK(0, 6);
-      bool okw = mbar_wait_bounded(&bars[6], par, p.status);
-      if (kShared) okw &= mbar_wait_bounded(&bars[7], par, p.status);
+      const uint64_t *hl = p.hl + (static_cast<size_t>(par) * kXRep + rep) * units * kSlot;
+      uint64_t v[2][2];
 #pragma unroll
       for (int s = 0; s < 2; ++s)
-        if (okw && d_part[s] >= 0)
-          part[d_part[s]] = q4k_half_dot(reinterpret_cast<const uint4 *>(smem + d_row[s]),
-                                         reinterpret_cast<const uint4 *>(smem + d_act[s]), ht.d + d_blk[s],
-                                         ht.s + d_blk[s], d_h[s]);
-      if (__syncthreads_or(!okw)) goto fail;
-      float ysum = 0.f;
-      if (tlive) {
+        if (g_q[s] >= 0) ld_tag2(hl + g_q[s], v[s][0], v[s][1]);
+      bool okw = mbar_wait_bounded(&bars[kBarDn], par, p.status);
+      if (kShared) okw &= mbar_wait_bounded(&bars[kBarSd], par, p.status);
+      Q4KHalf wq;
+      if (okw && d_live[0]) q4k_half_load(reinterpret_cast<const uint4 *>(smem + d_row[0]), d_h[0], wq);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (g_q[s] < 0) continue;
+        ok &= get_pair(hl + g_q[s], tag, v[s][0], v[s][1], p.status);
+        if (g_dst[s] >= 0) {
+          *reinterpret_cast<uint2 *>(smem + g_dst[s]) =
+              make_uint2(static_cast<uint32_t>(v[s][0]), static_cast<uint32_t>(v[s][1]));
+        } else {
+          const uint32_t w = static_cast<uint32_t>(v[s][0]);
+          ht.d[-g_dst[s] - 1] = half_bits_to_float(static_cast<uint16_t>(w & 0xFFFFu));
+          ht.s[-g_dst[s] - 1] = half_bits_to_float(static_cast<uint16_t>(w >> 16));
+        }
+      }
+      if (__syncthreads_or(!(ok && okw))) goto fail;
+      STK_TRACE(9);
+      STK_TRACE(10);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (s * kStkThreads < items) {   // block-uniform
+          float v = 0.f;
+          if (d_live[s]) {
+            const uint4 *a = reinterpret_cast<const uint4 *>(smem + d_act[s]);
+            v = s == 0 ? q4k_half_dot_loaded(wq, a, ht.d + d_blk[s], ht.s + d_blk[s], d_h[s])
+                       : q4k_half_dot(reinterpret_cast<const uint4 *>(smem + d_row[s]), a, ht.d + d_blk[s],
+                                      ht.s + d_blk[s], d_h[s]);
+          }
+          // the pieces of a (slot, row), summed in order by its first lane
+          float ysum = 0.f;
+          ysum += v;
 #pragma unroll 1
-        for (int qq = 0; qq < tPP; ++qq) ysum += part[(tr * J + tj) * P_max + qq];
+          for (int q = 1; q < P_max; ++q) {
+            const float o = __shfl_down_sync(0xffffffffu, v, q);
+            if (q < d_P[s]) ysum += o;
+          }
+          if (d_live[s] && d_first[s]) part[d_dst[s]] = ysum;
+        }
       }
       __syncthreads();
-      if (tlive) part[tr * J + tj] = ysum;
-      __syncthreads();
+      STK_TRACE(11);
       if (warp == 0) {
         uint32_t tb = 0u;
         if (lane < nrows) {
+          // the 8 partial rows first, then the rank-order fma chain
+          float pv[8], wv[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            pv[r] = r < k ? part[r * J + lane] : 0.f;
+            wv[r] = r < k ? s_wts[r] : 0.f;
+          }
           float acc = 0.f;
-#pragma unroll 1
-          for (int r = 0; r < k; ++r) acc = fmaf(s_wts[r], part[r * J + lane], acc);
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            if (r < k) acc = fmaf(wv[r], pv[r], acc);
           float tv = bf16_round(acc);
           if (kShared) tv = bf16_round(tv + bf16_round(sigma * part[k * J + lane]));
           tb = bf16_bits(tv);
         }
-        // lane m < np3 writes rows 4m .. 4m + 3: one coalesced store
-        const uint32_t r0 = __shfl_sync(0xffffffffu, tb, (4 * lane) & 31);
-        const uint32_t r1 = __shfl_sync(0xffffffffu, tb, (4 * lane + 1) & 31);
-        const uint32_t r2 = __shfl_sync(0xffffffffu, tb, (4 * lane + 2) & 31);
-        const uint32_t r3 = __shfl_sync(0xffffffffu, tb, (4 * lane + 3) & 31);
-        if (lane < p.np3)
-          st_tag2(p.ol + (static_cast<size_t>(par) * G + c) * kSlot + 2 * lane, tagged(tag, r0 | (r1 << 16)),
-                  tagged(tag, r2 | (r3 << 16)));
+        // item i = np3 r + m of copy r: rows 4m .. 4m + 3; lane L writes
+        // items L, L + 32, ...
+#pragma unroll 1
+        for (int i0 = 0; i0 < p.np3 * kXRep; i0 += 32) {
+          const int i = i0 + lane, r = i / p.np3, m = i - r * p.np3;
+          const uint32_t r0 = __shfl_sync(0xffffffffu, tb, (4 * m) & 31);
+          const uint32_t r1 = __shfl_sync(0xffffffffu, tb, (4 * m + 1) & 31);
+          const uint32_t r2 = __shfl_sync(0xffffffffu, tb, (4 * m + 2) & 31);
+          const uint32_t r3 = __shfl_sync(0xffffffffu, tb, (4 * m + 3) & 31);
+          if (i < p.np3 * kXRep)
+            st_tag2(p.ol + ((static_cast<size_t>(par) * kXRep + r) * G + c) * kSlot + 2 * m,
+                    tagged(tag, r0 | (r1 << 16)), tagged(tag, r2 | (r3 << 16)));
+        }
       }
-    } else if (warp == 0 && lane < p.np3) {
+    } else if (warp == 0) {
       // no rows: the slot still says that this block is done with iteration it
-      st_tag2(p.ol + (static_cast<size_t>(par) * G + c) * kSlot + 2 * lane, tagged(tag, 0u), tagged(tag, 0u));
+#pragma unroll 1
+      for (int i = lane; i < p.np3 * kXRep; i += 32) {
+        const int r = i / p.np3, m = i - r * p.np3;
+        st_tag2(p.ol + ((static_cast<size_t>(par) * kXRep + r) * G + c) * kSlot + 2 * m, tagged(tag, 0u),
+                tagged(tag, 0u));
+      }
     }
-    SI_TRACE_MARK(0, 7);
+    STK_TRACE(12);
     if (++l == p.n_layers) {
       l = 0;
       ++t;
@@ -734,10 +844,15 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   }
   goto finish;
 fail:
-  if (threadIdx.x == kArmT)
+  // every thread arrives here together (each jump follows a block-wide
+  // vote); wait for the last armed phase of each barrier
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t a = *s_arm;
 #pragma unroll 1
-    for (int b = 0; b < 8; ++b)
-      if ((used >> b) & 1u) mbar_wait_bounded(&bars[b], ((armed >> b) & 1u) ^ 1u, p.status);
+    for (int b = 0; b < kNumBars; ++b)
+      if ((a >> (16 + b)) & 1u) mbar_wait_bounded(&bars[b], ((a >> b) & 1u) ^ 1u, p.status);
+  }
 finish:
   // Tags of this launch are base + 1 .. base + n_iters; the next starts above.
   if (c == 0 && threadIdx.x == 0) *p.epoch = base + static_cast<uint32_t>(n_iters);
@@ -771,9 +886,9 @@ static StackGeom stack_geom(const si_moe_layer &L, int n_layers, int sms) {
   };
   take(g.off_epoch, 256);
   take(g.off_layers, sizeof(StackLayerPtrs) * n_layers);
-  take(g.off_lg, 2 * 8u * kSlot * sms);
-  take(g.off_hl, 2 * 8u * kSlot * g.units);
-  take(g.off_ol, 2 * 8u * kSlot * sms);
+  take(g.off_lg, 2 * 8u * kSlot * kXRep * sms);
+  take(g.off_hl, 2 * 8u * kSlot * kXRep * g.units);
+  take(g.off_ol, 2 * 8u * kSlot * kXRep * sms);
   g.bytes = off;
   return g;
 }
@@ -837,6 +952,11 @@ bool stack_supported(const si_moe_layer *layers, int n_layers) {
   if (sms < g.units || g.units * 5 > 2 * kStkThreads || g.J > 32 || sms * g.np3 > 2 * kStkThreads ||
       n_slots * g.J * P_max > 2 * kStkThreads || n_slots * g.J > kStkThreads)
     return false;
+  // the pieces of a (slot, row) of the down step are summed across lanes of
+  // one warp: the piece counts must divide 32, and the shared slot's pieces
+  // must start on a multiple of their count
+  const int P_r = 2 * L.inter / 256, P_s = 2 * L.shared_inter / 256;
+  if (32 % P_r || (L.shared_inter > 0 && (32 % P_s || (L.top_k * g.J * P_r) % P_s))) return false;
   if ((L.n_experts > 128 ? 2 * sms : sms) < L.n_experts) return false;
   if (sms > kStkThreads) return false;
   if (stack_smem(L, g.J, n_layers).bytes > 227 * 1024) return false;
@@ -895,8 +1015,6 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   p.rbd = L.inter / 256 * kQ4KBytes;
   p.rbsd = L.shared_inter / 256 * kQ4KBytes;
   p.J = g.J;
-  p.W = L.n_experts > 128 ? 4 : 8;      // as the router kernel's shape for these sizes
-  p.nch = L.hidden / 8 / 32 / p.W;
   p.np3 = g.np3;
   p.eps = L.eps;
   p.sm = stack_smem(L, g.J, n_layers);
@@ -953,6 +1071,9 @@ extern "C" si_status si_test_poll_timeout(uint64_t budget_ns, void *workspace, v
 }
 
 #ifdef SI_TRACE
+extern "C" int si_trace_stack_phase(int phase) {
+  return cudaMemcpyToSymbol(si::g_stk_trace_phase, &phase, sizeof(phase)) == cudaSuccess ? 0 : 4;
+}
 extern "C" int si_trace_dump_stack(void *dst) {
   return cudaMemcpyFromSymbol(dst, si::g_si_trace, sizeof(si::g_si_trace)) == cudaSuccess ? 0 : 4;
 }

@@ -197,6 +197,77 @@ def time_oracle(jobs):
     return (time.perf_counter() - t0) / len(jobs)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                v = line.split(":", 1)[1].strip()
+                if v and not v.isdigit():
+                    return v
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_worker(path, barrier, queue):
+    """One host core: load the sample, wait for every worker, time the
+    oracle's whole layer over the sample."""
+    import torch
+
+    from oracle import moe as M
+    jobs = torch.load(path, weights_only=False)
+    barrier.wait()
+    t0 = time.perf_counter()
+    for L, xt in jobs:
+        M.layer_forward(L, xt)
+    queue.put((t0, time.perf_counter(), len(jobs)))
+
+
+def time_oracle_all_cores(jobs, n_workers: int):
+    """Whole-host throughput of the oracle: n_workers processes (spawned, one
+    numpy thread each) each run every job of `jobs`; returns seconds per
+    layer-token over all of them (wall time from the first start to the last
+    finish, divided by the layer-tokens done)."""
+    import multiprocessing as mp
+
+    import torch
+    path = os.path.join("/tmp", f"si_oracle_jobs_{os.getpid()}.pt")
+    torch.save(jobs, path)
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(n_workers)
+    queue = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(path, barrier, queue)) for _ in range(n_workers)]
+    for pr in procs:
+        pr.start()
+    res = []
+    try:
+        while len(res) < n_workers:
+            try:
+                res.append(queue.get(timeout=5))
+            except Exception:
+                if any(pr.exitcode not in (None, 0) for pr in procs):
+                    raise RuntimeError("an oracle worker failed")
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+            if pr.is_alive():
+                pr.kill()
+        os.remove(path)
+    t0 = min(r[0] for r in res)
+    t1 = max(r[1] for r in res)
+    return (t1 - t0) / sum(r[2] for r in res)
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -315,10 +386,12 @@ def run_gpu(args):
 
     if rank != 0:
         return 0
-    cpu_us, cpu_n = (None, 0)
+    cpu_us, cpu_n, cpu_all_us, n_cores = None, 0, None, 0
     if world == 1 and not args.no_cpu_baseline:
         jobs = oracle_jobs(args.cpu_layer_tokens, device=dev)
         cpu_us, cpu_n = time_oracle(jobs) * 1e6, len(jobs)
+        n_cores = os.cpu_count() or 1
+        cpu_all_us = time_oracle_all_cores(jobs[:8], n_cores) * 1e6
     launches = args.steps * (1 if graph.persistent else N_LAYERS * N_TOKENS * 4)
     # The timed path is one persistent kernel launch per step (the dominant and
     # only kernel): algorithmic bytes per launch = weight bytes of all
@@ -359,10 +432,14 @@ def run_gpu(args):
         "device_status": m.status_string(status), "ids_valid": ids_ok,
     }
     if cpu_us is not None:
-        line["cpu_baseline"] = {"value": round(cpu_us, 1), "unit": UNIT, "cores": 1,
-                                "kind": "oracle",
-                                "sample": f"{cpu_n} layer-tokens of the same stack, fp64 oracle, "
-                                          "single thread"}
+        line["cpu_baseline"] = {
+            "value": round(cpu_all_us, 1), "unit": UNIT, "cores": n_cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": (f"whole host: {n_cores} processes (one numpy thread each) each run the same 8 "
+                       "layer-tokens of the stack through the fp64 oracle layer; wall time over all "
+                       "8 x processes layer-tokens"),
+            "single_thread": {"value": round(cpu_us, 1), "unit": UNIT, "cores": 1,
+                              "sample": f"{cpu_n} layer-tokens of the same stack, one thread"}}
     print(json.dumps(line), flush=True)
     graph.close()
     return 0
@@ -520,6 +597,26 @@ def run_configs(args):
                  round(U * Q4K_EXPERT_128E), distinct_experts=U, us_per_layer_token=round(us / T, 3),
                  device_status=m.status_string(st))
             del graph
+    del layers
+    torch.cuda.empty_cache()
+
+    # config 5 as stated: the 48-layer stack of that layer, T tokens through
+    # every layer together (router, grouped experts, norm), one graph
+    NL5 = 48
+    layers = [m.device_layer(spec, SEED + 600, l, device=dev) for l in range(NL5)]
+    for T in (1, 4, 16, 64):
+        xs = gen.make_tokens(SEED + 700 + T, T, device=dev)
+        g = m.BatchedStackGraph(layers, xs)
+        us = _time_replays(lambda: g.launch(stream), stream, warm=3, reps=10) / NL5
+        st = m.si_workspace_status(g.ws, stream)
+        U = sum(int(torch.unique(g.ids[l]).numel()) for l in range(NL5)) / NL5
+        nbytes = round(U * Q4K_EXPERT_128E + 128 * 2048 * 2)
+        emit(f"5: 48-layer stack, 128 experts, I=768, T={T}",
+             "batched layer stack (router + grouped experts + norm per layer), one graph", us,
+             "us/layer", nbytes, distinct_experts=U, us_per_layer_token=round(us / T, 3),
+             note="bytes = distinct experts' Q4_K weights + bf16 router, per layer",
+             device_status=m.status_string(st))
+        g.close()
     return 0
 
 

@@ -345,6 +345,44 @@ int si_graph_is_persistent(const si_graph *graph);
 si_status si_graph_launch(si_graph *graph, void *stream);
 void si_graph_destroy(si_graph *graph);
 
+/*
+ * si_moe_layer_decode_batched - one whole layer for n_tokens tokens, each
+ * routed on its own (not on the pages, which measure batch 1; the per-token
+ * arithmetic is si_moe_layer_decode's): router + top-k of every token, the
+ * routed experts grouped by expert (si_moe_ffn_batched, `mode` as there), and
+ * sum = bf16(routed + residual), norm = RMSNorm(sum) of every row.
+ *   x          device bf16 [T][H]: FFN input; residual device bf16 [T][H] (may equal x)
+ *   sum_out, norm_out device bf16 [T][H]
+ *   topk_ids, topk_w, routed_out: optional device outputs int32 [T][k],
+ *              fp32 [T][k], bf16 [T][H] (NULL to skip)
+ *   workspace  si_moe_layer_batched_workspace_bytes(L, T) bytes, zeroed once
+ * Supported: the layers si_moe_ffn_batched takes (Q4_K experts, no shared
+ * expert) with a bf16 or fp32 router. In SI_FFN_INT8 / SI_FFN_AUTO mode
+ * every token's results equal si_moe_layer_decode's on that token alone.
+ */
+size_t si_moe_layer_batched_workspace_bytes(const si_moe_layer *L, int n_tokens);
+si_status si_moe_layer_decode_batched(const si_moe_layer *L, int n_tokens, int mode, const void *x,
+                                      const void *residual, void *sum_out, void *norm_out,
+                                      int32_t *topk_ids, float *topk_w, void *routed_out,
+                                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Batched layer stack captured as one CUDA graph: n_tokens tokens go through
+ * n_layers layers together (si_moe_layer_decode_batched per layer); layer l
+ * takes (norm_out, sum_out) of layer l-1 as (x, residual), layer 0 takes
+ * (x_in, x_in).
+ *   x_in  device bf16 [T][H]; y_out device bf16 [T][H] (last norm);
+ *   sum_out device bf16 [T][H] (last residual) or NULL;
+ *   ids_out device int32 [n_layers][T][k] or NULL
+ *   workspace si_moe_stack_batched_workspace_bytes(layers, n_layers, T) bytes, zeroed once
+ * The graph captures the pointers; `stream` is used for capture only.
+ */
+size_t si_moe_stack_batched_workspace_bytes(const si_moe_layer *layers, int n_layers, int n_tokens);
+si_status si_moe_stack_graph_create_batched(const si_moe_layer *layers, int n_layers, int n_tokens,
+                                            int mode, const void *x_in, void *y_out, void *sum_out,
+                                            int32_t *ids_out, void *workspace, size_t workspace_bytes,
+                                            void *stream, si_graph **graph_out);
+
 /* Synchronises `stream`, then reads the device status word of a workspace
  * used by any call above (SI_OK if no device-side error was recorded) and
  * clears it. */

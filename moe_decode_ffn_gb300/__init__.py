@@ -73,6 +73,12 @@ SIGNATURES = {
                                               _vp, _vp, _vp, _sz, _i32, _vp,
                                               ctypes.POINTER(_vp)]),
     "si_graph_is_persistent": (_i32, [_vp]),
+    "si_moe_layer_batched_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
+    "si_moe_layer_decode_batched": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _i32, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _vp, _sz, _vp]),
+    "si_moe_stack_batched_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32, _i32]),
+    "si_moe_stack_graph_create_batched": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _i32, _i32, _vp,
+                                                 _vp, _vp, _vp, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "si_requant_q4_k": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "si_graph_launch": (_i32, [_vp, _vp]),
     "si_graph_destroy": (None, [_vp]),
@@ -386,6 +392,75 @@ class StackGraph:
         self.handle = h
         self.stream = stream
         self.persistent = bool(library().si_graph_is_persistent(h))
+
+    def launch(self, stream=None):
+        _check(library().si_graph_launch(self.handle, _stream(stream)), "si_graph_launch")
+
+    def close(self):
+        if self.handle:
+            library().si_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def layer_batched_workspace_bytes(layer: Layer, n_tokens: int) -> int:
+    return int(library().si_moe_layer_batched_workspace_bytes(layer.ref, n_tokens))
+
+
+def si_moe_layer_decode_batched(layer: Layer, x: torch.Tensor, residual=None, mode: int = SI_FFN_AUTO,
+                                ws=None, stream=None) -> dict:
+    """T tokens through one layer, each routed on its own: x bf16 [T, H] ->
+    {sum, y, routed: bf16 [T, H], ids: int32 [T, k], w: fp32 [T, k]}."""
+    T, H = x.shape
+    k = layer.spec.top_k
+    dev = x.device
+    out = {n: torch.empty(T, H, dtype=torch.bfloat16, device=dev) for n in ("sum", "y", "routed")}
+    out["ids"] = torch.empty(T, k, dtype=torch.int32, device=dev)
+    out["w"] = torch.empty(T, k, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(layer_batched_workspace_bytes(layer, T), dev)
+    res = x if residual is None else residual
+    _check(library().si_moe_layer_decode_batched(
+        layer.ref, T, mode, _shaped(x, "x", T * H, _BF16), _shaped(res, "residual", T * H, _BF16),
+        _cuda(out["sum"], "sum"), _cuda(out["y"], "y"), _cuda(out["ids"], "ids"), _cuda(out["w"], "w"),
+        _cuda(out["routed"], "routed"), _cuda(ws, "ws"), ws.numel(), _stream(stream)),
+        "si_moe_layer_decode_batched")
+    return out
+
+
+class BatchedStackGraph:
+    """T tokens through n_layers layers together (per-token routing), captured
+    as one CUDA graph; buffers owned here."""
+
+    def __init__(self, layers, x_in: torch.Tensor, mode: int = SI_FFN_AUTO, want_ids: bool = True):
+        self.layers = list(layers)
+        arr = (SiMoeLayer * len(self.layers))(*[l.c for l in self.layers])
+        self._arr = arr
+        T, H = x_in.shape
+        if H != self.layers[0].spec.hidden or x_in.dtype != torch.bfloat16:
+            raise ValueError(f"x_in must be bf16 [T, {self.layers[0].spec.hidden}]")
+        k = self.layers[0].spec.top_k
+        dev = x_in.device
+        self.x_in = x_in
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.sum = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.ids = (torch.empty(len(self.layers), T, k, dtype=torch.int32, device=dev)
+                    if want_ids else None)
+        nb = int(library().si_moe_stack_batched_workspace_bytes(arr, len(self.layers), T))
+        self.ws = workspace(nb, dev)
+        h = _vp()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        _check(library().si_moe_stack_graph_create_batched(
+            arr, len(self.layers), T, mode, _cuda(x_in, "x_in"), _cuda(self.y, "y"),
+            _cuda(self.sum, "sum"), _opt(self.ids, "ids"), _cuda(self.ws, "ws"), self.ws.numel(),
+            _stream(cap), ctypes.byref(h)), "si_moe_stack_graph_create_batched")
+        self.handle = h
 
     def launch(self, stream=None):
         _check(library().si_graph_launch(self.handle, _stream(stream)), "si_graph_launch")

@@ -313,6 +313,171 @@ extern "C" si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n
                                         graph_out);
 }
 
+// ---------------------------------------------------------------------------
+// Batched layer: n_tokens tokens routed independently, their experts grouped
+// (si_moe_ffn_batched), then the residual fold of every row.
+// ---------------------------------------------------------------------------
+namespace si {
+
+struct BLayerGeom {
+  size_t off_router, off_ffn, off_ids, off_wts, off_routed, bytes;
+};
+
+static BLayerGeom blayer_geom(const si_moe_layer &L, int T) {
+  BLayerGeom g{};
+  size_t off = sizeof(WsHeader);
+  auto take = [&](size_t &field, size_t bytes) {
+    field = off;
+    off = round_up(off + bytes, 256);
+  };
+  take(g.off_router, router_geom(L.n_experts, L.hidden, T).bytes);
+  take(g.off_ffn, batched_workspace_bytes(L, T));
+  take(g.off_ids, sizeof(int32_t) * static_cast<size_t>(T) * L.top_k);
+  take(g.off_wts, sizeof(float) * static_cast<size_t>(T) * L.top_k);
+  take(g.off_routed, 2u * static_cast<size_t>(T) * L.hidden);
+  g.bytes = off;
+  return g;
+}
+
+static si_status blayer_check(const si_moe_layer &L, int T) {
+  const si_status st = batched_validate(L, T);
+  if (st != SI_OK) return st;
+  if (L.n_experts < 8 || !L.w_router || !L.w_norm || !(L.eps >= 0.f)) return SI_ERR_INVALID_ARG;
+  if (L.router_type != SI_BF16 && L.router_type != SI_F32) return SI_ERR_UNSUPPORTED;
+  if (!aligned16(L.w_router) || !aligned16(L.w_norm) || L.hidden > 16384) return SI_ERR_INVALID_ARG;
+  return SI_OK;
+}
+
+static si_status blayer_enqueue(const si_moe_layer &L, int T, int mode, const void *x,
+                                const void *residual, void *sum_out, void *norm_out, int32_t *ids,
+                                float *wts, void *routed, void *ws, uint32_t *status, cudaStream_t s) {
+  const BLayerGeom g = blayer_geom(L, T);
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  if (!ids) ids = reinterpret_cast<int32_t *>(base + g.off_ids);
+  if (!wts) wts = reinterpret_cast<float *>(base + g.off_wts);
+  if (!routed) routed = base + g.off_routed;
+  si_status st = router_launch(x, SI_BF16, L.w_router, L.router_type, L.hidden, L.n_experts,
+                               L.top_k, T, ids, wts, nullptr, base + g.off_router, status, s);
+  if (st != SI_OK) return st;
+  st = batched_launch(&L, T, mode, x, ids, wts, routed, base + g.off_ffn, status, s);
+  if (st != SI_OK) return st;
+  return norm_launch(routed, residual, nullptr, L.w_norm, L.hidden, T, L.eps, sum_out, norm_out,
+                     nullptr, s);
+}
+
+// Batched stack workspace: header, then per layer [layer workspace][sum bf16 T x H][norm bf16 T x H].
+static size_t bstack_layer_bytes(const si_moe_layer &L, int T) {
+  return round_up(blayer_geom(L, T).bytes + 4 * static_cast<size_t>(T) * L.hidden, 256);
+}
+
+}  // namespace si
+
+extern "C" size_t si_moe_layer_batched_workspace_bytes(const si_moe_layer *L, int n_tokens) {
+  if (!L || blayer_check(*L, n_tokens) != SI_OK) return 0;
+  return blayer_geom(*L, n_tokens).bytes;
+}
+
+extern "C" si_status si_moe_layer_decode_batched(const si_moe_layer *L, int n_tokens, int mode,
+                                                 const void *x, const void *residual, void *sum_out,
+                                                 void *norm_out, int32_t *topk_ids, float *topk_w,
+                                                 void *routed_out, void *workspace,
+                                                 size_t workspace_bytes, void *stream) {
+  if (!L || !x || !residual || !sum_out || !norm_out) return SI_ERR_INVALID_ARG;
+  if (mode != SI_FFN_AUTO && mode != SI_FFN_INT8 && mode != SI_FFN_TENSOR) return SI_ERR_INVALID_ARG;
+  const si_status st = blayer_check(*L, n_tokens);
+  if (st != SI_OK) return st;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(sum_out) || !aligned16(norm_out) ||
+      (routed_out && !aligned16(routed_out)) ||
+      (topk_ids && (reinterpret_cast<uintptr_t>(topk_ids) & 3u)) ||
+      (topk_w && (reinterpret_cast<uintptr_t>(topk_w) & 3u)))
+    return SI_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < blayer_geom(*L, n_tokens).bytes)
+    return SI_ERR_WORKSPACE;
+  return blayer_enqueue(*L, n_tokens, mode, x, residual, sum_out, norm_out, topk_ids, topk_w,
+                        routed_out, workspace, static_cast<uint32_t *>(workspace),
+                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t si_moe_stack_batched_workspace_bytes(const si_moe_layer *layers, int n_layers,
+                                                       int n_tokens) {
+  if (!layers || n_layers < 1) return 0;
+  size_t off = sizeof(WsHeader);
+  for (int l = 0; l < n_layers; ++l) {
+    if (blayer_check(layers[l], n_tokens) != SI_OK) return 0;
+    off += bstack_layer_bytes(layers[l], n_tokens);
+  }
+  return off;
+}
+
+extern "C" si_status si_moe_stack_graph_create_batched(const si_moe_layer *layers, int n_layers,
+                                                       int n_tokens, int mode, const void *x_in,
+                                                       void *y_out, void *sum_out, int32_t *ids_out,
+                                                       void *workspace, size_t workspace_bytes,
+                                                       void *stream, si_graph **graph_out) {
+  if (!layers || n_layers < 1 || n_tokens < 1 || !x_in || !y_out || !graph_out) return SI_ERR_INVALID_ARG;
+  if (mode != SI_FFN_AUTO && mode != SI_FFN_INT8 && mode != SI_FFN_TENSOR) return SI_ERR_INVALID_ARG;
+  *graph_out = nullptr;
+  const int H = layers[0].hidden, k = layers[0].top_k;
+  for (int l = 0; l < n_layers; ++l) {
+    const si_status st = blayer_check(layers[l], n_tokens);
+    if (st != SI_OK) return st;
+    if (layers[l].hidden != H || layers[l].top_k != k) return SI_ERR_INVALID_ARG;
+  }
+  if (!aligned16(x_in) || !aligned16(y_out) || (sum_out && !aligned16(sum_out)) ||
+      (ids_out && (reinterpret_cast<uintptr_t>(ids_out) & 3u)))
+    return SI_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) ||
+      workspace_bytes < si_moe_stack_batched_workspace_bytes(layers, n_layers, n_tokens))
+    return SI_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (preload_router() != cudaSuccess || preload_batched() != cudaSuccess || preload_norm() != cudaSuccess)
+    return SI_ERR_CUDA;
+  cudaStreamCaptureStatus cs;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return SI_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return SI_ERR_INVALID_ARG;
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return SI_ERR_CUDA;
+  uint8_t *base = static_cast<uint8_t *>(workspace);
+  uint32_t *status = reinterpret_cast<uint32_t *>(base);
+  si_status st = SI_OK;
+  const void *x = x_in, *res = x_in;
+  size_t off = sizeof(WsHeader);
+  for (int l = 0; l < n_layers && st == SI_OK; ++l) {
+    const si_moe_layer &L = layers[l];
+    uint8_t *lws = base + off;
+    const size_t lb = blayer_geom(L, n_tokens).bytes;
+    void *sum = lws + lb;
+    void *y = lws + lb + 2 * static_cast<size_t>(n_tokens) * H;
+    if (l == n_layers - 1) {
+      y = y_out;
+      if (sum_out) sum = sum_out;
+    }
+    int32_t *ids = ids_out ? ids_out + static_cast<size_t>(l) * n_tokens * k : nullptr;
+    st = blayer_enqueue(L, n_tokens, mode, x, res, sum, y, ids, nullptr, nullptr, lws, status, s);
+    x = y;
+    res = sum;
+    off += bstack_layer_bytes(L, n_tokens);
+  }
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+  if (st != SI_OK || ec != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return st != SI_OK ? st : SI_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return SI_ERR_CUDA;
+  }
+  si_graph *g = new (std::nothrow) si_graph{graph, exec, 0};
+  if (!g) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(graph);
+    return SI_ERR_CUDA;
+  }
+  *graph_out = g;
+  return SI_OK;
+}
+
 extern "C" int si_graph_is_persistent(const si_graph *graph) {
   return graph ? graph->persistent : -1;
 }

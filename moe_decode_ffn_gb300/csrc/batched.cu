@@ -854,33 +854,22 @@ cudaError_t preload_batched() {
   return cudaSuccess;
 }
 
-}  // namespace si
-
-using namespace si;
-
-extern "C" size_t si_moe_ffn_batched_workspace_bytes(const si_moe_layer *L, int n_tokens) {
-  if (!L || batched_check(*L, n_tokens) != SI_OK) return 0;
-  return batched_geom(*L, n_tokens).bytes;
+size_t batched_workspace_bytes(const si_moe_layer &L, int n_tokens) {
+  return batched_geom(L, n_tokens).bytes;
 }
+si_status batched_validate(const si_moe_layer &L, int n_tokens) { return batched_check(L, n_tokens); }
 
-extern "C" si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int mode,
-                                        const void *x, const int32_t *topk_ids,
-                                        const float *topk_w, void *routed_out, void *workspace,
-                                        size_t workspace_bytes, void *stream) {
-  if (!L || !x || !topk_ids || !topk_w || !routed_out) return SI_ERR_INVALID_ARG;
-  if (mode != 0 && mode != 1 && mode != 2) return SI_ERR_INVALID_ARG;
+// Enqueue the batched routed FFN (arguments checked by the caller) into
+// workspace `workspace`, device errors reported to `status`.
+si_status batched_launch(const si_moe_layer *L, int n_tokens, int mode, const void *x,
+                         const int32_t *topk_ids, const float *topk_w, void *routed_out,
+                         void *workspace, uint32_t *status, cudaStream_t s) {
   // AUTO takes the integer path: measured faster than the tensor-core path at
   // every supported batch (1..128 tokens over 128 experts leave at most ~8
   // tokens per selected expert, so dequantising the weights to fp16 costs more
   // than the MMA saves).
   const bool tensor = mode == 2;
-  const si_status st = batched_check(*L, n_tokens);
-  if (st != SI_OK) return st;
-  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
-      (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(routed_out) & 1u))
-    return SI_ERR_INVALID_ARG;
   const BatchedGeom g = batched_geom(*L, n_tokens);
-  if (!workspace || !aligned256(workspace) || workspace_bytes < g.bytes) return SI_ERR_WORKSPACE;
   uint8_t *base = static_cast<uint8_t *>(workspace);
   BatchedParams p{};
   p.x = static_cast<const __nv_bfloat16 *>(x);
@@ -902,11 +891,10 @@ extern "C" si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int
   p.hrec = base + g.off_hrec;
   p.y = reinterpret_cast<float *>(base + g.off_y);
   p.routed = static_cast<__nv_bfloat16 *>(routed_out);
-  p.status = reinterpret_cast<uint32_t *>(base);
+  p.status = status;
   p.tensor = tensor ? 1 : 0;
   p.xh = reinterpret_cast<__half *>(base + g.off_xh);
   p.hh = reinterpret_cast<__half *>(base + g.off_hh);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (tensor) {
     if (L->hidden % 128 || L->inter % 256) return SI_ERR_UNSUPPORTED;
     const int max_active = n_tokens * L->top_k < L->n_experts ? n_tokens * L->top_k : L->n_experts;
@@ -939,6 +927,32 @@ extern "C" si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel, dim3((L->hidden + 255) / 256, n_tokens), dim3(256), 0, s, p);
   return cuda_status(e);
+}
+
+}  // namespace si
+
+using namespace si;
+
+extern "C" size_t si_moe_ffn_batched_workspace_bytes(const si_moe_layer *L, int n_tokens) {
+  if (!L || batched_check(*L, n_tokens) != SI_OK) return 0;
+  return batched_geom(*L, n_tokens).bytes;
+}
+
+extern "C" si_status si_moe_ffn_batched(const si_moe_layer *L, int n_tokens, int mode,
+                                        const void *x, const int32_t *topk_ids,
+                                        const float *topk_w, void *routed_out, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+  if (!L || !x || !topk_ids || !topk_w || !routed_out) return SI_ERR_INVALID_ARG;
+  if (mode != 0 && mode != 1 && mode != 2) return SI_ERR_INVALID_ARG;
+  const si_status st = batched_check(*L, n_tokens);
+  if (st != SI_OK) return st;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(routed_out) & 1u))
+    return SI_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < batched_geom(*L, n_tokens).bytes)
+    return SI_ERR_WORKSPACE;
+  return batched_launch(L, n_tokens, mode, x, topk_ids, topk_w, routed_out, workspace,
+                        static_cast<uint32_t *>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 extern "C" si_status si_test_umma_f16(const void *a, const void *b, int n, int k, float *out,

@@ -488,15 +488,20 @@ SI_DEV float q4k_half_dot(const uint4 *w, const uint4 *a, const float *da, const
 }
 
 SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const float *sa) {
-  int isum[8], sc[8], mn[8];
+  int isum[8];
   uint32_t dd, sw[3];
   q4k_isums(w, a, isum, dd, sw);
-  q4k_unpack_scales(sw, sc, mn);
+  // scales / mins of sub-blocks 0..3 and 4..7, one per byte
+  const uint32_t sc0 = sw[0] & 0x3F3F3F3Fu, mn0 = sw[1] & 0x3F3F3F3Fu;
+  const uint32_t sc1 = (sw[2] & 0x0F0F0F0Fu) | ((sw[0] >> 2) & 0x30303030u);
+  const uint32_t mn1 = ((sw[2] >> 4) & 0x0F0F0F0Fu) | ((sw[1] >> 2) & 0x30303030u);
   float acc_d = 0.f, acc_m = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    acc_d = fmaf(static_cast<float>(sc[j] * isum[j]), da[j], acc_d);
-    acc_m = fmaf(static_cast<float>(mn[j]), sa[j], acc_m);
+    const int sc = static_cast<int>(((j < 4 ? sc0 : sc1) >> (8 * (j & 3))) & 0xFFu);
+    const int mn = static_cast<int>(((j < 4 ? mn0 : mn1) >> (8 * (j & 3))) & 0xFFu);
+    acc_d = fmaf(static_cast<float>(sc * isum[j]), da[j], acc_d);
+    acc_m = fmaf(static_cast<float>(mn), sa[j], acc_m);
   }
   const float d = half_bits_to_float(static_cast<uint16_t>(dd & 0xFFFF));
   const float dmin = half_bits_to_float(static_cast<uint16_t>(dd >> 16));

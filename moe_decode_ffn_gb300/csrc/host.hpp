@@ -99,6 +99,14 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
                      const float *wts, void *routed, void *shared, void *ws, uint32_t *status,
                      cudaStream_t s, bool gateup_only = false);
 
+// ---- batched routed FFN (batched.cu): shape check, workspace, enqueue
+si_status batched_validate(const si_moe_layer &L, int n_tokens);
+size_t batched_workspace_bytes(const si_moe_layer &L, int n_tokens);
+si_status batched_launch(const si_moe_layer *L, int n_tokens, int mode, const void *x,
+                         const int32_t *topk_ids, const float *topk_w, void *routed_out,
+                         void *workspace, uint32_t *status, cudaStream_t s);
+cudaError_t preload_batched();
+
 // ---- test export of the batched helpers' integer block sums (batched.cu)
 si_status batched_test_dots(const void *w, int rows, int k, const void *a, int n_vec, int halves,
                             int32_t *out, cudaStream_t s);

@@ -54,11 +54,11 @@ constexpr int kArmT = 480;          // the thread that arms the prefetch barrier
 // a line polled by every block delays the store that the readers wait for
 // (the polls queue ahead of it at the line's L2 slice), so each copy has only
 // G / kXRep readers. The copies cost one warp-wide store instead of one.
-constexpr int kXRep = 8;
+constexpr int kXRep = 2;
 
 // The 64 rows of a gate/up unit arrive in kGuGroups groups of 32 / kGuGroups
 // gate rows and as many up rows, one bulk copy per matrix and group.
-constexpr int kGuGroups = 2;
+constexpr int kGuGroups = 4;
 constexpr int kGuRows = 32 / kGuGroups;
 // mbarriers of a stack block: 0, 1 the routing-independent prefetch (router
 // rows, shared-gate vector, norm weights) by iteration parity; then one per
@@ -195,10 +195,11 @@ SI_DEV float sigma_dot(const __nv_bfloat16 *w, const float *y, int n, float *red
   float acc = 0.f;
 #pragma unroll 1
   for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
-    float wv[8];
+    float wv[8], yv[8];
     Load8<__nv_bfloat16>::run(w + i0, wv);
+    Load8<float>::run(y + i0, yv);   // two 16-byte reads (no 8-way bank conflict)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], y[i0 + i], acc);
+    for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], yv[i], acc);
   }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
@@ -260,13 +261,18 @@ SI_DEV bool fold_sum(const StackParams &p, const uint64_t *ol, uint32_t tag, flo
     for (int r0 = 8 * threadIdx.x; r0 < H; r0 += 2048) {
       const float4 t0 = *reinterpret_cast<const float4 *>(tbuf + r0);
       const float4 t1 = *reinterpret_cast<const float4 *>(tbuf + r0 + 4);
+      const float4 c0 = *reinterpret_cast<const float4 *>(resid + r0);
+      const float4 c1 = *reinterpret_cast<const float4 *>(resid + r0 + 4);
       const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+      const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      float sv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float sv = bf16_round(tv[e] + resid[r0 + e]);
-        ss = fmaf(sv, sv, ss);
-        resid[r0 + e] = sv;
+        sv[e] = bf16_round(tv[e] + cv[e]);
+        ss = fmaf(sv[e], sv[e], ss);
       }
+      *reinterpret_cast<float4 *>(resid + r0) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+      *reinterpret_cast<float4 *>(resid + r0 + 4) = make_float4(sv[4], sv[5], sv[6], sv[7]);
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
@@ -325,15 +331,16 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   const int tr_sel = g_stk_trace_phase;
 #endif
   // ---- shared memory --------------------------------------------------------
+  static_assert(kNumBars <= 16, "barrier area holds 16 barriers");
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);     // kNumBars
-  uint32_t *s_arm = reinterpret_cast<uint32_t *>(smem + 64);
-  uint32_t *s_base = reinterpret_cast<uint32_t *>(smem + 68);
-  float *red = reinterpret_cast<float *>(smem + 128);      // [16]
-  float *s_part = reinterpret_cast<float *>(smem + 192);   // [2][8] router partials per warp
-  float *s_wts = reinterpret_cast<float *>(smem + 256);    // [8]
-  uint64_t *s_sel = reinterpret_cast<uint64_t *>(smem + 320);
-  uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + 384);   // [64]
-  float *h_s = reinterpret_cast<float *>(smem + 896);      // [32]
+  uint32_t *s_arm = reinterpret_cast<uint32_t *>(smem + 128);
+  uint32_t *s_base = reinterpret_cast<uint32_t *>(smem + 132);
+  float *red = reinterpret_cast<float *>(smem + 192);      // [16]
+  float *s_part = reinterpret_cast<float *>(smem + 256);   // [2][8] router partials per warp
+  float *s_wts = reinterpret_cast<float *>(smem + 320);    // [8]
+  uint64_t *s_sel = reinterpret_cast<uint64_t *>(smem + 384);
+  uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + 448);   // [64]
+  float *h_s = reinterpret_cast<float *>(smem + 960);      // [32]
   StackLayerPtrs *s_layers = reinterpret_cast<StackLayerPtrs *>(smem + p.sm.layers);
   float *resid = reinterpret_cast<float *>(smem + p.sm.resid);
   float *y = reinterpret_cast<float *>(smem + p.sm.y);

@@ -735,6 +735,15 @@ def run_profile_case(args):
     import moe_decode_ffn_gb300 as m
 
     m.build()
+    if args.quant:
+        n = args.quant
+        x = gen.to_bf16(gen.normal([gen.stream_key(args.seed, 77, n)], n, 0.0, 1.0, "cuda")[0])
+        q = torch.empty(n // 32 * 36, dtype=torch.uint8, device="cuda")
+        for _ in range(args.launches):
+            m.si_quantize_q8_1(x, out=q)
+        torch.cuda.synchronize()
+        print(f"quantize n={n} launches={args.launches}")
+        return 0
     if args.batched:
         T = args.batched
         L = m.device_layer(gen.Q4K_LAYER_128E, args.seed, 0)
@@ -792,6 +801,7 @@ def main():
     pc.add_argument("--spec", default="q4k", choices=["q4k", "q4k_q8_0", "bf16"])
     pc.add_argument("--batched", type=int, default=0, help="T: the batched FFN of T tokens instead")
     pc.add_argument("--mode", default="tensor", choices=["tensor", "int8"])
+    pc.add_argument("--quant", type=int, default=0, help="n: the Q8_1 quantiser on n bf16 values instead")
     args = ap.parse_args()
     if args.profile_case:
         return run_profile_case(args)

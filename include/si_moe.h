@@ -212,6 +212,33 @@ si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, const void *x,
                             size_t workspace_bytes, void *stream);
 
 /*
+ * Expert-parallel partitions of si_moe_ffn_decode (the routed expert weights
+ * read per token are what partitions: "Q4_K shared-expert FFN kernels +
+ * Q8_0/Q5_K->Q4_K requant of the MoE FFN stage", Summary). A partition owns
+ * the experts [e0, e1); every partition computes, for one token,
+ *   slot_y[r][:] = y_r = D_e h_e (fp32 [H], the down GEMV of slot r's expert
+ *                  e, as si_moe_ffn_decode forms it) if e lies in [e0, e1),
+ *                  and 0 (all bits zero) otherwise,
+ * and the shared expert in full (shared_out, replicated). Summing the
+ * partitions' slot_y as 32-bit integers (each slot is non-zero in exactly one
+ * partition) reproduces the single-partition values bit for bit, and
+ * si_moe_combine_slots then forms routed exactly as si_moe_ffn_decode does.
+ *   e0, e1     0 <= e0 <= e1 <= E; Q4_K routed experts only (SI_ERR_UNSUPPORTED otherwise)
+ *   slot_y     device fp32 [k][H]; shared_out device bf16 [H] (if the layer has a shared expert)
+ *   workspace  si_moe_ffn_workspace_bytes(L, 1) bytes
+ * Experts outside [e0, e1) are neither read nor computed.
+ *
+ * si_moe_combine_slots: routed[j] = bf16(sum_r topk_w[r] * slot_y[r][j]),
+ * the fp32 fma chain in rank order (k <= 8), on device buffers.
+ */
+si_status si_moe_ffn_decode_ep(const si_moe_layer *L, int e0, int e1, const void *x,
+                               const void *x_q8_1, const int32_t *topk_ids, float *slot_y,
+                               void *shared_out, void *workspace, size_t workspace_bytes,
+                               void *stream);
+si_status si_moe_combine_slots(const float *slot_y, const float *topk_w, int k, int hidden,
+                               void *routed_out, void *stream);
+
+/*
  * si_moe_ffn_batched - routed experts for n_tokens tokens with per-token
  * routing (not on the pages, which measure batch 1; the per-token arithmetic
  * is si_moe_ffn_decode's).

@@ -59,6 +59,9 @@ SIGNATURES = {
     "si_moe_ffn_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
     "si_moe_ffn_decode": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _vp, _sz, _vp]),
+    "si_moe_ffn_decode_ep": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _sz, _vp]),
+    "si_moe_combine_slots": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp]),
     "si_moe_ffn_batched_workspace_bytes": (_sz, [ctypes.POINTER(SiMoeLayer), _i32]),
     "si_moe_ffn_batched": (_i32, [ctypes.POINTER(SiMoeLayer), _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                   _sz, _vp]),
@@ -291,6 +294,32 @@ def si_moe_ffn_decode(layer: Layer, x: torch.Tensor, ids: torch.Tensor, w: torch
         _cuda(routed, "routed"), _opt(shared, "shared"), _cuda(ws, "ws"), ws.numel(),
         _stream(stream)), "si_moe_ffn_decode")
     return routed, shared
+
+
+def si_moe_ffn_decode_ep(layer: Layer, e0: int, e1: int, x: torch.Tensor, ids: torch.Tensor,
+                         ws: torch.Tensor | None = None, stream=None):
+    """The slots of experts in [e0, e1) for one token: -> (slot_y fp32 [k, H]
+    with zeros for the other slots, shared bf16 [H] or None)."""
+    H, k = layer.spec.hidden, layer.spec.top_k
+    slot_y = torch.empty(k, H, dtype=torch.float32, device=x.device)
+    shared = torch.empty(H, dtype=torch.bfloat16, device=x.device) if layer.spec.shared_inter else None
+    if ws is None:
+        ws = workspace(ffn_workspace_bytes(layer), x.device)
+    _check(library().si_moe_ffn_decode_ep(
+        layer.ref, e0, e1, _shaped(x, "x", H, _BF16), None, _shaped(ids, "ids", k, _I32),
+        _cuda(slot_y, "slot_y"), _opt(shared, "shared"), _cuda(ws, "ws"), ws.numel(), _stream(stream)),
+        "si_moe_ffn_decode_ep")
+    return slot_y, shared
+
+
+def si_moe_combine_slots(slot_y: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
+    """routed = bf16(sum_r w[r] * slot_y[r]) in rank order: slot_y fp32 [k, H], w fp32 [k]."""
+    k, H = slot_y.shape
+    routed = torch.empty(H, dtype=torch.bfloat16, device=slot_y.device)
+    _check(library().si_moe_combine_slots(_shaped(slot_y, "slot_y", k * H, _F32), _shaped(w, "w", k, _F32),
+                                          k, H, _cuda(routed, "routed"), _stream(stream)),
+           "si_moe_combine_slots")
+    return routed
 
 
 SI_FFN_AUTO, SI_FFN_INT8, SI_FFN_TENSOR = 0, 1, 2

@@ -56,6 +56,7 @@ struct GateUpParams {
   int8_t *hq;               // [k*I + Is] codes
   float *hd, *hs;           // [(k*I + Is)/32] block scale / sum (fp16 values)
   float *hf;                // [k*I + Is] h in fp32
+  int e0, e1;               // routed experts computed: [e0, e1) (all of them: [0, E))
   uint32_t *status;
 };
 
@@ -71,6 +72,8 @@ struct DownParams {
   const int8_t *hq;
   const float *hd, *hs, *hf;
   __nv_bfloat16 *routed, *shared;
+  int e0, e1;                 // routed experts computed: [e0, e1)
+  float *slot_y;              // nullable: [k][H] fp32 slot outputs instead of `routed`
   uint32_t *status;
 };
 
@@ -157,10 +160,16 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_q_kernel(GateUpParams p)
   grid_dep_launch();
   SI_TRACE_MARK(1, 2);
 
+  __shared__ int s_owned;
   if (!shared && threadIdx.x == 0) {
     const int e = load_expert(p.ids, slot, p.E, p.status);
+    s_owned = e >= p.e0 && e < p.e1;
     const size_t row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(hb) * 32;
-    issue(p.wg + row0 * rb, p.wu + row0 * rb);
+    if (s_owned) issue(p.wg + row0 * rb, p.wu + row0 * rb);
+  }
+  if (!shared) {
+    __syncthreads();
+    if (!s_owned) return;   // an expert another partition computes: nothing requested, nothing to wait for
   }
   SI_TRACE_MARK(1, 3);
 
@@ -250,23 +259,28 @@ __global__ void __launch_bounds__(kDownQThreads, 2) down_q_kernel(DownParams p) 
   SI_TRACE_MARK(2, 0);
   const int j0 = blockIdx.x * p.J;
   const int nrows = min(p.J, p.H - j0);
+  __shared__ int s_own[8];   // slot r's expert lies in [e0, e1)
   if (threadIdx.x == 0) {
     mbar_init(bar, n_slots);
     fence_mbar_init();
   }
   __syncthreads();
   // Expert ids and weights come from the router (two kernels back): one
-  // thread per slot reads its id and requests that expert's rows at once.
+  // thread per slot reads its id and requests that expert's rows at once
+  // (a slot of an expert outside [e0, e1) only arrives).
   if (threadIdx.x < n_slots) {
     const uint64_t pol = policy_evict_first();
     const int r = threadIdx.x;
     if (r < p.k) {
       const int e = load_expert(p.ids, r, p.E, p.status);
-      wts[r] = __ldcg(p.wts + r);
-      const uint32_t br = static_cast<uint32_t>(nrows) * p.rbd_r;
+      const bool own = e >= p.e0 && e < p.e1;
+      s_own[r] = own;
+      wts[r] = p.wts ? __ldcg(p.wts + r) : 0.f;
+      const uint32_t br = own ? static_cast<uint32_t>(nrows) * p.rbd_r : 0u;
       mbar_arrive_expect_tx(bar, br);
-      bulk_g2s_evict_first(wbuf + static_cast<size_t>(r) * p.J * p.rbd_r,
-                           p.wd + (static_cast<size_t>(e) * p.H + j0) * p.rbd_r, br, bar, pol);
+      if (own)
+        bulk_g2s_evict_first(wbuf + static_cast<size_t>(r) * p.J * p.rbd_r,
+                             p.wd + (static_cast<size_t>(e) * p.H + j0) * p.rbd_r, br, bar, pol);
     } else {
       const uint32_t bs = static_cast<uint32_t>(nrows) * p.rbd_s;
       mbar_arrive_expect_tx(bar, bs);
@@ -324,6 +338,10 @@ __global__ void __launch_bounds__(kDownQThreads, 2) down_q_kernel(DownParams p) 
       q = (u - items_r) % P_s;
     }
     if (jl >= nrows) continue;
+    if (r < p.k && !s_own[r]) {   // computed by another partition
+      part[(r * p.J + jl) * P_max + q] = 0.f;
+      continue;
+    }
     const bool sh = kShared && r == p.k;
     const uint8_t *row = wbuf + static_cast<size_t>(r) * p.J * p.rbd_r +
                          static_cast<size_t>(jl) * (sh ? p.rbd_s : p.rbd_r);
@@ -364,9 +382,16 @@ __global__ void __launch_bounds__(kDownQThreads, 2) down_q_kernel(DownParams p) 
   __syncthreads();
   if (threadIdx.x < nrows) {
     const int jl = threadIdx.x;
-    float acc = 0.f;
-    for (int r = 0; r < p.k; ++r) acc = fmaf(wts[r], ys[r * p.J + jl], acc);
-    p.routed[j0 + jl] = __float2bfloat16_rn(acc);
+    if (p.slot_y) {
+      // expert-parallel form: every slot's output (0 bits for the slots of
+      // other partitions), combined after the partitions' outputs are summed
+      for (int r = 0; r < p.k; ++r)
+        p.slot_y[static_cast<size_t>(r) * p.H + j0 + jl] = s_own[r] ? ys[r * p.J + jl] : 0.f;
+    } else {
+      float acc = 0.f;
+      for (int r = 0; r < p.k; ++r) acc = fmaf(wts[r], ys[r * p.J + jl], acc);
+      p.routed[j0 + jl] = __float2bfloat16_rn(acc);
+    }
     if (kShared) p.shared[j0 + jl] = __float2bfloat16_rn(sigma * ys[p.k * p.J + jl]);
   }
   SI_TRACE_MARK(2, 7);
@@ -620,6 +645,18 @@ __global__ void q4k_block_dots_kernel(const uint8_t *w, int rows, int k, const u
   }
 }
 
+// routed[j] = bf16(sum_r w[r] * y[r][j]): the fp32 fma chain over the slots
+// in rank order, the down kernel's combine, on slot outputs gathered from
+// expert partitions.
+__global__ void __launch_bounds__(256) combine_slots_kernel(const float *y, const float *w, int k,
+                                                            int H, __nv_bfloat16 *routed) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= H) return;
+  float acc = 0.f;
+  for (int r = 0; r < k; ++r) acc = fmaf(__ldg(w + r), __ldg(y + static_cast<size_t>(r) * H + j), acc);
+  routed[j] = __float2bfloat16_rn(acc);
+}
+
 // Test export: exact per-(vector, row, 32-block) integer sums of the
 // single-token helpers: whole Q4_K super-blocks (gate/up), Q4_K halves
 // (routed and shared down) or Q5_K halves (the Q5_K routed down).
@@ -772,7 +809,7 @@ cudaError_t preload_ffn() {
 
 si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, const int32_t *ids,
                      const float *wts, void *routed, void *shared, void *ws, uint32_t *status,
-                     cudaStream_t s, bool gateup_only) {
+                     cudaStream_t s, bool gateup_only, int e0, int e1, float *slot_y) {
   const FfnGeom g = ffn_geom(L);
   const bool sh = L.shared_inter > 0;
   uint8_t *base = static_cast<uint8_t *>(ws);
@@ -793,6 +830,8 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
   gp.hd = reinterpret_cast<float *>(base + g.off_hd);
   gp.hs = reinterpret_cast<float *>(base + g.off_hs);
   gp.hf = reinterpret_cast<float *>(base + g.off_hf);
+  gp.e0 = e0;
+  gp.e1 = e1 < 0 ? L.n_experts : e1;
   gp.status = status;
 
   const int sms = sm_count();
@@ -810,6 +849,9 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
   dp.hq = gp.hq; dp.hd = gp.hd; dp.hs = gp.hs; dp.hf = gp.hf;
   dp.routed = static_cast<__nv_bfloat16 *>(routed);
   dp.shared = static_cast<__nv_bfloat16 *>(shared);
+  dp.e0 = gp.e0;
+  dp.e1 = gp.e1;
+  dp.slot_y = slot_y;
   dp.status = gp.status;
   const int down_ctas = (L.hidden + dp.J - 1) / dp.J;
   if (L.expert_type == SI_BF16 && !gateup_only) {
@@ -869,6 +911,38 @@ extern "C" si_status si_moe_ffn_decode(const si_moe_layer *L, int n_tokens, cons
     return SI_ERR_WORKSPACE;
   return ffn_launch(*L, x, x_q8_1, topk_ids, topk_w, routed_out, shared_out, workspace,
                     static_cast<uint32_t *>(workspace), static_cast<cudaStream_t>(stream), false);
+}
+
+extern "C" si_status si_moe_ffn_decode_ep(const si_moe_layer *L, int e0, int e1, const void *x,
+                                          const void *x_q8_1, const int32_t *topk_ids, float *slot_y,
+                                          void *shared_out, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+  if (!L || !x || !topk_ids || !slot_y) return SI_ERR_INVALID_ARG;
+  const si_status st = ffn_check(*L);
+  if (st != SI_OK) return st;
+  if (L->expert_type != SI_Q4_K) return SI_ERR_UNSUPPORTED;
+  if (e0 < 0 || e1 < e0 || e1 > L->n_experts) return SI_ERR_INVALID_ARG;
+  if (L->shared_inter > 0 && !shared_out) return SI_ERR_INVALID_ARG;
+  if (!aligned16(x) || (x_q8_1 && (reinterpret_cast<uintptr_t>(x_q8_1) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(slot_y) & 3u) ||
+      (shared_out && (reinterpret_cast<uintptr_t>(shared_out) & 1u)))
+    return SI_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < ffn_geom(*L).bytes)
+    return SI_ERR_WORKSPACE;
+  return ffn_launch(*L, x, x_q8_1, topk_ids, nullptr, nullptr, shared_out, workspace,
+                    static_cast<uint32_t *>(workspace), static_cast<cudaStream_t>(stream), false, e0, e1,
+                    slot_y);
+}
+
+extern "C" si_status si_moe_combine_slots(const float *slot_y, const float *topk_w, int k, int hidden,
+                                          void *routed_out, void *stream) {
+  if (!slot_y || !topk_w || !routed_out || k < 1 || k > 8 || hidden < 1) return SI_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(slot_y) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) ||
+      (reinterpret_cast<uintptr_t>(routed_out) & 1u))
+    return SI_ERR_INVALID_ARG;
+  return cuda_status(launch_pdl(combine_slots_kernel, dim3((hidden + 255) / 256), dim3(256), 0,
+                                static_cast<cudaStream_t>(stream), slot_y, topk_w, k, hidden,
+                                static_cast<__nv_bfloat16 *>(routed_out)));
 }
 
 extern "C" si_status si_moe_ffn_gateup(const si_moe_layer *L, int n_tokens, const void *x,

@@ -95,9 +95,12 @@ struct FfnGeom {
 };
 FfnGeom ffn_geom(const si_moe_layer &L);
 si_status ffn_check(const si_moe_layer &L);
+// e0, e1: the routed experts computed ([0, E) by default: e1 < 0); slot_y
+// non-null: per-slot fp32 outputs [k][H] instead of the combined `routed`.
 si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, const int32_t *ids,
                      const float *wts, void *routed, void *shared, void *ws, uint32_t *status,
-                     cudaStream_t s, bool gateup_only = false);
+                     cudaStream_t s, bool gateup_only = false, int e0 = 0, int e1 = -1,
+                     float *slot_y = nullptr);
 
 // ---- batched routed FFN (batched.cu): shape check, workspace, enqueue
 si_status batched_validate(const si_moe_layer &L, int n_tokens);

@@ -353,7 +353,8 @@ si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n_layers, in
  *                        whole stack ("perf(qwen3.6): fuse decode kernel
  *                        launches", Summary: decode is launch bound); returns
  *                        SI_ERR_UNSUPPORTED unless every layer has Q4_K routed
- *                        experts, a Q4_K or no shared expert and a bf16 router,
+ *                        experts, a Q4_K, Q8_0 or no shared expert (one format
+ *                        for all layers) and a bf16 router,
  *                        all layers share one shape with H a multiple of 2048
  *                        (<= 4096), E even (<= 256), top_k <= 8, n_layers <= 128,
  *                        and one block per SM covers every gate/up unit of 32

@@ -7,37 +7,57 @@
 // (sparkinfer PR #273), Summary item 2: routed + shared + residual folded into
 // one add+RMSNorm, bit-identical to the residual add followed by the 2-input
 // norm.
+#include <algorithm>
+
 #include "common.cuh"
 #include "host.hpp"
 
 namespace si {
 
-// One thread per 8 values; 4 consecutive lanes form one 32-value block.
+// One thread per 8 values; 4 consecutive lanes form one 32-value block. A
+// grid-stride loop over warps' 256-value spans, kQuantUnroll spans per pass
+// with all their 16-byte loads issued before the first encode: one load per
+// thread in flight left HBM idle between a block's load and its store.
+constexpr int kQuantUnroll = 4;
 template <typename T>
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const T *__restrict__ x, int64_t n,
                                                             uint8_t *__restrict__ y) {
   grid_dep_wait();
   grid_dep_launch();
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t groups = n / 8;
-  const bool live = g < groups;
-  float v[8];
-  if (live) {
-    Load8<T>::run(x + 8 * g, v);
-  } else {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  // the loop bound is the warp's first group, so whole warps run every pass
+  // (the encoder shuffles across 4 lanes)
+  for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); w0 < groups;
+       w0 += kQuantUnroll * stride) {
+    float v[kQuantUnroll][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t g = w0 + u * stride + lane;
+      if (g < groups) {
+        Load8<T>::run(x + 8 * g, v[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t g = w0 + u * stride + lane;
+      uint32_t lo, hi;
+      uint16_t d16, s16;
+      q8_1_encode_4lanes(v[u], lo, hi, d16, s16);
+      if (g < groups) {
+        uint8_t *blk = y + (g >> 2) * kQ81Bytes;
+        const int part = static_cast<int>(g & 3);
+        uint32_t *q = reinterpret_cast<uint32_t *>(blk + 4 + 8 * part);  // 4-byte aligned
+        q[0] = lo;
+        q[1] = hi;
+        if (part == 0) *reinterpret_cast<uint32_t *>(blk) = d16 | (static_cast<uint32_t>(s16) << 16);
+      }
+    }
   }
-  uint32_t lo, hi;
-  uint16_t d16, s16;
-  q8_1_encode_4lanes(v, lo, hi, d16, s16);
-  if (!live) return;
-  uint8_t *blk = y + (g >> 2) * kQ81Bytes;
-  const int part = static_cast<int>(g & 3);
-  uint32_t *q = reinterpret_cast<uint32_t *>(blk + 4 + 8 * part);  // 4-byte aligned
-  q[0] = lo;
-  q[1] = hi;
-  if (part == 0) *reinterpret_cast<uint32_t *>(blk) = d16 | (static_cast<uint32_t>(s16) << 16);
 }
 
 // ---------------------------------------------------------------------------
@@ -174,7 +194,10 @@ extern "C" si_status si_quantize_q8_1(const void *x, si_dtype x_type, int64_t n,
   if (x_type != SI_F32 && x_type != SI_BF16) return SI_ERR_UNSUPPORTED;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y_q8_1) & 3u)) return SI_ERR_INVALID_ARG;
   const int64_t groups = n / 8;
-  const dim3 grid(static_cast<unsigned>((groups + 255) / 256));
+  // at most 8 resident blocks of 256 threads per SM; each thread then takes
+  // kQuantUnroll groups per pass
+  const int64_t need = (groups + 256 * kQuantUnroll - 1) / (256 * kQuantUnroll);
+  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(need, 8 * static_cast<int64_t>(sm_count()))));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (x_type == SI_F32)

@@ -83,7 +83,7 @@ struct StackParams {
   const StackLayerPtrs *layers;
   int n_layers, n_tokens;
   int H, E, k, I, Is;         // Is == 0: no shared expert
-  int rb, rbd, rbsd;          // row bytes: gate/up rows (H), routed down rows (I), shared down rows
+  int rb, rbs, rbd, rbsd;     // row bytes: routed / shared gate/up rows (H), routed / shared down rows
   int J;                      // down output rows per block (even)
   int np3;                    // X3: pairs of elements per block slot (ceil(J / 4))
   float eps;
@@ -317,12 +317,21 @@ template <int SFMT>
 __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr bool kShared = SFMT != 0;
+  // A Q8_0 shared expert: its gate/up unit (64 rows of H / 32 blocks of 34
+  // bytes) is about twice a Q4_K unit, so in the block that owns it the
+  // unit's buffer also holds the routed down rows, which arrive only after
+  // the unit's dot products are done; the next unit is requested once the
+  // down rows are consumed.
+  constexpr bool kShQ80 = SFMT == SI_Q8_0;
   const int G = gridDim.x, c = blockIdx.x;
   const int H = p.H, I = p.I, Is = kShared ? p.Is : 0, k = p.k, E = p.E;
   const int nsb = H / kQKK;
   const int units_r = k * I / 32, units = units_r + Is / 32;
   const int nsb_r = I / kQKK, nsb_s = Is / kQKK;
-  const int P_r = 2 * nsb_r, P_s = kShared ? 2 * nsb_s : 1, P_max = P_r > P_s ? P_r : P_s;
+  // down pieces of a row: Q4_K halves of 128 weights, Q8_0 whole 256-weight
+  // groups (a Q8_0 half would start off a 16-byte boundary)
+  const int P_r = 2 * nsb_r, P_s = kShared ? (kShQ80 ? nsb_s : 2 * nsb_s) : 1,
+            P_max = P_r > P_s ? P_r : P_s;
   const int n_iters = p.n_tokens * p.n_layers;
   const int J = p.J;
   const int nvec = H / 2048;   // router: 16-byte vectors of a row per thread of the first 256
@@ -353,12 +362,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   uint8_t *pbuf = smem + p.sm.pbuf;   // [2]: router rows (2 x H bf16), w_sg (H), w_norm (H)
   const uint32_t pstr = p.sm.pbuf_stride;
   uint8_t *gu_buf = smem + p.sm.gu;   // gate [32] + up [32] rows
-  uint8_t *dn_buf = smem + p.sm.dn;   // [k][J] routed down rows
   uint8_t *sd_buf = smem + p.sm.sd;   // [J] shared down rows
 
   // ---- static assignment ----------------------------------------------------
   const int my_unit = c < units ? c : -1;
   const bool shared_unit = kShared && my_unit >= units_r;
+  const int dn_off = static_cast<int>((kShQ80 && shared_unit) ? p.sm.gu : p.sm.dn);
+  uint8_t *dn_buf = smem + dn_off;    // [k][J] routed down rows
+  const int rb_unit = shared_unit ? p.rbs : p.rb;   // row bytes of this block's gate/up unit
   const int j0 = c * J;
   const int nrows = j0 < H ? min(J, H - j0) : 0;
   const int row_a = c, row_b = c + G;   // router rows of this block
@@ -385,7 +396,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   // the P pieces of a (slot, row) lie in consecutive lanes of one warp, the
   // first of them (qq == 0) sums them in order
   int d_row[2], d_act[2], d_blk[2], d_h[2], d_dst[2], d_P[2];
-  bool d_live[2], d_first[2];
+  bool d_live[2], d_first[2], d_q80[2];
   const int items_r = k * J * P_r;
   const int items = items_r + (kShared ? J * P_s : 0);
   {
@@ -404,13 +415,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         qq = (u - items_r) - jl * P_s;
       }
       const bool sh = kShared && r == k;
-      const int sb = qq >> 1;
+      d_q80[s] = kShQ80 && sh;
+      const int sb = d_q80[s] ? qq : qq >> 1;
       d_live[s] = u < items && jl < nrows;
       d_first[s] = qq == 0;
       d_P[s] = sh ? P_s : P_r;
       d_dst[s] = r * J + jl;
-      d_row[s] = (sh ? static_cast<int>(p.sm.sd) + jl * p.rbsd
-                     : static_cast<int>(p.sm.dn) + (r * J + jl) * p.rbd) + sb * kQ4KBytes;
+      d_row[s] = (sh ? static_cast<int>(p.sm.sd) + jl * p.rbsd : dn_off + (r * J + jl) * p.rbd) +
+                 sb * (d_q80[s] ? 8 * kQ80Bytes : kQ4KBytes);
       d_act[s] = static_cast<int>(p.sm.ht_qs) + (r * nsb_r + sb) * kActSbStride;
       d_blk[s] = (r * I) / 32 + 8 * sb;
       d_h[s] = qq & 1;
@@ -446,6 +458,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   int t = 0, l = 0;   // token and layer of iteration it
   const uint32_t gbytes = static_cast<uint32_t>((nrr + (kShared ? 1 : 0) + 1) * H * 2);
   const uint32_t cbytes = static_cast<uint32_t>(kGuRows) * p.rb;   // one copy: a group's gate (or up) rows
+  const uint32_t cbytes_s = static_cast<uint32_t>(kGuRows) * p.rbs;   // the same of a shared unit
   if (threadIdx.x == kArmT && n_iters > 0) {
     // iteration 0's routing-independent bytes and shared gate/up unit
     const StackLayerPtrs &L0 = s_layers[0];
@@ -458,11 +471,11 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32;
 #pragma unroll 1
       for (int g = 0; g < kGuGroups; ++g) {
-        arm(bars, s_arm, kBarGu + g, 2 * cbytes);
-        bulk_g2s_evict_first(gu_buf + kGuRows * g * p.rb, L0.wsg + (row0 + kGuRows * g) * p.rb, cbytes,
+        arm(bars, s_arm, kBarGu + g, 2 * cbytes_s);
+        bulk_g2s_evict_first(gu_buf + kGuRows * g * p.rbs, L0.wsg + (row0 + kGuRows * g) * p.rbs, cbytes_s,
                              &bars[kBarGu + g], pol);
-        bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rb, L0.wsu + (row0 + kGuRows * g) * p.rb,
-                             cbytes, &bars[kBarGu + g], pol);
+        bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rbs, L0.wsu + (row0 + kGuRows * g) * p.rbs,
+                             cbytes_s, &bars[kBarGu + g], pol);
       }
     }
   }
@@ -681,11 +694,17 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       float acc = 0.f;
       const bool ok = mbar_wait_bounded(&bars[kBarGu + pr / kGuRows], par, p.status);
       if (ok) {
-        const uint8_t *row = gu_buf + (gm * 32 + pr) * p.rb;
-        for (int sb = lane8; sb < nsb; sb += 8)
-          acc += q4k_sb_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes),
-                            reinterpret_cast<const uint4 *>(xt.qs + sb * kActSbStride), xt.d + 8 * sb,
-                            xt.s + 8 * sb);
+        const uint8_t *row = gu_buf + (gm * 32 + pr) * rb_unit;
+        if (kShQ80 && shared_unit) {
+          for (int sb = lane8; sb < nsb; sb += 8)
+            acc += q80_sb_dot(reinterpret_cast<const uint4 *>(row + sb * 8 * kQ80Bytes),
+                              reinterpret_cast<const uint4 *>(xt.qs + sb * kActSbStride), xt.d + 8 * sb);
+        } else {
+          for (int sb = lane8; sb < nsb; sb += 8)
+            acc += q4k_sb_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes),
+                              reinterpret_cast<const uint4 *>(xt.qs + sb * kActSbStride), xt.d + 8 * sb,
+                              xt.s + 8 * sb);
+        }
       }
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
@@ -705,15 +724,16 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
                              Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
                              static_cast<uint32_t>(nrows) * p.rbd, &bars[kBarDn], pol);
       }
-      if (lane == 0 && warp >= 2 && warp < 2 + kGuGroups && shared_unit && it + 1 < n_iters) {
+      if (!kShQ80 && lane == 0 && warp >= 2 && warp < 2 + kGuGroups && shared_unit && it + 1 < n_iters) {
         // the next iteration's shared gate/up group warp - 2, armed and
         // requested by one thread
         const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];
         const int g = warp - 2;
         const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32 + kGuRows * g;
-        arm(bars, s_arm, kBarGu + g, 2 * cbytes);
-        bulk_g2s_evict_first(gu_buf + kGuRows * g * p.rb, Ln.wsg + row0 * p.rb, cbytes, &bars[kBarGu + g], pol);
-        bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rb, Ln.wsu + row0 * p.rb, cbytes,
+        arm(bars, s_arm, kBarGu + g, 2 * cbytes_s);
+        bulk_g2s_evict_first(gu_buf + kGuRows * g * p.rbs, Ln.wsg + row0 * p.rbs, cbytes_s, &bars[kBarGu + g],
+                             pol);
+        bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rbs, Ln.wsu + row0 * p.rbs, cbytes_s,
                              &bars[kBarGu + g], pol);
       }
       if (warp == 0) {
@@ -762,7 +782,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       bool okw = mbar_wait_bounded(&bars[kBarDn], par, p.status);
       if (kShared) okw &= mbar_wait_bounded(&bars[kBarSd], par, p.status);
       Q4KHalf wq;
-      if (okw && d_live[0]) q4k_half_load(reinterpret_cast<const uint4 *>(smem + d_row[0]), d_h[0], wq);
+      if (okw && d_live[0] && !d_q80[0])
+        q4k_half_load(reinterpret_cast<const uint4 *>(smem + d_row[0]), d_h[0], wq);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (g_q[s] < 0) continue;
@@ -785,9 +806,12 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
           float v = 0.f;
           if (d_live[s]) {
             const uint4 *a = reinterpret_cast<const uint4 *>(smem + d_act[s]);
-            v = s == 0 ? q4k_half_dot_loaded(wq, a, ht.d + d_blk[s], ht.s + d_blk[s], d_h[s])
-                       : q4k_half_dot(reinterpret_cast<const uint4 *>(smem + d_row[s]), a, ht.d + d_blk[s],
-                                      ht.s + d_blk[s], d_h[s]);
+            if (kShQ80 && d_q80[s])
+              v = q80_sb_dot(reinterpret_cast<const uint4 *>(smem + d_row[s]), a, ht.d + d_blk[s]);
+            else
+              v = s == 0 ? q4k_half_dot_loaded(wq, a, ht.d + d_blk[s], ht.s + d_blk[s], d_h[s])
+                         : q4k_half_dot(reinterpret_cast<const uint4 *>(smem + d_row[s]), a, ht.d + d_blk[s],
+                                        ht.s + d_blk[s], d_h[s]);
           }
           // the pieces of a (slot, row), summed in order by its first lane
           float ysum = 0.f;
@@ -842,6 +866,19 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         st_tag2(p.ol + ((static_cast<size_t>(par) * kXRep + r) * G + c) * kSlot + 2 * m, tagged(tag, 0u),
                 tagged(tag, 0u));
       }
+    }
+    if (kShQ80 && lane == 0 && warp >= 2 && warp < 2 + kGuGroups && shared_unit && it + 1 < n_iters) {
+      // the next iteration's shared gate/up group warp - 2: this block's
+      // down rows, which share its buffer, have been consumed (the barrier
+      // after the down dot products; a block without rows never used them)
+      const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];
+      const int g = warp - 2;
+      const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32 + kGuRows * g;
+      arm(bars, s_arm, kBarGu + g, 2 * cbytes_s);
+      bulk_g2s_evict_first(gu_buf + kGuRows * g * p.rbs, Ln.wsg + row0 * p.rbs, cbytes_s, &bars[kBarGu + g],
+                           pol);
+      bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rbs, Ln.wsu + row0 * p.rbs, cbytes_s,
+                           &bars[kBarGu + g], pol);
     }
     STK_TRACE(12);
     if (++l == p.n_layers) {
@@ -900,14 +937,27 @@ static StackGeom stack_geom(const si_moe_layer &L, int n_layers, int sms) {
   return g;
 }
 
+// Row bytes of a shared-expert matrix row of `width` weights.
+static int shared_row_bytes(const si_moe_layer &L, int width) {
+  return L.shared_type == SI_Q8_0 ? width / 32 * kQ80Bytes : width / 256 * kQ4KBytes;
+}
+
+// Pieces of one routed / shared down row (the down step's work items).
+static int down_pieces_routed(const si_moe_layer &L) { return 2 * L.inter / 256; }
+static int down_pieces_shared(const si_moe_layer &L) {
+  return L.shared_type == SI_Q8_0 ? L.shared_inter / 256 : 2 * L.shared_inter / 256;
+}
+
 static StackSmem stack_smem(const si_moe_layer &L, int J, int n_layers) {
   StackSmem s{};
   const bool sh = L.shared_inter > 0;
+  const bool q80 = sh && L.shared_type == SI_Q8_0;
   const int H = L.hidden, k = L.top_k, nsb = H / 256;
   const int nq = k * L.inter + L.shared_inter, n_slots = k + (sh ? 1 : 0);
-  const int P_max = 2 * (L.inter > L.shared_inter ? L.inter : L.shared_inter) / 256;
+  const int P_r = down_pieces_routed(L), P_s = sh ? down_pieces_shared(L) : 0;
+  const int P_max = P_r > P_s ? P_r : P_s;
   const int rb = H / 256 * kQ4KBytes, rbd = L.inter / 256 * kQ4KBytes,
-            rbsd = sh ? L.shared_inter / 256 * kQ4KBytes : 0;
+            rbsd = sh ? shared_row_bytes(L, L.shared_inter) : 0;
   size_t off = kStkFixedBytes;
   auto take = [&](uint32_t &field, size_t bytes, size_t align) {
     off = round_up(off, align);
@@ -927,16 +977,25 @@ static StackSmem stack_smem(const si_moe_layer &L, int J, int n_layers) {
   take(s.ht_s, 4u * (nq / 32), 16);
   s.pbuf_stride = static_cast<uint32_t>(round_up(8u * H, 128));
   take(s.pbuf, 2u * s.pbuf_stride, 128);
-  take(s.gu, 64u * rb, 128);
-  take(s.dn, static_cast<size_t>(J) * k * rbd, 128);
+  if (q80) {
+    // one region: a routed unit followed by the routed down rows, or the
+    // shared unit (the routed down rows of its block overlap it)
+    const size_t routed = 64u * rb + static_cast<size_t>(J) * k * rbd;
+    const size_t shared = 64u * static_cast<size_t>(shared_row_bytes(L, H));
+    take(s.gu, routed > shared ? routed : shared, 128);
+    s.dn = s.gu + 64u * rb;
+  } else {
+    take(s.gu, 64u * rb, 128);
+    take(s.dn, static_cast<size_t>(J) * k * rbd, 128);
+  }
   take(s.sd, static_cast<size_t>(J) * rbsd, 128);
   s.bytes = static_cast<uint32_t>(off);
   return s;
 }
 
 // Whether the persistent kernel serves these layers: same shapes, Q4_K
-// routed experts, Q4_K or no shared expert, bf16 router, and one resident
-// block per SM covers every gate/up unit, down row and router row.
+// routed experts, a Q4_K, Q8_0 or no shared expert, bf16 router, and one
+// resident block per SM covers every gate/up unit, down row and router row.
 bool stack_supported(const si_moe_layer *layers, int n_layers) {
   const si_moe_layer &L = layers[0];
   for (int l = 0; l < n_layers; ++l) {
@@ -944,8 +1003,9 @@ bool stack_supported(const si_moe_layer *layers, int n_layers) {
     if (M.hidden != L.hidden || M.n_experts != L.n_experts || M.top_k != L.top_k ||
         M.inter != L.inter || M.shared_inter != L.shared_inter || M.expert_type != SI_Q4_K ||
         down_type_of(M) != SI_Q4_K ||
-        M.router_type != SI_BF16 || (M.shared_inter > 0 && M.shared_type != SI_Q4_K) ||
-        M.eps != L.eps)
+        M.router_type != SI_BF16 ||
+        (M.shared_inter > 0 && M.shared_type != SI_Q4_K && M.shared_type != SI_Q8_0) ||
+        (M.shared_inter > 0 && M.shared_type != L.shared_type) || M.eps != L.eps)
       return false;
   }
   if (L.hidden % 2048 != 0 || L.hidden > 4096 || L.n_experts > 256 || (L.n_experts & 1) ||
@@ -955,14 +1015,14 @@ bool stack_supported(const si_moe_layer *layers, int n_layers) {
   if (sms <= 0) return false;
   const StackGeom g = stack_geom(L, n_layers, sms);
   const int n_slots = L.top_k + (L.shared_inter > 0 ? 1 : 0);
-  const int P_max = 2 * (L.inter > L.shared_inter ? L.inter : L.shared_inter) / 256;
+  const int P_r = down_pieces_routed(L), P_s = L.shared_inter > 0 ? down_pieces_shared(L) : 0;
+  const int P_max = P_r > P_s ? P_r : P_s;
   if (sms < g.units || g.units * 5 > 2 * kStkThreads || g.J > 32 || sms * g.np3 > 2 * kStkThreads ||
       n_slots * g.J * P_max > 2 * kStkThreads || n_slots * g.J > kStkThreads)
     return false;
   // the pieces of a (slot, row) of the down step are summed across lanes of
   // one warp: the piece counts must divide 32, and the shared slot's pieces
   // must start on a multiple of their count
-  const int P_r = 2 * L.inter / 256, P_s = 2 * L.shared_inter / 256;
   if (32 % P_r || (L.shared_inter > 0 && (32 % P_s || (L.top_k * g.J * P_r) % P_s))) return false;
   if ((L.n_experts > 128 ? 2 * sms : sms) < L.n_experts) return false;
   if (sms > kStkThreads) return false;
@@ -978,6 +1038,7 @@ cudaError_t preload_stack() {
   cudaFuncAttributes a;
   cudaError_t e = cudaFuncGetAttributes(&a, stack_kernel<0>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q8_0>);
   return e;
 }
 
@@ -1019,8 +1080,9 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   p.n_tokens = n_tokens;
   p.H = L.hidden; p.E = L.n_experts; p.k = L.top_k; p.I = L.inter; p.Is = L.shared_inter;
   p.rb = L.hidden / 256 * kQ4KBytes;
+  p.rbs = L.shared_inter > 0 ? shared_row_bytes(L, L.hidden) : p.rb;
   p.rbd = L.inter / 256 * kQ4KBytes;
-  p.rbsd = L.shared_inter / 256 * kQ4KBytes;
+  p.rbsd = L.shared_inter > 0 ? shared_row_bytes(L, L.shared_inter) : 0;
   p.J = g.J;
   p.np3 = g.np3;
   p.eps = L.eps;
@@ -1036,7 +1098,8 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   p.ol = reinterpret_cast<uint64_t *>(base + g.off_ol);
   const size_t smem = p.sm.bytes;
   if (smem > 227 * 1024) return SI_ERR_UNSUPPORTED;
-  auto kern = L.shared_inter > 0 ? stack_kernel<SI_Q4_K> : stack_kernel<0>;
+  auto kern = L.shared_inter == 0 ? stack_kernel<0>
+              : L.shared_type == SI_Q8_0 ? stack_kernel<SI_Q8_0> : stack_kernel<SI_Q4_K>;
   cudaError_t e = allow_smem(kern, smem);
   if (e != cudaSuccess) return SI_ERR_CUDA;
   int per_sm = 0;

@@ -95,13 +95,14 @@ def test_stack_graph_against_oracle_per_layer():
 
 @pytest.mark.parametrize("name", ["q4k_shared_q8_0", "q4k_shared_q4k"])
 def test_stack_graph_equals_eager_layers_and_replays_bit_exact(name):
-    """The Q4_K-shared stack runs as one persistent kernel, the Q8_0-shared one
-    as four kernels per layer: both must reproduce the per-layer calls bit for
-    bit, and every replay of the graph must give the same bits."""
+    """The Q4_K-shared and the Q8_0-shared stack both run as one persistent
+    kernel: each must reproduce the per-layer calls bit for bit, and every
+    replay of the graph must give the same bits."""
     spec = SPECS[name]
     layers = _stack_layers(spec, 4, seed=300)
     x = gen.make_tokens(900, 3).cuda()
     g = m.StackGraph(layers, x)
+    assert g.persistent
     g.launch()
     torch.cuda.synchronize()
     y1, s1, i1 = g.y.clone(), g.sum.clone(), g.ids.clone()
@@ -119,11 +120,12 @@ def test_stack_graph_equals_eager_layers_and_replays_bit_exact(name):
     g.close()
 
 
-def test_stack_paths_agree_bit_exact_and_report_their_kind():
-    """The same Q4_K stack through the persistent kernel and through four
-    kernels per layer: identical bits; a stack the persistent kernel does not
-    serve is refused when that path is forced."""
-    spec = gen.Q4K_LAYER_SHARED_Q4_K
+@pytest.mark.parametrize("name", ["q4k_shared_q4k", "q4k_shared_q8_0"])
+def test_stack_paths_agree_bit_exact_and_report_their_kind(name):
+    """The same stack through the persistent kernel and through four kernels
+    per layer: identical bits; a stack the persistent kernel does not serve
+    (bf16 experts) is refused when that path is forced."""
+    spec = SPECS[name]
     layers = _stack_layers(spec, 3, seed=310)
     x = gen.make_tokens(910, 2).cuda()
     gp = m.StackGraph(layers, x, mode=m.SI_STACK_PERSISTENT)
@@ -137,11 +139,11 @@ def test_stack_paths_agree_bit_exact_and_report_their_kind():
     for g in (gp, gl, ga):
         assert m.si_workspace_status(g.ws) == m.SI_OK
         g.close()
-    q8 = _stack_layers(gen.Q4K_LAYER_SHARED_Q8_0, 2, seed=311)
+    bf = _stack_layers(gen.BF16_LAYER, 2, seed=311)
     with pytest.raises(m.SiError) as e:
-        m.StackGraph(q8, x, mode=m.SI_STACK_PERSISTENT)
+        m.StackGraph(bf, x, mode=m.SI_STACK_PERSISTENT)
     assert e.value.status == m.SI_ERR_UNSUPPORTED
-    assert not m.StackGraph(q8, x).persistent
+    assert not m.StackGraph(bf, x).persistent
 
 
 PERSISTENT_SHAPES = {
@@ -149,6 +151,8 @@ PERSISTENT_SHAPES = {
     "e256_no_shared": gen.LayerSpec(shared_inter=0, shared_type="q4_k"),
     "e64_top4_shared_q4k": gen.LayerSpec(n_experts=64, top_k=4, shared_type="q4_k"),
     "i256_shared_q4k": gen.LayerSpec(inter=256, shared_type="q4_k"),
+    "e128_shared_q8_0": gen.LayerSpec(n_experts=128, shared_type="q8_0"),
+    "i256_shared_q8_0_is1024": gen.LayerSpec(inter=256, shared_inter=1024, shared_type="q8_0"),
 }
 
 

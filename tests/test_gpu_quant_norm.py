@@ -30,7 +30,9 @@ def _activation_vector(n, seed):
     return x
 
 
-@pytest.mark.parametrize("n", [32, 256, 2048, 32 * 1001, 1 << 20])
+# 32 * 393217: more groups of 8 values than one pass of the grid-stride
+# quantiser covers on a 152-SM part, ending in a partial warp
+@pytest.mark.parametrize("n", [32, 256, 2048, 32 * 1001, 1 << 20, 32 * 393217])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_quantize_q8_1_bit_exact(n, dtype):
     x = _activation_vector(n, 5).to(dtype)

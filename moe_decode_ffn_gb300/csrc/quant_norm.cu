@@ -7,56 +7,65 @@
 // (sparkinfer PR #273), Summary item 2: routed + shared + residual folded into
 // one add+RMSNorm, bit-identical to the residual add followed by the 2-input
 // norm.
-#include <algorithm>
-
 #include "common.cuh"
 #include "host.hpp"
 
 namespace si {
 
-// One thread per 8 values; 4 consecutive lanes form one 32-value block. A
-// grid-stride loop over warps' 256-value spans, kQuantUnroll spans per pass
-// with all their 16-byte loads issued before the first encode: one load per
-// thread in flight left HBM idle between a block's load and its store.
+// A block quantises a chunk of 256 Q8_1 blocks (8192 values): its loads are
+// 16-byte, coalesced, four per thread issued before the first encode; the
+// encoder takes 4 consecutive lanes per 32-value block (lane 4j + i holds
+// values 8i .. 8i + 7 of one block); the 36-byte blocks are assembled in
+// shared memory and leave as consecutive 16-byte stores (4-byte stores when
+// y is not 16-byte aligned or for the last, partial chunk).
+constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;
+constexpr int kQuantChunkBlocks = kQuantThreads * kQuantUnroll / 4;   // 256 Q8_1 blocks
 template <typename T>
-__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const T *__restrict__ x, int64_t n,
-                                                            uint8_t *__restrict__ y) {
+__global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *__restrict__ x, int64_t n,
+                                                                     uint8_t *__restrict__ y, int y_vec16) {
+  __shared__ __align__(16) uint32_t s_out[kQuantChunkBlocks * kQ81Bytes / 4];
   grid_dep_wait();
   grid_dep_launch();
   const int64_t groups = n / 8;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int lane = threadIdx.x & 31;
-  // the loop bound is the warp's first group, so whole warps run every pass
-  // (the encoder shuffles across 4 lanes)
-  for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); w0 < groups;
-       w0 += kQuantUnroll * stride) {
-    float v[kQuantUnroll][8];
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kQuantThreads * kQuantUnroll;
+  float v[kQuantUnroll][8];
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t g = w0 + u * stride + lane;
-      if (g < groups) {
-        Load8<T>::run(x + 8 * g, v[u]);
-      } else {
+  for (int u = 0; u < kQuantUnroll; ++u) {
+    const int64_t g = g0 + u * kQuantThreads + threadIdx.x;
+    if (g < groups) {
+      Load8<T>::run(x + 8 * g, v[u]);
+    } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
-      }
+      for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
     }
+  }
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t g = w0 + u * stride + lane;
-      uint32_t lo, hi;
-      uint16_t d16, s16;
-      q8_1_encode_4lanes(v[u], lo, hi, d16, s16);
-      if (g < groups) {
-        uint8_t *blk = y + (g >> 2) * kQ81Bytes;
-        const int part = static_cast<int>(g & 3);
-        uint32_t *q = reinterpret_cast<uint32_t *>(blk + 4 + 8 * part);  // 4-byte aligned
-        q[0] = lo;
-        q[1] = hi;
-        if (part == 0) *reinterpret_cast<uint32_t *>(blk) = d16 | (static_cast<uint32_t>(s16) << 16);
-      }
-    }
+  for (int u = 0; u < kQuantUnroll; ++u) {
+    uint32_t lo, hi;
+    uint16_t d16, s16;
+    q8_1_encode_4lanes(v[u], lo, hi, d16, s16);
+    const int gl = u * kQuantThreads + threadIdx.x;   // group within the chunk
+    uint32_t *blk = s_out + (gl >> 2) * (kQ81Bytes / 4);
+    const int part = gl & 3;
+    blk[1 + 2 * part] = lo;
+    blk[2 + 2 * part] = hi;
+    if (part == 0) blk[0] = d16 | (static_cast<uint32_t>(s16) << 16);
+  }
+  __syncthreads();
+  const int64_t nblk_all = n / 32;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kQuantChunkBlocks;
+  const int nblk = nblk_all - b0 < kQuantChunkBlocks ? static_cast<int>(nblk_all - b0) : kQuantChunkBlocks;
+  uint8_t *dst = y + b0 * kQ81Bytes;
+  if (y_vec16 && nblk == kQuantChunkBlocks) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(s_out);
+#pragma unroll 1
+    for (int i = threadIdx.x; i < kQuantChunkBlocks * kQ81Bytes / 16; i += kQuantThreads)
+      reinterpret_cast<uint4 *>(dst)[i] = src[i];
+  } else {
+#pragma unroll 1
+    for (int i = threadIdx.x; i < nblk * (kQ81Bytes / 4); i += kQuantThreads)
+      reinterpret_cast<uint32_t *>(dst)[i] = s_out[i];
   }
 }
 
@@ -193,19 +202,18 @@ extern "C" si_status si_quantize_q8_1(const void *x, si_dtype x_type, int64_t n,
   if (!x || !y_q8_1 || n <= 0 || n % 32 != 0) return SI_ERR_INVALID_ARG;
   if (x_type != SI_F32 && x_type != SI_BF16) return SI_ERR_UNSUPPORTED;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y_q8_1) & 3u)) return SI_ERR_INVALID_ARG;
-  const int64_t groups = n / 8;
-  // at most 8 resident blocks of 256 threads per SM; each thread then takes
-  // kQuantUnroll groups per pass
-  const int64_t need = (groups + 256 * kQuantUnroll - 1) / (256 * kQuantUnroll);
-  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(need, 8 * static_cast<int64_t>(sm_count()))));
+  const int64_t chunks = (n / 32 + kQuantChunkBlocks - 1) / kQuantChunkBlocks;
+  if (chunks > 0x7FFFFFFF) return SI_ERR_INVALID_ARG;
+  const dim3 grid(static_cast<unsigned>(chunks));
+  const int vec16 = (reinterpret_cast<uintptr_t>(y_q8_1) & 15u) == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (x_type == SI_F32)
-    e = launch_pdl(quantize_q8_1_kernel<float>, grid, dim3(256), 0, s,
-                   static_cast<const float *>(x), n, static_cast<uint8_t *>(y_q8_1));
+    e = launch_pdl(quantize_q8_1_kernel<float>, grid, dim3(kQuantThreads), 0, s,
+                   static_cast<const float *>(x), n, static_cast<uint8_t *>(y_q8_1), vec16);
   else
-    e = launch_pdl(quantize_q8_1_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
-                   static_cast<const __nv_bfloat16 *>(x), n, static_cast<uint8_t *>(y_q8_1));
+    e = launch_pdl(quantize_q8_1_kernel<__nv_bfloat16>, grid, dim3(kQuantThreads), 0, s,
+                   static_cast<const __nv_bfloat16 *>(x), n, static_cast<uint8_t *>(y_q8_1), vec16);
   return cuda_status(e);
 }
 

@@ -41,6 +41,21 @@ def test_quantize_q8_1_bit_exact(n, dtype):
     assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
 
 
+@pytest.mark.parametrize("offset", [4, 8, 12])
+def test_quantize_q8_1_output_only_4_byte_aligned(offset):
+    """An output that starts 4 bytes past a 16-byte boundary (the minimum
+    alignment the call accepts): the same bytes, none written outside it."""
+    n = 32 * 8192 + 32 * 37          # 32 full chunks of 256 blocks, then a partial one
+    x = _activation_vector(n, 6).to(torch.bfloat16)
+    buf = torch.full((n // 32 * 36 + 32,), 0xA5, dtype=torch.uint8, device="cuda")
+    out = buf[offset:offset + n // 32 * 36]
+    m.si_quantize_q8_1(x.cuda(), out=out)
+    got = buf.cpu().numpy()
+    ref = F.q8_1_to_bytes(F.q8_1_quantize(x.float().numpy())).reshape(-1)
+    assert np.array_equal(got[offset:offset + ref.size], ref)
+    assert (got[:offset] == 0xA5).all() and (got[offset + ref.size:] == 0xA5).all()
+
+
 def _near_half_quotients(n_blocks, seed):
     """Blocks whose quotients x / d sit on, or within a few 1e-5 of, the
     half-integer rounding boundaries (and others well inside), for scales d

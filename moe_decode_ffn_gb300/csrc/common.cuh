@@ -600,4 +600,63 @@ SI_DEV float q80_sb_dot(const uint4 *w, const uint4 *a, const float *da) {
   return acc;
 }
 
+// Global -> L2 bulk prefetch (no destination, no completion; address and
+// bytes multiples of 16). A later read of the range hits L2.
+SI_DEV void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// bf16 weight rows against fp32 activations (the bf16 gate/up and down dot
+// products; every path that computes them uses these, in this order).
+// ---------------------------------------------------------------------------
+// Lane `lane` of every warp owns columns c0 + 256 c + 8 lane .. + 7 (c < 8)
+// of each 2048-wide chunk of a row; x sits in shared memory as packed bf16
+// (exact), so a lane's 16-byte reads of it are consecutive across the warp
+// (no bank conflicts).
+SI_DEV void load_row8(const __nv_bfloat16 *row, int c0, int H, int lane, uint4 w[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int k0 = c0 + (c * 32 + lane) * 8;
+    if (k0 < H) w[c] = __ldcs(reinterpret_cast<const uint4 *>(row + k0));
+  }
+}
+
+SI_DEV void dot_row8(const uint4 w[8], const uint4 *xs, int c0, int H, int lane, float &acc) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int k0 = c0 + (c * 32 + lane) * 8;
+    if (k0 < H) {
+      float wv[8], xv[8];
+      Load8<__nv_bfloat16>::run(&w[c], wv);
+      Load8<__nv_bfloat16>::run(&xs[k0 / 8], xv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], xv[i], acc);
+    }
+  }
+}
+
+// A 512-wide chunk of a down row: lane l8 of the task's 8 lanes holds
+// columns cc + 8 l8 + 64 it .. + 7 (it < 8).
+SI_DEV void load_down8(const __nv_bfloat16 *row, int cc, int width, int l8, uint4 u[8]) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int c = cc + l8 * 8 + 64 * it;
+    if (row && c < width) u[it] = __ldcs(reinterpret_cast<const uint4 *>(row + c));
+  }
+}
+
+SI_DEV void dot_down8(const uint4 u[8], const float *hv, int cc, int width, int l8, float &acc) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int c = cc + l8 * 8 + 64 * it;
+    if (c < width) {
+      float wv[8];
+      Load8<__nv_bfloat16>::run(&u[it], wv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], hv[c + i], acc);
+    }
+  }
+}
+
 }  // namespace si

@@ -212,7 +212,37 @@ SI_DEV float sigma_dot(const __nv_bfloat16 *w, const float *y, int n, float *red
   return tot;
 }
 
+// The same sum with y as packed bf16 (identical values and order).
+SI_DEV float sigma_dot_bf(const __nv_bfloat16 *w, const uint4 *y_bf, int n, float *red) {
+  float acc = 0.f;
+#pragma unroll 1
+  for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+    float wv[8], yv[8];
+    Load8<__nv_bfloat16>::run(w + i0, wv);
+    Load8<__nv_bfloat16>::run(y_bf + i0 / 8, yv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], yv[i], acc);
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll 1
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) tot += red[i];
+  __syncthreads();
+  return tot;
+}
+
 // ---- copies ---------------------------------------------------------------------
+// bf16 gate/up units: 8 groups of 4 gate + 4 up rows through a ring of
+// kBfRing slots of 8 rows.
+constexpr int kBfGroups = 8;
+constexpr int kBfRing = 4;
+// after this many groups the block requests its routed down rows into L2
+// (earlier they would take DRAM time from the gate/up rows it waits for)
+constexpr int kBfDownAt = 3;
+static_assert(kBfRing <= kGuGroups, "the ring's slots use the gate/up barriers");
 // Issuing one bulk copy occupies the issuing thread for a few hundred cycles
 // whatever its size, and many small copies ramp up more slowly than a few
 // large ones, so copies are few and large and issued one per warp (lane 0)
@@ -225,6 +255,35 @@ SI_DEV void arm(uint64_t *bars, uint32_t *s_arm, int b, uint32_t bytes) {
   mbar_arrive_expect_tx(&bars[b], bytes);
   atomicXor(s_arm, 1u << b);
   atomicOr(s_arm, 1u << (16 + b));
+}
+
+// bf16 ring: group g (rows 4g .. 4g + 3 of the unit's gate and of its up
+// matrix) into slot g % kBfRing, armed and requested by the calling thread.
+SI_DEV void issue_bf16_group(const StackParams &p, const StackLayerPtrs &Lp, const uint64_t *s_sel, int unit,
+                             int units_r, bool shared_unit, int g, uint8_t *ring, uint64_t *bars,
+                             uint32_t *s_arm, uint64_t pol) {
+  const int sl = g % kBfRing;
+  const uint8_t *gsrc, *usrc;
+  size_t row0;
+  if (shared_unit) {
+    row0 = static_cast<size_t>(unit - units_r) * 32;
+    gsrc = Lp.wsg;
+    usrc = Lp.wsu;
+  } else {
+    const int nhb = p.I / 32, slot = unit / nhb, hb = unit - slot * nhb;
+    int e = key_index(s_sel[slot]);
+    if (e < 0 || e >= p.E) e = 0;
+    row0 = static_cast<size_t>(e) * p.I + static_cast<size_t>(hb) * 32;
+    gsrc = Lp.wg;
+    usrc = Lp.wu;
+  }
+  row0 += 4 * g;
+  const uint32_t bytes = 4u * p.rb;
+  arm(bars, s_arm, kBarGu + sl, 2 * bytes);
+  bulk_g2s_evict_first(ring + static_cast<size_t>(sl) * 8 * p.rb, gsrc + row0 * p.rb, bytes, &bars[kBarGu + sl],
+                       pol);
+  bulk_g2s_evict_first(ring + (static_cast<size_t>(sl) * 8 + 4) * p.rb, usrc + row0 * p.rb, bytes,
+                       &bars[kBarGu + sl], pol);
 }
 
 // Gather X3 (t = bf16(routed + shared) per row) into `tbuf` and fold it into
@@ -313,10 +372,18 @@ static __device__ int g_stk_trace_phase;
   } while (0)
 #endif
 
-template <int SFMT>
+template <int EFMT, int SFMT>
 __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr bool kShared = SFMT != 0;
+  // bf16 experts (and shared expert): the gate/up rows stream from global
+  // memory into registers, two rows per warp in flight (a unit of 64 rows of
+  // H bf16 is larger than shared memory); h travels as fp32 (two slots per
+  // unit); the down rows of every selected expert are requested at the
+  // selection.
+  constexpr bool kBf = EFMT == SI_BF16;
+  constexpr int kSu = kBf ? 2 : 1;           // X2 slots per gate/up unit
+  constexpr int kGq = kBf ? 5 : 2;           // X2 pairs gathered per thread
   // A Q8_0 shared expert: its gate/up unit (64 rows of H / 32 blocks of 34
   // bytes) is about twice a Q4_K unit, so in the block that owns it the
   // unit's buffer also holds the routed down rows, which arrive only after
@@ -350,6 +417,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   uint64_t *s_sel = reinterpret_cast<uint64_t *>(smem + 384);
   uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + 448);   // [64]
   float *h_s = reinterpret_cast<float *>(smem + 960);      // [32]
+  float *s_gu = reinterpret_cast<float *>(smem + 1088);    // [2][8] bf16 gate/up row dots
   StackLayerPtrs *s_layers = reinterpret_cast<StackLayerPtrs *>(smem + p.sm.layers);
   float *resid = reinterpret_cast<float *>(smem + p.sm.resid);
   float *y = reinterpret_cast<float *>(smem + p.sm.y);
@@ -363,6 +431,9 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   const uint32_t pstr = p.sm.pbuf_stride;
   uint8_t *gu_buf = smem + p.sm.gu;   // gate [32] + up [32] rows
   uint8_t *sd_buf = smem + p.sm.sd;   // [J] shared down rows
+  // bf16 layers: y as packed bf16 and h as fp32 in place of the Q8_1 tiles
+  uint4 *y_bf = reinterpret_cast<uint4 *>(smem + p.sm.xt_qs);   // [H / 8]
+  float *hf = reinterpret_cast<float *>(smem + p.sm.ht_qs);      // [k I + Is]
 
   // ---- static assignment ----------------------------------------------------
   const int my_unit = c < units ? c : -1;
@@ -381,16 +452,25 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   // X2 gather: pair q (5 per unit slot: 4 code pairs, 1 scale pair) ->
   // element offset g_q and shared memory destination g_dst (byte offset of 8
   // codes, or -(unit + 1) for the scales)
-  int g_q[2], g_dst[2];
+  // (bf16: pair q = unit q / 16, values 2 (q % 16), + 1 of its h, g_dst the
+  // index of the first in hf)
+  int g_q[kGq], g_dst[kGq];
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
+  for (int s = 0; s < kGq; ++s) {
     const int q = static_cast<int>(threadIdx.x) + s * kStkThreads;
-    const int u = q / 5, sub = q - 5 * (q / 5);
-    g_q[s] = q < units * 5 ? u * kSlot + 2 * sub : -1;   // element offset of the pair
-    const int base_sb = u < units_r ? (u / (I / 32)) * nsb_r : k * nsb_r;
-    const int hb = u < units_r ? u % (I / 32) : u - units_r;
-    g_dst[s] = sub < 4 ? static_cast<int>(p.sm.ht_qs) + (base_sb + hb / 8) * kActSbStride + (hb % 8) * 32 + 8 * sub
-                       : -(u + 1);
+    if constexpr (kBf) {
+      const int u = q / 16, m = q % 16;
+      g_q[s] = q < units * 16 ? u * 2 * kSlot + 2 * m : -1;
+      g_dst[s] = 32 * u + 2 * m;
+    } else {
+      const int u = q / 5, sub = q - 5 * (q / 5);
+      g_q[s] = q < units * 5 ? u * kSlot + 2 * sub : -1;   // element offset of the pair
+      const int base_sb = u < units_r ? (u / (I / 32)) * nsb_r : k * nsb_r;
+      const int hb = u < units_r ? u % (I / 32) : u - units_r;
+      g_dst[s] = sub < 4 ? static_cast<int>(p.sm.ht_qs) + (base_sb + hb / 8) * kActSbStride + (hb % 8) * 32 +
+                               8 * sub
+                         : -(u + 1);
+    }
   }
   // down: item (slot r, row jl, half-super-block qq) of this thread in pass s;
   // the P pieces of a (slot, row) lie in consecutive lanes of one warp, the
@@ -399,7 +479,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   bool d_live[2], d_first[2], d_q80[2];
   const int items_r = k * J * P_r;
   const int items = items_r + (kShared ? J * P_s : 0);
-  {
+  if constexpr (!kBf) {
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int u = static_cast<int>(threadIdx.x) + s * kStkThreads;
@@ -467,7 +547,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     if (nrr > 1) bulk_g2s(pbuf + 2 * H, L0.w_router + static_cast<size_t>(row_b) * H, H * 2, &bars[kBarPre]);
     if (kShared) bulk_g2s(pbuf + 4 * H, L0.w_sg, H * 2, &bars[kBarPre]);
     bulk_g2s(pbuf + 6 * H, L0.w_norm, H * 2, &bars[kBarPre]);
-    if (shared_unit) {
+    if (!kBf && shared_unit) {
       const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32;
 #pragma unroll 1
       for (int g = 0; g < kGuGroups; ++g) {
@@ -481,6 +561,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   }
 
   float r_norm = 0.f;   // rsqrt(mean(s^2) + eps) of the latest fold
+  uint32_t bf_ph = 0u;  // bf16 ring: bit s = parity of slot s's next phase
   for (int it = 0;; ++it) {
     const uint32_t tag = base + static_cast<uint32_t>(it) + 1u, par = it & 1u;
     STK_TRACE_START();
@@ -542,8 +623,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) yv[e] = bf16_round(__fmul_rn(__fmul_rn(sv[e], r_norm), wv[e]));
           }
-          *reinterpret_cast<float4 *>(y + 8 * v) = make_float4(yv[0], yv[1], yv[2], yv[3]);
-          *reinterpret_cast<float4 *>(y + 8 * v + 4) = make_float4(yv[4], yv[5], yv[6], yv[7]);
+          if constexpr (!kBf) {
+            *reinterpret_cast<float4 *>(y + 8 * v) = make_float4(yv[0], yv[1], yv[2], yv[3]);
+            *reinterpret_cast<float4 *>(y + 8 * v + 4) = make_float4(yv[4], yv[5], yv[6], yv[7]);
+          } else
+            y_bf[v] = make_uint4(bf16_bits(yv[0]) | (static_cast<uint32_t>(bf16_bits(yv[1])) << 16),
+                                 bf16_bits(yv[2]) | (static_cast<uint32_t>(bf16_bits(yv[3])) << 16),
+                                 bf16_bits(yv[4]) | (static_cast<uint32_t>(bf16_bits(yv[5])) << 16),
+                                 bf16_bits(yv[6]) | (static_cast<uint32_t>(bf16_bits(yv[7])) << 16));
           if (ok && nrr > 0) {
             float wa[8];
             Load8<__nv_bfloat16>::run(pb + 16 * v, wa);
@@ -585,7 +672,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     }
     STK_TRACE(2);
     // the gate/up activations, while the logits travel
-    quantize_y(y, H, xt);   // ends with __syncthreads
+    if constexpr (!kBf) quantize_y(y, H, xt);   // ends with __syncthreads
     STK_TRACE(3);
 
     // [S] warps 0..7 gather the logits of experts 32w .. 32w + 31 (expert e
@@ -610,7 +697,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         if (lane < 8) s_cand[warp * 8 + lane] = key;
       } else if (lane == 0) {
         if (threadIdx.x == kArmT) {
-          if (my_unit >= 0 && !shared_unit)
+          if (!kBf && my_unit >= 0 && !shared_unit)
 #pragma unroll 1
             for (int g = 0; g < kGuGroups; ++g) arm(bars, s_arm, kBarGu + g, 2 * cbytes);
           if (nrows > 0) arm(bars, s_arm, kBarDn, static_cast<uint32_t>(k * nrows * p.rbd));
@@ -653,7 +740,9 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     // with a unit requests them once its gate/up rows have landed)
     if (lane == 0) {
       const StackLayerPtrs &Lp = s_layers[l];
-      if (warp < 2 * kGuGroups && my_unit >= 0 && !shared_unit) {
+      if (kBf && warp < kBfRing && my_unit >= 0)
+        issue_bf16_group(p, Lp, s_sel, my_unit, units_r, shared_unit, warp, gu_buf, bars, s_arm, pol);
+      if (!kBf && warp < 2 * kGuGroups && my_unit >= 0 && !shared_unit) {
         const int slot = my_unit / (I / 32), hb = my_unit - slot * (I / 32);
         int e = key_index(s_sel[slot]);
         if (e < 0 || e >= E) e = 0;
@@ -663,12 +752,13 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         bulk_g2s_evict_first(gu_buf + ((up ? 32 : 0) + kGuRows * g) * p.rb, (up ? Lp.wu : Lp.wg) + row0 * p.rb,
                              cbytes, &bars[kBarGu + g], pol);
       }
-      if (warp >= 8 && warp < 8 + k && nrows > 0 && my_unit < 0) {
+      if (warp >= 8 && warp < 8 + k && nrows > 0 && (kBf || my_unit < 0)) {
         int e = key_index(s_sel[warp - 8]);
         if (e < 0 || e >= E) e = 0;
-        bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
-                             Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
-                             static_cast<uint32_t>(nrows) * p.rbd, &bars[kBarDn], pol);
+        const uint8_t *src = Lp.wd + (static_cast<size_t>(e) * H + j0) * p.rbd;
+        if (my_unit < 0)   // (a bf16 unit block's ring holds its gate/up rows until [G] ends)
+          bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd, src,
+                               static_cast<uint32_t>(nrows) * p.rbd, &bars[kBarDn], pol);
       }
     }
     // while the routed bytes travel: softmax over the selected logits (rank
@@ -690,7 +780,77 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     STK_TRACE(6);
 
     // [G] gate/up of this block's unit -> h line
-    if (my_unit >= 0) {
+    if constexpr (kBf) {
+      if (my_unit >= 0) {
+        // the unit's 8 groups of 4 gate + 4 up rows pass through the ring:
+        // warp w < 8 dots row w of the group in the four-kernel path's lane
+        // order and reduction; after a group's barrier its slot is refilled
+        // with the group 3 ahead and threads 0..3 form its 4 values of h
+        bool ok = true;
+#pragma unroll 1
+        for (int g = 0; g < kBfGroups; ++g) {
+          const int sl = g % kBfRing;
+          ok = mbar_wait_bounded(&bars[kBarGu + sl], (bf_ph >> sl) & 1u, p.status);
+          bf_ph ^= 1u << sl;
+          if (ok && warp < 8) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(gu_buf + (sl * 8 + warp) * p.rb);
+            float acc = 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < H; c0 += 2048) {
+              uint4 w[8];
+#pragma unroll
+              for (int cc = 0; cc < 8; ++cc) {
+                const int k0 = c0 + (cc * 32 + lane) * 8;
+                if (k0 < H) w[cc] = row[k0 / 8];
+              }
+              dot_row8(w, y_bf, c0, H, lane, acc);
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+            if (lane == 0) s_gu[8 * (g & 1) + warp] = acc;
+          }
+          if (__syncthreads_or(!ok)) goto fail;
+          if (threadIdx.x < 4) {
+            const float ag = s_gu[8 * (g & 1) + threadIdx.x], au = s_gu[8 * (g & 1) + 4 + threadIdx.x];
+            h_s[4 * g + threadIdx.x] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
+          }
+          if (threadIdx.x == 256 && g + kBfRing < kBfGroups)
+            issue_bf16_group(p, s_layers[l], s_sel, my_unit, units_r, shared_unit, g + kBfRing, gu_buf, bars,
+                             s_arm, pol);
+          if (g + 1 == kBfDownAt && lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {
+            int e = key_index(s_sel[warp - 8]);
+            if (e < 0 || e >= E) e = 0;
+            bulk_prefetch_l2(s_layers[l].wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
+                             static_cast<uint32_t>(nrows) * p.rbd);
+          }
+        }
+        // the routed down rows (in L2 since the selection) into the ring's
+        // space, which no copy of this iteration targets any more
+        if (lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {
+          int e = key_index(s_sel[warp - 8]);
+          if (e < 0 || e >= E) e = 0;
+          bulk_g2s_evict_first(dn_buf + static_cast<size_t>(warp - 8) * J * p.rbd,
+                               s_layers[l].wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
+                               static_cast<uint32_t>(nrows) * p.rbd, &bars[kBarDn], pol);
+        }
+        __syncwarp();
+        STK_TRACE(7);
+        if (warp == 0) {
+          // item i = 16 r + m of copy r: values 2m, 2m + 1; lane L writes
+          // items L, L + 32, ...
+          const uint32_t hv = __float_as_uint(h_s[lane]);
+#pragma unroll
+          for (int i0 = 0; i0 < 16 * kXRep; i0 += 32) {
+            const int i = i0 + lane, r = i / 16, m = i - 16 * r;
+            const uint32_t wa2 = __shfl_sync(0xffffffffu, hv, (2 * m) & 31);
+            const uint32_t wb2 = __shfl_sync(0xffffffffu, hv, (2 * m + 1) & 31);
+            if (i < 16 * kXRep)
+              st_tag2(p.hl + ((static_cast<size_t>(par) * kXRep + r) * units + my_unit) * kSu * kSlot + 2 * m,
+                      tagged(tag, wa2), tagged(tag, wb2));
+          }
+        }
+      }
+    } else if (my_unit >= 0) {
       float acc = 0.f;
       const bool ok = mbar_wait_bounded(&bars[kBarGu + pr / kGuRows], par, p.status);
       if (ok) {
@@ -765,7 +925,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     float sigma = 0.f;
     if (kShared && nrows > 0) {
       const __nv_bfloat16 *wsg = reinterpret_cast<const __nv_bfloat16 *>(pbuf + par * pstr + 4 * H);
-      sigma = __fdiv_rn(1.f, 1.f + expf(-sigma_dot(wsg, y, H, red)));
+      const float z = kBf ? sigma_dot_bf(wsg, y_bf, H, red) : sigma_dot(wsg, y, H, red);
+      sigma = __fdiv_rn(1.f, 1.f + expf(-z));
     }
 
     // [D] gather h, down for this block's rows -> X3 line. The first reads of
@@ -774,21 +935,26 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     // lines are polled.
     if (nrows > 0) {
       bool ok = true;
-      const uint64_t *hl = p.hl + (static_cast<size_t>(par) * kXRep + rep) * units * kSlot;
-      uint64_t v[2][2];
+      const uint64_t *hl = p.hl + (static_cast<size_t>(par) * kXRep + rep) * units * kSu * kSlot;
+      uint64_t v[kGq][2];
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < kGq; ++s)
         if (g_q[s] >= 0) ld_tag2(hl + g_q[s], v[s][0], v[s][1]);
       bool okw = mbar_wait_bounded(&bars[kBarDn], par, p.status);
       if (kShared) okw &= mbar_wait_bounded(&bars[kBarSd], par, p.status);
       Q4KHalf wq;
-      if (okw && d_live[0] && !d_q80[0])
-        q4k_half_load(reinterpret_cast<const uint4 *>(smem + d_row[0]), d_h[0], wq);
+      if constexpr (!kBf)
+        if (okw && d_live[0] && !d_q80[0])
+          q4k_half_load(reinterpret_cast<const uint4 *>(smem + d_row[0]), d_h[0], wq);
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < kGq; ++s) {
         if (g_q[s] < 0) continue;
         ok &= get_pair(hl + g_q[s], tag, v[s][0], v[s][1], p.status);
-        if (g_dst[s] >= 0) {
+        if constexpr (kBf) {
+          *reinterpret_cast<float2 *>(hf + g_dst[s]) =
+              make_float2(__uint_as_float(static_cast<uint32_t>(v[s][0])),
+                          __uint_as_float(static_cast<uint32_t>(v[s][1])));
+        } else if (g_dst[s] >= 0) {
           *reinterpret_cast<uint2 *>(smem + g_dst[s]) =
               make_uint2(static_cast<uint32_t>(v[s][0]), static_cast<uint32_t>(v[s][1]));
         } else {
@@ -800,6 +966,48 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       if (__syncthreads_or(!(ok && okw))) goto fail;
       STK_TRACE(9);
       STK_TRACE(10);
+      if constexpr (kBf) {
+        // tasks (slot, row) of 8 lanes each, the four-kernel path's order:
+        // lane l8 holds columns cc + 8 l8 + 64 i (i < 8) of each 512-wide
+        // chunk, then the 8 lanes are summed
+        const int sub = lane >> 3, l8 = lane & 7;
+        const int ntask = (k + (kShared ? 1 : 0)) * J;
+#pragma unroll 1
+        for (int t0 = 0; t0 < ntask; t0 += 4 * (kStkThreads / 32)) {
+          const int task = t0 + 4 * warp + sub;
+          const int r = task / J, jl = task - r * J;
+          const bool live = task < ntask && jl < nrows;
+          float acc = 0.f;
+          if (live) {
+            const bool sh = kShared && r == k;
+            const int width = sh ? Is : I;
+            const uint8_t *row = sh ? sd_buf + static_cast<size_t>(jl) * p.rbsd
+                                    : dn_buf + static_cast<size_t>(r * J + jl) * p.rbd;
+            const float *hv = hf + r * I;
+#pragma unroll 1
+            for (int cc = 0; cc < width; cc += 512) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int col = cc + l8 * 8 + 64 * i;
+                if (col < width) {
+                  // dot_down8's products and order; h read as two float4
+                  float wv[8];
+                  Load8<__nv_bfloat16>::run(row + 2 * col, wv);
+                  const float4 h0 = *reinterpret_cast<const float4 *>(hv + col);
+                  const float4 h1 = *reinterpret_cast<const float4 *>(hv + col + 4);
+                  const float hh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) acc = fmaf(wv[q], hh[q], acc);
+                }
+              }
+            }
+          }
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+          if (live && l8 == 0) part[r * J + jl] = acc;
+        }
+      } else {
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (s * kStkThreads < items) {   // block-uniform
@@ -823,6 +1031,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
           }
           if (d_live[s] && d_first[s]) part[d_dst[s]] = ysum;
         }
+      }
       }
       __syncthreads();
       STK_TRACE(11);
@@ -931,7 +1140,8 @@ static StackGeom stack_geom(const si_moe_layer &L, int n_layers, int sms) {
   take(g.off_epoch, 256);
   take(g.off_layers, sizeof(StackLayerPtrs) * n_layers);
   take(g.off_lg, 2 * 8u * kSlot * kXRep * sms);
-  take(g.off_hl, 2 * 8u * kSlot * kXRep * g.units);
+  const size_t su = L.expert_type == SI_BF16 ? 2 : 1;   // X2 slots per unit
+  take(g.off_hl, 2 * 8u * kSlot * kXRep * g.units * su);
   take(g.off_ol, 2 * 8u * kSlot * kXRep * sms);
   g.bytes = off;
   return g;
@@ -948,7 +1158,44 @@ static int down_pieces_shared(const si_moe_layer &L) {
   return L.shared_type == SI_Q8_0 ? L.shared_inter / 256 : 2 * L.shared_inter / 256;
 }
 
+// bf16 layers: no Q8_1 tiles; y as packed bf16 (in the place of the x
+// tile), h as fp32 (in the place of the h tile); the gate/up ring and the
+// routed down rows share one region.
+static StackSmem stack_smem_bf16(const si_moe_layer &L, int J, int n_layers) {
+  StackSmem s{};
+  const bool sh = L.shared_inter > 0;
+  const int H = L.hidden, k = L.top_k;
+  const int nq = k * L.inter + L.shared_inter, n_slots = k + (sh ? 1 : 0);
+  size_t off = kStkFixedBytes;
+  auto take = [&](uint32_t &field, size_t bytes, size_t align) {
+    off = round_up(off, align);
+    field = static_cast<uint32_t>(off);
+    off += bytes;
+  };
+  take(s.layers, sizeof(StackLayerPtrs) * n_layers, 16);
+  take(s.resid, 4u * H, 16);
+  take(s.tbuf, 4u * H, 16);
+  s.y = s.tbuf;   // unused: y lives as packed bf16 only
+  take(s.part, 4u * n_slots * J, 16);
+  take(s.xt_qs, 2u * H, 16);
+  s.xt_d = s.xt_s = s.xt_qs;
+  take(s.ht_qs, 4u * nq, 16);
+  s.ht_d = s.ht_s = s.ht_qs;
+  s.pbuf_stride = static_cast<uint32_t>(round_up(8u * H, 128));
+  take(s.pbuf, 2u * s.pbuf_stride, 128);
+  // the gate/up ring (kBfRing slots of 8 rows of H) and, once the ring is
+  // drained, the routed down rows: one region
+  const size_t ring = static_cast<size_t>(kBfRing) * 8 * H * 2;
+  const size_t down = static_cast<size_t>(J) * k * L.inter * 2;
+  take(s.gu, ring > down ? ring : down, 128);
+  s.dn = s.gu;
+  take(s.sd, static_cast<size_t>(J) * L.shared_inter * 2, 128);
+  s.bytes = static_cast<uint32_t>(off);
+  return s;
+}
+
 static StackSmem stack_smem(const si_moe_layer &L, int J, int n_layers) {
+  if (L.expert_type == SI_BF16) return stack_smem_bf16(L, J, n_layers);
   StackSmem s{};
   const bool sh = L.shared_inter > 0;
   const bool q80 = sh && L.shared_type == SI_Q8_0;
@@ -996,8 +1243,36 @@ static StackSmem stack_smem(const si_moe_layer &L, int J, int n_layers) {
 // Whether the persistent kernel serves these layers: same shapes, Q4_K
 // routed experts, a Q4_K, Q8_0 or no shared expert, bf16 router, and one
 // resident block per SM covers every gate/up unit, down row and router row.
+// bf16 layers: bf16 routed and shared experts and router, the same shapes,
+// H a multiple of 2048 (<= 4096), I and Is multiples of 32, and every task of
+// the down step (slot, row) and every h pair within the block's threads.
+static bool stack_supported_bf16(const si_moe_layer *layers, int n_layers) {
+  const si_moe_layer &L = layers[0];
+  for (int l = 0; l < n_layers; ++l) {
+    const si_moe_layer &M = layers[l];
+    if (M.hidden != L.hidden || M.n_experts != L.n_experts || M.top_k != L.top_k ||
+        M.inter != L.inter || M.shared_inter != L.shared_inter || M.expert_type != SI_BF16 ||
+        down_type_of(M) != SI_BF16 || M.router_type != SI_BF16 ||
+        (M.shared_inter > 0 && M.shared_type != SI_BF16) || M.eps != L.eps)
+      return false;
+  }
+  if (L.hidden % 2048 != 0 || L.hidden > 4096 || L.n_experts > 256 || (L.n_experts & 1) ||
+      L.inter % 32 || L.shared_inter % 32 || L.inter <= 0 || L.top_k > 8 || L.top_k < 1 || n_layers > 128)
+    return false;
+  const int sms = device_sms();
+  if (sms <= 0 || sms > kStkThreads) return false;
+  const StackGeom g = stack_geom(L, n_layers, sms);
+  const int n_slots = L.top_k + (L.shared_inter > 0 ? 1 : 0);
+  if (sms < g.units || g.units * 16 > 5 * kStkThreads || g.J > 32 || sms * g.np3 > 2 * kStkThreads ||
+      n_slots * g.J > kStkThreads)
+    return false;
+  if ((L.n_experts > 128 ? 2 * sms : sms) < L.n_experts) return false;
+  return stack_smem(L, g.J, n_layers).bytes <= 227 * 1024;
+}
+
 bool stack_supported(const si_moe_layer *layers, int n_layers) {
   const si_moe_layer &L = layers[0];
+  if (L.expert_type == SI_BF16) return stack_supported_bf16(layers, n_layers);
   for (int l = 0; l < n_layers; ++l) {
     const si_moe_layer &M = layers[l];
     if (M.hidden != L.hidden || M.n_experts != L.n_experts || M.top_k != L.top_k ||
@@ -1036,9 +1311,11 @@ size_t stack_workspace_bytes(const si_moe_layer *layers, int n_layers) {
 
 cudaError_t preload_stack() {
   cudaFuncAttributes a;
-  cudaError_t e = cudaFuncGetAttributes(&a, stack_kernel<0>);
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K>);
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q8_0>);
+  cudaError_t e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, 0>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, SI_Q4_K>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, SI_Q8_0>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_BF16, 0>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_BF16, SI_BF16>);
   return e;
 }
 
@@ -1079,10 +1356,11 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   p.n_layers = n_layers;
   p.n_tokens = n_tokens;
   p.H = L.hidden; p.E = L.n_experts; p.k = L.top_k; p.I = L.inter; p.Is = L.shared_inter;
-  p.rb = L.hidden / 256 * kQ4KBytes;
-  p.rbs = L.shared_inter > 0 ? shared_row_bytes(L, L.hidden) : p.rb;
-  p.rbd = L.inter / 256 * kQ4KBytes;
-  p.rbsd = L.shared_inter > 0 ? shared_row_bytes(L, L.shared_inter) : 0;
+  const bool bf = L.expert_type == SI_BF16;
+  p.rb = bf ? L.hidden * 2 : L.hidden / 256 * kQ4KBytes;
+  p.rbs = L.shared_inter > 0 && !bf ? shared_row_bytes(L, L.hidden) : p.rb;
+  p.rbd = bf ? L.inter * 2 : L.inter / 256 * kQ4KBytes;
+  p.rbsd = L.shared_inter > 0 ? (bf ? L.shared_inter * 2 : shared_row_bytes(L, L.shared_inter)) : 0;
   p.J = g.J;
   p.np3 = g.np3;
   p.eps = L.eps;
@@ -1098,8 +1376,10 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   p.ol = reinterpret_cast<uint64_t *>(base + g.off_ol);
   const size_t smem = p.sm.bytes;
   if (smem > 227 * 1024) return SI_ERR_UNSUPPORTED;
-  auto kern = L.shared_inter == 0 ? stack_kernel<0>
-              : L.shared_type == SI_Q8_0 ? stack_kernel<SI_Q8_0> : stack_kernel<SI_Q4_K>;
+  auto kern = bf ? (L.shared_inter == 0 ? stack_kernel<SI_BF16, 0> : stack_kernel<SI_BF16, SI_BF16>)
+              : L.shared_inter == 0      ? stack_kernel<SI_Q4_K, 0>
+              : L.shared_type == SI_Q8_0 ? stack_kernel<SI_Q4_K, SI_Q8_0>
+                                         : stack_kernel<SI_Q4_K, SI_Q4_K>;
   cudaError_t e = allow_smem(kern, smem);
   if (e != cudaSuccess) return SI_ERR_CUDA;
   int per_sm = 0;

@@ -93,11 +93,11 @@ def test_stack_graph_against_oracle_per_layer():
     g.close()
 
 
-@pytest.mark.parametrize("name", ["q4k_shared_q8_0", "q4k_shared_q4k"])
+@pytest.mark.parametrize("name", ["q4k_shared_q8_0", "q4k_shared_q4k", "bf16"])
 def test_stack_graph_equals_eager_layers_and_replays_bit_exact(name):
-    """The Q4_K-shared and the Q8_0-shared stack both run as one persistent
-    kernel: each must reproduce the per-layer calls bit for bit, and every
-    replay of the graph must give the same bits."""
+    """The Q4_K-shared, the Q8_0-shared and the bf16 stack each run as one
+    persistent kernel: each must reproduce the per-layer calls bit for bit,
+    and every replay of the graph must give the same bits."""
     spec = SPECS[name]
     layers = _stack_layers(spec, 4, seed=300)
     x = gen.make_tokens(900, 3).cuda()
@@ -120,11 +120,11 @@ def test_stack_graph_equals_eager_layers_and_replays_bit_exact(name):
     g.close()
 
 
-@pytest.mark.parametrize("name", ["q4k_shared_q4k", "q4k_shared_q8_0"])
+@pytest.mark.parametrize("name", ["q4k_shared_q4k", "q4k_shared_q8_0", "bf16"])
 def test_stack_paths_agree_bit_exact_and_report_their_kind(name):
     """The same stack through the persistent kernel and through four kernels
     per layer: identical bits; a stack the persistent kernel does not serve
-    (bf16 experts) is refused when that path is forced."""
+    (Q5_K routed down rows) is refused when that path is forced."""
     spec = SPECS[name]
     layers = _stack_layers(spec, 3, seed=310)
     x = gen.make_tokens(910, 2).cuda()
@@ -139,11 +139,11 @@ def test_stack_paths_agree_bit_exact_and_report_their_kind(name):
     for g in (gp, gl, ga):
         assert m.si_workspace_status(g.ws) == m.SI_OK
         g.close()
-    bf = _stack_layers(gen.BF16_LAYER, 2, seed=311)
+    q5 = _stack_layers(gen.NATIVE_LAYER_Q5K_DOWN, 2, seed=311)
     with pytest.raises(m.SiError) as e:
-        m.StackGraph(bf, x, mode=m.SI_STACK_PERSISTENT)
+        m.StackGraph(q5, x, mode=m.SI_STACK_PERSISTENT)
     assert e.value.status == m.SI_ERR_UNSUPPORTED
-    assert not m.StackGraph(bf, x).persistent
+    assert not m.StackGraph(q5, x).persistent
 
 
 PERSISTENT_SHAPES = {
@@ -153,6 +153,11 @@ PERSISTENT_SHAPES = {
     "i256_shared_q4k": gen.LayerSpec(inter=256, shared_type="q4_k"),
     "e128_shared_q8_0": gen.LayerSpec(n_experts=128, shared_type="q8_0"),
     "i256_shared_q8_0_is1024": gen.LayerSpec(inter=256, shared_inter=1024, shared_type="q8_0"),
+    "bf16_no_shared": gen.LayerSpec(expert_type="bf16", shared_inter=0, shared_type="bf16"),
+    "bf16_e128_top4_i768": gen.LayerSpec(expert_type="bf16", n_experts=128, top_k=4, inter=768,
+                                         shared_type="bf16"),
+    "bf16_e64_top2_i256": gen.LayerSpec(expert_type="bf16", n_experts=64, top_k=2, inter=256,
+                                        shared_inter=256, shared_type="bf16"),
 }
 
 

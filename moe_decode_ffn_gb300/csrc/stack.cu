@@ -239,9 +239,10 @@ SI_DEV float sigma_dot_bf(const __nv_bfloat16 *w, const uint4 *y_bf, int n, floa
 // kBfRing slots of 8 rows.
 constexpr int kBfGroups = 8;
 constexpr int kBfRing = 4;
-// after this many groups the block requests its routed down rows into L2
-// (earlier they would take DRAM time from the gate/up rows it waits for)
-constexpr int kBfDownAt = 3;
+// after this many rounds of two groups the block requests its routed down
+// rows into L2 (earlier they would take DRAM time from the gate/up rows it
+// waits for)
+constexpr int kBfDownAt = 2;
 static_assert(kBfRing <= kGuGroups, "the ring's slots use the gate/up barriers");
 // Issuing one bulk copy occupies the issuing thread for a few hundred cycles
 // whatever its size, and many small copies ramp up more slowly than a few
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   uint64_t *s_sel = reinterpret_cast<uint64_t *>(smem + 384);
   uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + 448);   // [64]
   float *h_s = reinterpret_cast<float *>(smem + 960);      // [32]
-  float *s_gu = reinterpret_cast<float *>(smem + 1088);    // [2][8] bf16 gate/up row dots
+  float *s_gu = reinterpret_cast<float *>(smem + 1088);    // [64] bf16 gate/up row dots
   StackLayerPtrs *s_layers = reinterpret_cast<StackLayerPtrs *>(smem + p.sm.layers);
   float *resid = reinterpret_cast<float *>(smem + p.sm.resid);
   float *y = reinterpret_cast<float *>(smem + p.sm.y);
@@ -782,18 +783,20 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
     // [G] gate/up of this block's unit -> h line
     if constexpr (kBf) {
       if (my_unit >= 0) {
-        // the unit's 8 groups of 4 gate + 4 up rows pass through the ring:
-        // warp w < 8 dots row w of the group in the four-kernel path's lane
-        // order and reduction; after a group's barrier its slot is refilled
-        // with the group 3 ahead and threads 0..3 form its 4 values of h
+        // the unit's 8 groups of 4 gate + 4 up rows pass through the ring two
+        // at a time: warps 0..7 take row w of group 2j, warps 8..15 row w - 8
+        // of group 2j + 1, each row dotted by one warp in the four-kernel
+        // path's lane order and reduction; after a round's barrier its two
+        // slots are refilled with the groups 4 ahead; h is formed at the end
         bool ok = true;
+        const int half = warp >> 3, wr = warp & 7;
 #pragma unroll 1
-        for (int g = 0; g < kBfGroups; ++g) {
-          const int sl = g % kBfRing;
+        for (int j = 0; j < kBfGroups / 2; ++j) {
+          const int g = 2 * j + half, sl = g % kBfRing;
           ok = mbar_wait_bounded(&bars[kBarGu + sl], (bf_ph >> sl) & 1u, p.status);
           bf_ph ^= 1u << sl;
-          if (ok && warp < 8) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(gu_buf + (sl * 8 + warp) * p.rb);
+          if (ok) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(gu_buf + (sl * 8 + wr) * p.rb);
             float acc = 0.f;
 #pragma unroll 1
             for (int c0 = 0; c0 < H; c0 += 2048) {
@@ -807,22 +810,23 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
             }
 #pragma unroll
             for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-            if (lane == 0) s_gu[8 * (g & 1) + warp] = acc;
+            if (lane == 0) s_gu[8 * g + wr] = acc;
           }
           if (__syncthreads_or(!ok)) goto fail;
-          if (threadIdx.x < 4) {
-            const float ag = s_gu[8 * (g & 1) + threadIdx.x], au = s_gu[8 * (g & 1) + 4 + threadIdx.x];
-            h_s[4 * g + threadIdx.x] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
-          }
-          if (threadIdx.x == 256 && g + kBfRing < kBfGroups)
-            issue_bf16_group(p, s_layers[l], s_sel, my_unit, units_r, shared_unit, g + kBfRing, gu_buf, bars,
-                             s_arm, pol);
-          if (g + 1 == kBfDownAt && lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {
+          if ((threadIdx.x == 256 || threadIdx.x == 288) && 2 * j + kBfRing < kBfGroups)
+            issue_bf16_group(p, s_layers[l], s_sel, my_unit, units_r, shared_unit,
+                             2 * j + kBfRing + (threadIdx.x == 288 ? 1 : 0), gu_buf, bars, s_arm, pol);
+          if (j + 1 == kBfDownAt && lane == 4 && warp >= 8 && warp < 8 + k && nrows > 0) {
             int e = key_index(s_sel[warp - 8]);
             if (e < 0 || e >= E) e = 0;
             bulk_prefetch_l2(s_layers[l].wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
                              static_cast<uint32_t>(nrows) * p.rbd);
           }
+        }
+        if (warp == 0) {   // pair q: gate row 8 (q / 4) + q % 4, up row + 4
+          const int gi = 8 * (lane >> 2) + (lane & 3);
+          const float ag = s_gu[gi], au = s_gu[gi + 4];
+          h_s[lane] = __fdiv_rn(ag, 1.f + expf(-ag)) * au;
         }
         // the routed down rows (in L2 since the selection) into the ring's
         // space, which no copy of this iteration targets any more

@@ -42,6 +42,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *_
   }
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
+    // a warp whose groups all lie past the end skips the encode (its lanes
+    // agree: the bound is the warp's first group), so a short vector costs
+    // one encode per thread, not kQuantUnroll
+    if (g0 + u * kQuantThreads + (threadIdx.x & ~31u) >= groups) break;
     uint32_t lo, hi;
     uint16_t d16, s16;
     q8_1_encode_4lanes(v[u], lo, hi, d16, s16);

@@ -97,108 +97,198 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
     }
     return;
   }
+  // Group the pairs q = (token q / k, rank q % k) by expert, stably: the
+  // position of pair q inside its expert's range is the number of pairs j < q
+  // with the same expert. Pairs are taken in chunks of 32 (one warp): within
+  // a chunk the lanes with the same expert find each other with a match, and
+  // a per-(chunk, expert) count, summed over the earlier chunks, gives the rest.
   __shared__ int s_cnt[kBatchedMaxExperts];
   __shared__ int s_off[kBatchedMaxExperts + 1];
   __shared__ int s_e[1024];
-  const int P = p.T * p.k;
+  __shared__ unsigned char s_rank[1024];
+  __shared__ unsigned short s_wc[32][kBatchedMaxExperts];   // [chunk][expert]
+  const int P = p.T * p.k;   // <= 1024 (host check)
+  const int nchunk = (P + 31) / 32;
+  const int lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_cnt[e] = 0;
+  for (int i = threadIdx.x; i < 32 * kBatchedMaxExperts; i += blockDim.x) (&s_wc[0][0])[i] = 0;
   __syncthreads();
-  for (int q = threadIdx.x; q < P; q += blockDim.x) {
-    int e = p.ids[q];
-    if (e < 0 || e >= p.E) {
-      record_status(p.status, SI_ERR_INVALID_ARG);
-      e = 0;
+  for (int q = threadIdx.x; q < 32 * nchunk; q += blockDim.x) {   // whole warps
+    int e = -1;
+    if (q < P) {
+      e = p.ids[q];
+      if (e < 0 || e >= p.E) {
+        record_status(p.status, SI_ERR_INVALID_ARG);
+        e = 0;
+      }
     }
-    if (q < 1024) s_e[q] = e;
-    atomicAdd(&s_cnt[e], 1);
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    if (q < P) {
+      s_e[q] = e;
+      s_rank[q] = static_cast<unsigned char>(__popc(same & ((1u << lane) - 1u)));
+      if ((__ffs(same) - 1) == lane) {   // the chunk's first pair of expert e
+        s_wc[q >> 5][e] = static_cast<unsigned short>(__popc(same));
+        atomicAdd(&s_cnt[e], __popc(same));
+      }
+    }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0, na = 0;
-    for (int e = 0; e < p.E; ++e) {
-      s_off[e] = acc;
-      acc += s_cnt[e];
-      if (s_cnt[e] > 0) p.active[na++] = e;
+  if (static_cast<int>(threadIdx.x) < p.E) {   // counts of the earlier chunks
+    const int e = threadIdx.x;
+    int acc = 0;
+    for (int c = 0; c < nchunk; ++c) {
+      const int v = s_wc[c][e];
+      s_wc[c][e] = static_cast<unsigned short>(acc);
+      acc += v;
     }
-    s_off[p.E] = acc;
-    *p.n_active = na;
+  } else if (threadIdx.x >= kPrepThreads - 32) {
+    // the last warp: expert offsets and the active list (ascending expert),
+    // lane L owning experts 8L .. 8L + 7
+    int cnt[8], sum = 0, nz = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * lane + i;
+      cnt[i] = e < p.E ? s_cnt[e] : 0;
+      sum += cnt[i];
+      nz += cnt[i] > 0;
+    }
+    int incl = sum, incl_nz = nz;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d), onz = __shfl_up_sync(0xffffffffu, incl_nz, d);
+      if (lane >= d) {
+        incl += o;
+        incl_nz += onz;
+      }
+    }
+    int acc = incl - sum, na = incl_nz - nz;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * lane + i;
+      if (e < p.E) {
+        s_off[e] = acc;
+        acc += cnt[i];
+        if (cnt[i] > 0) p.active[na++] = e;
+      }
+    }
+    if (lane == 31) {
+      s_off[p.E] = incl;
+      *p.n_active = incl_nz;
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) {
     p.offset[e] = s_off[e];
     if (e < p.E) p.count[e] = s_cnt[e];
   }
-  // Stable position of pair q inside its expert: pairs of that expert with a
-  // smaller index come first (token order, then rank order).
   for (int q = threadIdx.x; q < P; q += blockDim.x) {
     const int e = s_e[q];
-    int before = 0;
-    for (int j = 0; j < q; ++j) before += (s_e[j] == e);
-    const int pos = s_off[e] + before;
+    const int pos = s_off[e] + s_wc[q >> 5][e] + s_rank[q];
     p.pair_of[q] = pos;
     p.pair_token[pos] = q / p.k;
   }
 }
 
 // ---------------------------------------------------------------------------
-// One Q4_K super-block `w` (144 bytes, shared memory) against super-block sb
-// of the first nt token tiles at xt (Q8_1 tile records of width H, xrb bytes
-// apart): for each token exactly the single-token super-block dot (integer
-// sub-block sums, the fmas in sub-block order, one rounding per product and
-// one for the difference); the weight words and scales are read and unpacked
-// once for all the tokens.
-// The 32 code words of a Q4_K super-block (all 8 sub-blocks), loaded once
-// for every token; and the exact int32 sums of its 8 sub-blocks with one
-// token's 256 activation codes (a: that super-block of the token's tile).
-SI_DEV void q4k_sb_words(const uint4 *wv, uint32_t qw[32]) {
+// The code words of pair p (sub-blocks 2p, 2p + 1) of a Q4_K super-block,
+// split once into their low (sub-block 2p) and high (2p + 1) nibbles, and
+// the exact int32 sums of those nibbles with one token's 64 activation codes
+// of the pair (a4: sub-block 2p's 32 codes, then 2p + 1's): the integer sums
+// of q4k_pair_isums.
+SI_DEV void q4k_pair_nibbles(const uint4 *wv, int p, uint32_t lo[8], uint32_t hi[8]) {
+  uint32_t qw[8];
+  q4k_pair_words(wv, p, qw);
 #pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const uint4 u = wv[1 + v];
-    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
+  for (int i = 0; i < 8; ++i) {
+    lo[i] = qw[i] & 0x0F0F0F0Fu;
+    hi[i] = (qw[i] >> 4) & 0x0F0F0F0Fu;
   }
 }
-SI_DEV void q4k_sb_token_isums(const uint32_t qw[32], const uint4 *a, int isum[8]) {
+SI_DEV void q4k_pair_nibble_isums(const uint32_t lo[8], const uint32_t hi[8], const uint4 a4[4], int &slo,
+                                  int &shi) {
+  const uint32_t al[8] = {a4[0].x, a4[0].y, a4[0].z, a4[0].w, a4[1].x, a4[1].y, a4[1].z, a4[1].w};
+  const uint32_t ah[8] = {a4[2].x, a4[2].y, a4[2].z, a4[2].w, a4[3].x, a4[3].y, a4[3].z, a4[3].w};
+  slo = 0;
+  shi = 0;
 #pragma unroll
-  for (int pp = 0; pp < 4; ++pp) q4k_pair_isums(qw + 8 * pp, a + 4 * pp, isum[2 * pp], isum[2 * pp + 1]);
+  for (int i = 0; i < 8; ++i) {
+    slo = __dp4a(static_cast<int>(lo[i]), static_cast<int>(al[i]), slo);
+    shi = __dp4a(static_cast<int>(hi[i]), static_cast<int>(ah[i]), shi);
+  }
 }
 
-SI_DEV void q4k_sb_dot_tokens(const uint8_t *w, const uint8_t *xt, int xrb, int H, int sb, int nt,
-                              float out[kGuTok]) {
-  const uint4 *wv = reinterpret_cast<const uint4 *>(w);
-  const uint4 hd = wv[0];
-  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
-  int sc[8], mn[8];
-  q4k_unpack_scales(sw, sc, mn);
-  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
-  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
-  uint32_t qw[32];
-  q4k_sb_words(wv, qw);
+// Two rows' Q4_K super-blocks w0, w1 (the same super-block sb, shared
+// memory) against super-block sb of the first nt token tiles at xt: per
+// (row, token) exactly q4k_sb_dot's value (its integer sums, its fmas in
+// sub-block order, one rounding per product and one for the difference).
+// Each pair of sub-blocks is split into nibbles once for all the tokens and
+// each token's activation codes are read once for both rows.
+SI_DEV void q4k_sb_dot_2rows_tokens(const uint8_t *w0, const uint8_t *w1, const uint8_t *xt, int xrb, int H,
+                                    int sb, int nt, float out[2][kGuTok]) {
+  const uint4 *wv[2] = {reinterpret_cast<const uint4 *>(w0), reinterpret_cast<const uint4 *>(w1)};
+  uint32_t scp[2][2], mnp[2][2];   // 6-bit scales / mins of sub-blocks 0..3 and 4..7, one per byte
+  float d[2], dmin[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const uint4 hd = wv[r][0];
+    scp[r][0] = hd.y & 0x3F3F3F3Fu;
+    mnp[r][0] = hd.z & 0x3F3F3F3Fu;
+    scp[r][1] = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+    mnp[r][1] = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+    d[r] = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+    dmin[r] = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
+  }
+  float ad[2][kGuTok], am[2][kGuTok];
+#pragma unroll
+  for (int t = 0; t < kGuTok; ++t) ad[0][t] = ad[1][t] = am[0][t] = am[1][t] = 0.f;
   const int nsb = H / kQKK;
 #pragma unroll
-  for (int i = 0; i < kGuTok; ++i) {
-    if (i < nt) {
-      const uint8_t *rec = xt + i * xrb;
-      const uint4 *a = reinterpret_cast<const uint4 *>(rec + sb * kActSbStride);
-      const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb;
-      const float *sa = da + H / 32;
-      int isum[8];
-      q4k_sb_token_isums(qw, a, isum);
-      float acc_d = 0.f, acc_m = 0.f;
+  for (int pp = 0; pp < 4; ++pp) {
+    uint32_t lo[2][8], hi[2][8];
+    q4k_pair_nibbles(wv[0], pp, lo[0], hi[0]);
+    q4k_pair_nibbles(wv[1], pp, lo[1], hi[1]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc_d = fmaf(static_cast<float>(sc[j] * isum[j]), da[j], acc_d);
-        acc_m = fmaf(static_cast<float>(mn[j]), sa[j], acc_m);
+    for (int t = 0; t < kGuTok; ++t) {
+      if (t < nt) {
+        const uint8_t *rec = xt + t * xrb;
+        const uint4 *a = reinterpret_cast<const uint4 *>(rec + sb * kActSbStride) + 4 * pp;
+        const uint4 a4[4] = {a[0], a[1], a[2], a[3]};
+        const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb + 2 * pp;
+        const float *sa = da + H / 32;
+        const float da0 = da[0], da1 = da[1], sa0 = sa[0], sa1 = sa[1];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          int slo, shi;
+          q4k_pair_nibble_isums(lo[r], hi[r], a4, slo, shi);
+          const int j = 2 * pp;   // sub-blocks j, j + 1 (the same scale word)
+          const uint32_t sw = scp[r][j >> 2], mw = mnp[r][j >> 2];
+          const int sc0 = static_cast<int>((sw >> (8 * (j & 3))) & 0xFFu);
+          const int sc1 = static_cast<int>((sw >> (8 * ((j + 1) & 3))) & 0xFFu);
+          const int mn0 = static_cast<int>((mw >> (8 * (j & 3))) & 0xFFu);
+          const int mn1 = static_cast<int>((mw >> (8 * ((j + 1) & 3))) & 0xFFu);
+          ad[r][t] = fmaf(static_cast<float>(sc0 * slo), da0, ad[r][t]);
+          am[r][t] = fmaf(static_cast<float>(mn0), sa0, am[r][t]);
+          ad[r][t] = fmaf(static_cast<float>(sc1 * shi), da1, ad[r][t]);
+          am[r][t] = fmaf(static_cast<float>(mn1), sa1, am[r][t]);
+        }
       }
-      out[i] = __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
     }
   }
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int t = 0; t < kGuTok; ++t)
+      if (t < nt) out[r][t] = __fsub_rn(__fmul_rn(d[r], ad[r][t]), __fmul_rn(dmin[r], am[r][t]));
 }
 
 // Gate/up, integer mode: one block per (active expert, 32-row unit of h).
 // Warp w issues one bulk copy of 8 gate (w < 4) or up rows and, per chunk of
 // up to kGuTok of the expert's tokens, the copy of token tile w. Thread
 // (row pair prq, gate/up m, lane8) owns super-blocks lane8, lane8 + 8, ... of
-// rows prq and prq + 16 and dots each against all the chunk's tokens.
+// rows prq and prq + 16 and dots both against all the chunk's tokens (each
+// pair of sub-blocks split into nibbles once, each token's codes read once
+// for both rows); the row dots go to shared memory and warp w forms token
+// w's h = silu(gate) * up and its Q8_1 block.
 __global__ void __launch_bounds__(kGuBThreads, 2) gateup_grouped_kernel(BatchedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int units = p.I / 32;
@@ -206,8 +296,8 @@ __global__ void __launch_bounds__(kGuBThreads, 2) gateup_grouped_kernel(BatchedP
   const int xrb = tile_record_bytes(p.H);
   const int hrb = tile_record_bytes(p.I);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);        // 4 weight groups + 1 tokens
-  float *h_s = reinterpret_cast<float *>(smem + 64);          // [kGuTok][32]
-  uint8_t *xt = smem + 64 + kGuTok * 32 * 4;                  // [kGuTok][xrb]
+  float *s_raw = reinterpret_cast<float *>(smem + 64);        // [kGuTok][gate, up][32] row dots
+  uint8_t *xt = smem + 64 + kGuTok * 64 * 4;                  // [kGuTok][xrb]
   uint8_t *wbuf = xt + kGuTok * xrb;                          // gate [32][rb], up [32][rb]
   grid_dep_wait();
   grid_dep_launch();
@@ -244,39 +334,47 @@ __global__ void __launch_bounds__(kGuBThreads, 2) gateup_grouped_kernel(BatchedP
     }
     mbar_wait_bounded(&bars[4], phase, p.status);
     phase ^= 1u;
+    // rows prq and prq + 16 of matrix m, together
+    if (c0 == 0) {
+      mbar_wait_bounded(&bars[prq >> 3], 0, p.status);
+      mbar_wait_bounded(&bars[(prq + 16) >> 3], 0, p.status);
+    }
+    const uint8_t *row0 = (m ? up_buf : gate_buf) + prq * rb;
+    float acc[2][kGuTok];
+#pragma unroll
+    for (int i = 0; i < kGuTok; ++i) acc[0][i] = acc[1][i] = 0.f;
 #pragma unroll 1
+    for (int sb = lane8; sb < nsb; sb += 8) {
+      float dv[2][kGuTok];
+      q4k_sb_dot_2rows_tokens(row0 + sb * kQ4KBytes, row0 + 16 * rb + sb * kQ4KBytes, xt, xrb, p.H, sb, nc, dv);
+#pragma unroll
+      for (int i = 0; i < kGuTok; ++i)
+        if (i < nc) {
+          acc[0][i] += dv[0][i];
+          acc[1][i] += dv[1][i];
+        }
+    }
+#pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int pr = prq + 16 * rr;
-      if (c0 == 0) mbar_wait_bounded(&bars[pr >> 3], 0, p.status);
-      const uint8_t *row = (m ? up_buf : gate_buf) + pr * rb;
-      float acc[kGuTok];
-#pragma unroll
-      for (int i = 0; i < kGuTok; ++i) acc[i] = 0.f;
-#pragma unroll 1
-      for (int sb = lane8; sb < nsb; sb += 8) {
-        float dv[kGuTok];
-        q4k_sb_dot_tokens(row + sb * kQ4KBytes, xt, xrb, p.H, sb, nc, dv);
-#pragma unroll
-        for (int i = 0; i < kGuTok; ++i)
-          if (i < nc) acc[i] += dv[i];
-      }
 #pragma unroll
       for (int i = 0; i < kGuTok; ++i) {
         if (i < nc) {   // nc is uniform over the block
-          float v = acc[i];
+          float v = acc[rr][i];
           v += __shfl_xor_sync(0xffffffffu, v, 1);
           v += __shfl_xor_sync(0xffffffffu, v, 2);
           v += __shfl_xor_sync(0xffffffffu, v, 4);
-          const float u = __shfl_xor_sync(0xffffffffu, v, 8);
-          if ((threadIdx.x & 15) == 0) h_s[i * 32 + pr] = __fdiv_rn(v, 1.f + expf(-v)) * u;
+          if (lane8 == 0) s_raw[(2 * i + m) * 32 + pr] = v;
         }
       }
     }
     __syncthreads();
-    // Q8_1 of each token's 32 values of h: warp w encodes token w of the chunk
+    // warp w: token w of the chunk; lane j: h_j = silu(gate_j) * up_j, then
+    // the Q8_1 block of the token's 32 values of h
     for (int i = warp; i < nc; i += kGuBThreads / 32) {
+      const float g = s_raw[(2 * i) * 32 + lane], u = s_raw[(2 * i + 1) * 32 + lane];
       uint16_t d16, s16;
-      const int q = q8_1_encode_warp(h_s[i * 32 + lane], d16, s16);
+      const int q = q8_1_encode_warp(__fdiv_rn(g, 1.f + expf(-g)) * u, d16, s16);
       ActTile h = tile_at(p.hrec + static_cast<size_t>(p0 + c0 + i) * hrb, p.I);
       const int j0 = unit * 32;   // element offset of this unit inside the pair's h
       h.qs[(j0 / kQKK) * kActSbStride + j0 % kQKK + lane] = static_cast<uint8_t>(q);
@@ -285,7 +383,7 @@ __global__ void __launch_bounds__(kGuBThreads, 2) gateup_grouped_kernel(BatchedP
         h.s[j0 / 32] = half_bits_to_float(s16);
       }
     }
-    __syncthreads();   // h_s and the token tiles are reused by the next chunk
+    __syncthreads();   // the row dots and the token tiles are reused by the next chunk
   }
 }
 
@@ -747,13 +845,18 @@ __global__ void tokens_block_dots_kernel(const uint8_t *w, int rows, int k, cons
     const uint4 *wv = reinterpret_cast<const uint4 *>(w + (static_cast<size_t>(r) * nsb + sb) * kQ4KBytes);
     int32_t *o = out + static_cast<size_t>(r) * nb + 8 * sb;
     if (!halves) {
-      uint32_t qw[32];
-      q4k_sb_words(wv, qw);
-      for (int t = 0; t < n_vec; ++t) {
-        int isum[8];
-        q4k_sb_token_isums(qw, reinterpret_cast<const uint4 *>(smem + t * rec + sb * kActSbStride), isum);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o[static_cast<size_t>(t) * rows * nb + j] = isum[j];
+#pragma unroll 1
+      for (int pp = 0; pp < 4; ++pp) {
+        uint32_t lo[8], hi[8];
+        q4k_pair_nibbles(wv, pp, lo, hi);
+        for (int t = 0; t < n_vec; ++t) {
+          const uint4 *a = reinterpret_cast<const uint4 *>(smem + t * rec + sb * kActSbStride) + 4 * pp;
+          const uint4 a4[4] = {a[0], a[1], a[2], a[3]};
+          int slo, shi;
+          q4k_pair_nibble_isums(lo, hi, a4, slo, shi);
+          o[static_cast<size_t>(t) * rows * nb + 2 * pp] = slo;
+          o[static_cast<size_t>(t) * rows * nb + 2 * pp + 1] = shi;
+        }
       }
     } else {
 #pragma unroll 1
@@ -829,7 +932,7 @@ static si_status batched_check(const si_moe_layer &L, int T) {
 }
 
 static size_t gateup_grouped_smem(const si_moe_layer &L) {
-  return 64 + kGuTok * 32 * 4 + static_cast<size_t>(kGuTok) * tile_record_bytes(L.hidden) +
+  return 64 + kGuTok * 64 * 4 + static_cast<size_t>(kGuTok) * tile_record_bytes(L.hidden) +
          64u * (L.hidden / 256 * kQ4KBytes);
 }
 static size_t down_grouped_smem(const si_moe_layer &L) {

@@ -35,7 +35,8 @@ constexpr int kGuBThreads = 256;     // two gate/up blocks per SM: one's copies 
 constexpr int kGuTok = 8;            // token tiles resident per gate/up block at once
 constexpr int kDownBThreads = 256;
 constexpr int kDnTok = 8;            // token tiles resident per down block at once
-constexpr int kDownRows = 32;        // output rows per down block
+// down blocks: 32 R output rows (R = 2 unless the block's shared memory
+// would not fit), 32 threads per half super-block of a row (at most 8 warps)
 
 // Size of one token's Q8_1 tile record: codes at the padded super-block
 // stride, then d and s (fp32) per 32-block; a multiple of 16 bytes.
@@ -388,87 +389,95 @@ __global__ void __launch_bounds__(kGuBThreads, 2) gateup_grouped_kernel(BatchedP
 }
 
 // ---------------------------------------------------------------------------
-// Half h (sub-blocks 4h..4h+3) of one Q4_K super-block `w` against
-// super-block sb of the first nt Q8_1 tiles at ht (width I, hrb bytes apart):
-// per token exactly the single-token half dot (the same integer sums, fmas in
-// sub-block order and roundings); the weight words and scales are read and
-// unpacked once for all the tokens.
-// The 16 code words of half h of a Q4_K super-block (sub-blocks 4h .. 4h +
-// 3), loaded once for every token; and the exact int32 sums of those 4
-// sub-blocks with one token's activation codes (a: the super-block of the
-// token's tile).
-SI_DEV void q4k_half_words(const uint4 *wv, int h, uint32_t qw[16]) {
+// Half h (sub-blocks 4h .. 4h + 3, 128 weights) of super-block sb of R rows
+// (w[r], shared memory) against super-block sb of the first nt Q8_1 tiles at
+// ht (width I, hrb bytes apart): per (row, token) exactly the single-token
+// half dot (the integer sums of q4k_pair_isums, the fmas in sub-block order,
+// one rounding per product and one for the difference). Each pair of
+// sub-blocks is split into nibbles once and each token's codes are read once
+// for all R rows.
+template <int R>
+SI_DEV void q4k_half_dot_rows_tokens(const uint8_t *const w[R], const uint8_t *ht, int hrb, int I, int sb, int h,
+                                     int nt, float out[R][kDnTok]) {
+  uint32_t scw[R], mnw[R];   // 6-bit scales / mins of sub-blocks 4h .. 4h + 3, one per byte
+  float d[R], dmin[R];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 u = wv[1 + 4 * h + v];
-    qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
+  for (int r = 0; r < R; ++r) {
+    const uint4 hd = reinterpret_cast<const uint4 *>(w[r])[0];
+    scw[r] = h ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
+    mnw[r] = h ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
+    d[r] = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
+    dmin[r] = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
   }
-}
-SI_DEV void q4k_half_token_isums(const uint32_t qw[16], const uint4 *a, int h, int isum[4]) {
+  float ad[R][kDnTok], am[R][kDnTok];
 #pragma unroll
-  for (int pp = 0; pp < 2; ++pp)
-    q4k_pair_isums(qw + 8 * pp, a + 4 * (2 * h + pp), isum[2 * pp], isum[2 * pp + 1]);
-}
-
-SI_DEV void q4k_half_dot_tokens(const uint8_t *w, const uint8_t *ht, int hrb, int I, int sb, int h,
-                                int nt, float out[kDnTok]) {
-  const uint4 *wv = reinterpret_cast<const uint4 *>(w);
-  const uint4 hd = wv[0];
-  int sc8[8], mn8[8];
-  const uint32_t sw[3] = {hd.y, hd.z, hd.w};
-  q4k_unpack_scales(sw, sc8, mn8);
-  int sc[4], mn[4];
+  for (int r = 0; r < R; ++r)
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    sc[i] = h ? sc8[4 + i] : sc8[i];
-    mn[i] = h ? mn8[4 + i] : mn8[i];
-  }
-  const float d = half_bits_to_float(static_cast<uint16_t>(hd.x & 0xFFFF));
-  const float dmin = half_bits_to_float(static_cast<uint16_t>(hd.x >> 16));
-  uint32_t qw[16];   // the half's 64 code bytes
-  q4k_half_words(wv, h, qw);
+    for (int t = 0; t < kDnTok; ++t) ad[r][t] = am[r][t] = 0.f;
   const int nsb = I / kQKK;
 #pragma unroll
-  for (int i = 0; i < kDnTok; ++i) {
-    if (i < nt) {
-      const uint8_t *rec = ht + i * hrb;
-      const uint4 *a = reinterpret_cast<const uint4 *>(rec + sb * kActSbStride);
-      const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb;
-      const float *sa = da + I / 32;
-      int isum[4];
-      q4k_half_token_isums(qw, a, h, isum);
-      float acc_d = 0.f, acc_m = 0.f;
+  for (int pp = 0; pp < 2; ++pp) {
+    const int pr = 2 * h + pp;   // pair of the super-block
+    uint32_t lo[R][8], hi[R][8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc_d = fmaf(static_cast<float>(sc[q] * isum[q]), da[4 * h + q], acc_d);
-        acc_m = fmaf(static_cast<float>(mn[q]), sa[4 * h + q], acc_m);
+    for (int r = 0; r < R; ++r) q4k_pair_nibbles(reinterpret_cast<const uint4 *>(w[r]), pr, lo[r], hi[r]);
+#pragma unroll
+    for (int t = 0; t < kDnTok; ++t) {
+      if (t < nt) {
+        const uint8_t *rec = ht + t * hrb;
+        const uint4 *a = reinterpret_cast<const uint4 *>(rec + sb * kActSbStride) + 4 * pr;
+        const uint4 a4[4] = {a[0], a[1], a[2], a[3]};
+        const float *da = reinterpret_cast<const float *>(rec + nsb * kActSbStride) + 8 * sb + 2 * pr;
+        const float *sa = da + I / 32;
+        const float da0 = da[0], da1 = da[1], sa0 = sa[0], sa1 = sa[1];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          int slo, shi;
+          q4k_pair_nibble_isums(lo[r], hi[r], a4, slo, shi);
+          const int sc0 = static_cast<int>((scw[r] >> (16 * pp)) & 0xFFu);
+          const int sc1 = static_cast<int>((scw[r] >> (16 * pp + 8)) & 0xFFu);
+          const int mn0 = static_cast<int>((mnw[r] >> (16 * pp)) & 0xFFu);
+          const int mn1 = static_cast<int>((mnw[r] >> (16 * pp + 8)) & 0xFFu);
+          ad[r][t] = fmaf(static_cast<float>(sc0 * slo), da0, ad[r][t]);
+          am[r][t] = fmaf(static_cast<float>(mn0), sa0, am[r][t]);
+          ad[r][t] = fmaf(static_cast<float>(sc1 * shi), da1, ad[r][t]);
+          am[r][t] = fmaf(static_cast<float>(mn1), sa1, am[r][t]);
+        }
       }
-      out[i] = __fsub_rn(__fmul_rn(d, acc_d), __fmul_rn(dmin, acc_m));
     }
   }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int t = 0; t < kDnTok; ++t)
+      if (t < nt) out[r][t] = __fsub_rn(__fmul_rn(d[r], ad[r][t]), __fmul_rn(dmin[r], am[r][t]));
 }
 
-// Down, integer mode: one block per (active expert, 32 output rows). The
+// Down, integer mode: one block per (active expert, 32 R output rows). The
 // rows arrive once by bulk copy; per chunk of up to kDnTok of the expert's
-// pairs, each (row, half super-block) piece is dotted with every pair's h,
-// then each (pair, row) sums its pieces in order.
+// pairs, warp w takes the half super-blocks q = w, w + warps, ... of every
+// row (so its lanes read the same activation codes) and lane l the rows l,
+// l + 32, ...; then each (pair, row) sums its pieces in order.
+template <int R>
 __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const int tiles = p.H / kDownRows;
+  constexpr int kRows = 32 * R;
+  const int tiles = p.H / kRows;
   const int nsb = p.I / kQKK;
   const int P = 2 * nsb;                 // half super-block pieces per row
   const int hrb = tile_record_bytes(p.I);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);           // weights, tokens
-  float *part = reinterpret_cast<float *>(smem + 64);            // [kDnTok][kDownRows][P]
-  uint8_t *ht = smem + 64 + kDnTok * kDownRows * P * 4;          // [kDnTok][hrb]
-  uint8_t *wbuf = ht + kDnTok * hrb;                             // [kDownRows][rb_d]
+  float *part = reinterpret_cast<float *>(smem + 64);            // [kDnTok][P][kRows]
+  uint8_t *ht = smem + 64 + kDnTok * kRows * P * 4;              // [kDnTok][hrb]
+  uint8_t *wbuf = ht + kDnTok * hrb;                             // [kRows][rb_d]
   grid_dep_wait();
   grid_dep_launch();
   const int na = __ldcg(p.n_active);
   if (static_cast<int>(blockIdx.x) >= na * tiles) return;
   const int e = __ldcg(p.active + blockIdx.x / tiles);
-  const int j0 = (blockIdx.x % tiles) * kDownRows;
+  const int j0 = (blockIdx.x % tiles) * kRows;
   const int n_e = __ldcg(p.count + e), p0 = __ldcg(p.offset + e);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   if (threadIdx.x == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
@@ -476,7 +485,7 @@ __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedPara
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    const uint32_t bytes = static_cast<uint32_t>(kDownRows) * p.rb_d;
+    const uint32_t bytes = static_cast<uint32_t>(kRows) * p.rb_d;
     mbar_arrive_expect_tx(&bars[0], bytes);
     bulk_g2s_evict_first(wbuf, p.wd + (static_cast<size_t>(e) * p.H + j0) * p.rb_d, bytes, &bars[0],
                          policy_evict_first());
@@ -491,19 +500,25 @@ __global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedPara
     mbar_wait_bounded(&bars[1], phase, p.status);
     phase ^= 1u;
     if (c0 == 0) mbar_wait_bounded(&bars[0], 0, p.status);
-    for (int u = threadIdx.x; u < kDownRows * P; u += blockDim.x) {
-      const int jl = u / P, q = u % P, sb = q >> 1;
-      float dv[kDnTok];
-      q4k_half_dot_tokens(wbuf + jl * p.rb_d + sb * kQ4KBytes, ht, hrb, p.I, sb, q & 1, nc, dv);
+#pragma unroll 1
+    for (int q = warp; q < P; q += nw) {   // warp-uniform
+      const int sb = q >> 1, h = q & 1;
+      const uint8_t *w[R];
 #pragma unroll
-      for (int i = 0; i < kDnTok; ++i)
-        if (i < nc) part[(i * kDownRows + jl) * P + q] = dv[i];
+      for (int r = 0; r < R; ++r) w[r] = wbuf + (lane + 32 * r) * p.rb_d + sb * kQ4KBytes;
+      float dv[R][kDnTok];
+      q4k_half_dot_rows_tokens<R>(w, ht, hrb, p.I, sb, h, nc, dv);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int i = 0; i < kDnTok; ++i)
+          if (i < nc) part[(i * P + q) * kRows + lane + 32 * r] = dv[r][i];
     }
     __syncthreads();
-    for (int v = threadIdx.x; v < nc * kDownRows; v += blockDim.x) {
-      const int i = v / kDownRows, jl = v % kDownRows;
+    for (int v = threadIdx.x; v < nc * kRows; v += blockDim.x) {
+      const int i = v / kRows, jl = v % kRows;
       float y = 0.f;
-      for (int q = 0; q < P; ++q) y += part[(i * kDownRows + jl) * P + q];
+      for (int q = 0; q < P; ++q) y += part[(i * P + q) * kRows + jl];
       p.y[static_cast<size_t>(p0 + c0 + i) * p.H + j0 + jl] = y;
     }
     __syncthreads();   // part and the h tiles are reused by the next chunk
@@ -859,16 +874,18 @@ __global__ void tokens_block_dots_kernel(const uint8_t *w, int rows, int k, cons
         }
       }
     } else {
+      // halves: the same nibble functions, pair by pair as the down kernel
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        uint32_t qw[16];
-        q4k_half_words(wv, h, qw);
+      for (int pp = 0; pp < 4; ++pp) {
+        uint32_t lo[8], hi[8];
+        q4k_pair_nibbles(wv, pp, lo, hi);
         for (int t = 0; t < n_vec; ++t) {
-          int isum[4];
-          q4k_half_token_isums(qw, reinterpret_cast<const uint4 *>(smem + t * rec + sb * kActSbStride), h,
-                               isum);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) o[static_cast<size_t>(t) * rows * nb + 4 * h + j] = isum[j];
+          const uint4 *a = reinterpret_cast<const uint4 *>(smem + t * rec + sb * kActSbStride) + 4 * pp;
+          const uint4 a4[4] = {a[0], a[1], a[2], a[3]};
+          int slo, shi;
+          q4k_pair_nibble_isums(lo, hi, a4, slo, shi);
+          o[static_cast<size_t>(t) * rows * nb + 2 * pp] = slo;
+          o[static_cast<size_t>(t) * rows * nb + 2 * pp + 1] = shi;
         }
       }
     }
@@ -935,18 +952,22 @@ static size_t gateup_grouped_smem(const si_moe_layer &L) {
   return 64 + kGuTok * 64 * 4 + static_cast<size_t>(kGuTok) * tile_record_bytes(L.hidden) +
          64u * (L.hidden / 256 * kQ4KBytes);
 }
-static size_t down_grouped_smem(const si_moe_layer &L) {
-  const int P = 2 * (L.inter / 256);
-  return 64 + static_cast<size_t>(kDnTok) * kDownRows * P * 4 +
+static size_t down_grouped_smem(const si_moe_layer &L, int R) {
+  const int P = 2 * (L.inter / 256), rows = 32 * R;
+  return 64 + static_cast<size_t>(kDnTok) * rows * P * 4 +
          static_cast<size_t>(kDnTok) * tile_record_bytes(L.inter) +
-         static_cast<size_t>(kDownRows) * (L.inter / 256 * kQ4KBytes);
+         static_cast<size_t>(rows) * (L.inter / 256 * kQ4KBytes);
+}
+static int down_rows_per_lane(const si_moe_layer &L) {
+  return down_grouped_smem(L, 2) <= 227 * 1024 ? 2 : 1;
 }
 
 cudaError_t preload_batched() {
   cudaFuncAttributes a;
   const void *ks[] = {reinterpret_cast<const void *>(batched_prep_kernel),
                       reinterpret_cast<const void *>(gateup_grouped_kernel),
-                      reinterpret_cast<const void *>(down_grouped_kernel),
+                      reinterpret_cast<const void *>(down_grouped_kernel<1>),
+                      reinterpret_cast<const void *>(down_grouped_kernel<2>),
                       reinterpret_cast<const void *>(tc_gateup_kernel),
                       reinterpret_cast<const void *>(tc_down_kernel),
                       reinterpret_cast<const void *>(combine_kernel)};
@@ -1015,18 +1036,22 @@ si_status batched_launch(const si_moe_layer *L, int n_tokens, int mode, const vo
       e = launch_pdl(combine_kernel, dim3((L->hidden + 255) / 256, n_tokens), dim3(256), 0, s, p);
     return cuda_status(e);
   }
-  const int units = L->inter / 32, tiles = L->hidden / kDownRows;
+  const int R = down_rows_per_lane(*L);
+  const int units = L->inter / 32, tiles = L->hidden / (32 * R);
   const int max_active = n_tokens * L->top_k < L->n_experts ? n_tokens * L->top_k : L->n_experts;
-  const size_t gsm = gateup_grouped_smem(*L), dsm = down_grouped_smem(*L);
+  const size_t gsm = gateup_grouped_smem(*L), dsm = down_grouped_smem(*L, R);
   if (gsm > 227 * 1024 || dsm > 227 * 1024) return SI_ERR_UNSUPPORTED;
+  auto down = R == 2 ? down_grouped_kernel<2> : down_grouped_kernel<1>;
+  const int P = 2 * (L->inter / 256);
+  const int down_threads = 32 * (P < kDownBThreads / 32 ? P : kDownBThreads / 32);
   cudaError_t e = allow_smem(gateup_grouped_kernel, gsm);
-  if (e == cudaSuccess) e = allow_smem(down_grouped_kernel, dsm);
+  if (e == cudaSuccess) e = allow_smem(down, dsm);
   if (e == cudaSuccess)
     e = launch_pdl(batched_prep_kernel, dim3(1 + n_tokens), dim3(kPrepThreads), 0, s, p);
   if (e == cudaSuccess)
     e = launch_pdl(gateup_grouped_kernel, dim3(max_active * units), dim3(kGuBThreads), gsm, s, p);
   if (e == cudaSuccess)
-    e = launch_pdl(down_grouped_kernel, dim3(max_active * tiles), dim3(kDownBThreads), dsm, s, p);
+    e = launch_pdl(down, dim3(max_active * tiles), dim3(down_threads), dsm, s, p);
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel, dim3((L->hidden + 255) / 256, n_tokens), dim3(256), 0, s, p);
   return cuda_status(e);

@@ -32,9 +32,9 @@ namespace si {
 constexpr int kBatchedMaxExperts = 256;
 constexpr int kPrepThreads = 512;
 constexpr int kGuBThreads = 256;     // two gate/up blocks per SM: one's copies overlap the other's dots
-constexpr int kGuTok = 8;            // token tiles resident per gate/up block at once
+constexpr int kGuTok = 4;            // token tiles resident per gate/up block at once
 constexpr int kDownBThreads = 256;
-constexpr int kDnTok = 8;            // token tiles resident per down block at once
+constexpr int kDnTok = 4;            // token tiles resident per down block at once
 // down blocks: 32 R output rows (R = 2 unless the block's shared memory
 // would not fit), 32 threads per half super-block of a row (at most 8 warps)
 

@@ -40,6 +40,7 @@ constexpr int kRouterThreads = 256;
 constexpr int kRouterWarps = kRouterThreads / 32;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxChunkTokens = 8;
+static_assert(kMaxChunkTokens <= kRouterWarps, "the last block selects one token per warp");
 
 struct RouterParams {
   const void *x;
@@ -186,16 +187,35 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
     return;
   }
 
-  // Per token: every warp sorts 32 of the logits; the first 8 of each warp
-  // are the only candidates; each candidate's rank among the <= 64
-  // candidates is its rank overall (a key in the overall first k is in the
-  // first k of its own warp).
-  __shared__ uint64_t s_cand[kRouterWarps * kMaxTopK];
-  __shared__ uint64_t s_sel[kMaxTopK];
-  for (int tt = 0; tt < ntok; ++tt) {
-    const int t = t0 + tt;
+  // The selection: top k of the E keys in rank order (keys are unique, so it
+  // is one set whatever the method), then the softmax over them in rank
+  // order, written by write_selection.
+  auto write_selection = [&](int t, const uint64_t sel[kMaxTopK]) {
+    const float v0 = key_value(sel[0]);
+    float exv[kMaxTopK];
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxTopK; ++q) {
+      exv[q] = q < p.k ? expf(key_value(sel[q]) - v0) : 0.f;
+      sum += exv[q];
+    }
+    const float inv = __frcp_rn(sum);
+#pragma unroll
+    for (int q = 0; q < kMaxTopK; ++q) {
+      if (q < p.k) {
+        p.ids[static_cast<size_t>(t) * p.k + q] = key_index(sel[q]);
+        p.wts[static_cast<size_t>(t) * p.k + q] = exv[q] * inv;
+      }
+    }
+  };
+  if (ntok == 1) {
+    // one token: every warp sorts 32 of its keys; the first k of each warp
+    // are the only candidates, and a candidate's rank among them is its
+    // rank overall
+    __shared__ uint64_t s_cand[kRouterWarps * kMaxTopK];
+    __shared__ uint64_t s_sel[kMaxTopK];
     const int ex = threadIdx.x;
-    uint64_t key = ex < p.E ? make_key(s_logit[tt][ex], ex) : 0ull;   // 0: below every real key
+    uint64_t key = ex < p.E ? make_key(s_logit[0][ex], ex) : 0ull;   // 0: below every real key
     key = warp_sort32(key, lane);
     if (lane < kMaxTopK) s_cand[warp * kMaxTopK + lane] = key;
     __syncthreads();
@@ -208,24 +228,40 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      const float v0 = key_value(s_sel[0]);
-      float exv[kMaxTopK];
-      float sum = 0.f;
+      uint64_t sel[kMaxTopK];
 #pragma unroll
-      for (int q = 0; q < kMaxTopK; ++q) {
-        exv[q] = q < p.k ? expf(key_value(s_sel[q]) - v0) : 0.f;
-        sum += exv[q];
-      }
-      const float inv = __frcp_rn(sum);
+      for (int q = 0; q < kMaxTopK; ++q) sel[q] = q < p.k ? s_sel[q] : 0ull;
+      write_selection(t0, sel);
+    }
+  } else if (warp < ntok) {
+    // several tokens, one warp each (warp w takes token t0 + w, all at
+    // once): lane l holds the keys of experts l, l + 32, ...; k rounds of a
+    // warp-wide maximum take the top k in rank order (each round's maximum
+    // sits in one lane, which drops it)
+    const int t = t0 + warp;
+    uint64_t kk[256 / 32];
 #pragma unroll
-      for (int q = 0; q < kMaxTopK; ++q) {
-        if (q < p.k) {
-          p.ids[static_cast<size_t>(t) * p.k + q] = key_index(s_sel[q]);
-          p.wts[static_cast<size_t>(t) * p.k + q] = exv[q] * inv;
-        }
+    for (int i = 0; i < 256 / 32; ++i) {
+      const int e = lane + 32 * i;
+      kk[i] = e < p.E ? make_key(s_logit[warp][e], e) : 0ull;   // 0: below every real key
+    }
+    uint64_t sel[kMaxTopK];
+#pragma unroll
+    for (int q = 0; q < kMaxTopK; ++q) {
+      sel[q] = 0ull;
+      if (q < p.k) {
+        uint64_t m = kk[0];
+#pragma unroll
+        for (int i = 1; i < 256 / 32; ++i) m = kmax(m, kk[i]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = kmax(m, __shfl_xor_sync(0xffffffffu, m, off));
+#pragma unroll
+        for (int i = 0; i < 256 / 32; ++i)
+          if (kk[i] == m) kk[i] = 0ull;
+        sel[q] = m;
       }
     }
-    __syncthreads();
+    if (lane == 0) write_selection(t, sel);
   }
   SI_TRACE_MARK(0, 6);
 }

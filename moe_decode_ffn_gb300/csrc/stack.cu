@@ -976,40 +976,57 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         // chunk, then the 8 lanes are summed
         const int sub = lane >> 3, l8 = lane & 7;
         const int ntask = (k + (kShared ? 1 : 0)) * J;
+        // two tasks per 8 lanes at a time (tasks t and t + 64), their
+        // products interleaved: two independent fma chains, each in the
+        // order of its own task
 #pragma unroll 1
-        for (int t0 = 0; t0 < ntask; t0 += 4 * (kStkThreads / 32)) {
-          const int task = t0 + 4 * warp + sub;
-          const int r = task / J, jl = task - r * J;
-          const bool live = task < ntask && jl < nrows;
-          float acc = 0.f;
-          if (live) {
-            const bool sh = kShared && r == k;
-            const int width = sh ? Is : I;
-            const uint8_t *row = sh ? sd_buf + static_cast<size_t>(jl) * p.rbsd
-                                    : dn_buf + static_cast<size_t>(r * J + jl) * p.rbd;
-            const float *hv = hf + r * I;
-#pragma unroll 1
-            for (int cc = 0; cc < width; cc += 512) {
+        for (int t0 = 0; t0 < ntask; t0 += 8 * (kStkThreads / 32)) {
+          int tr[2], tj[2], tw[2];
+          bool live[2];
+          const uint8_t *row[2];
+          const float *hv[2];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
+          for (int u = 0; u < 2; ++u) {
+            const int task = t0 + 4 * (kStkThreads / 32) * u + 4 * warp + sub;
+            tr[u] = task / J;
+            tj[u] = task - tr[u] * J;
+            live[u] = task < ntask && tj[u] < nrows;
+            const bool sh = kShared && tr[u] == k;
+            tw[u] = live[u] ? (sh ? Is : I) : 0;
+            row[u] = sh ? sd_buf + static_cast<size_t>(tj[u]) * p.rbsd
+                        : dn_buf + static_cast<size_t>(tr[u] * J + tj[u]) * p.rbd;
+            hv[u] = hf + tr[u] * I;
+          }
+          float acc[2] = {0.f, 0.f};
+          const int wmax = tw[0] > tw[1] ? tw[0] : tw[1];
+#pragma unroll 1
+          for (int cc = 0; cc < wmax; cc += 512) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
                 const int col = cc + l8 * 8 + 64 * i;
-                if (col < width) {
+                if (col < tw[u]) {
                   // dot_down8's products and order; h read as two float4
                   float wv[8];
-                  Load8<__nv_bfloat16>::run(row + 2 * col, wv);
-                  const float4 h0 = *reinterpret_cast<const float4 *>(hv + col);
-                  const float4 h1 = *reinterpret_cast<const float4 *>(hv + col + 4);
+                  Load8<__nv_bfloat16>::run(row[u] + 2 * col, wv);
+                  const float4 h0 = *reinterpret_cast<const float4 *>(hv[u] + col);
+                  const float4 h1 = *reinterpret_cast<const float4 *>(hv[u] + col + 4);
                   const float hh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-                  for (int q = 0; q < 8; ++q) acc = fmaf(wv[q], hh[q], acc);
+                  for (int q = 0; q < 8; ++q) acc[u] = fmaf(wv[q], hh[q], acc[u]);
                 }
               }
             }
           }
-          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-          if (live && l8 == 0) part[r * J + jl] = acc;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float v = acc[u];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            if (live[u] && l8 == 0) part[tr[u] * J + tj[u]] = v;
+          }
         }
       } else {
 #pragma unroll

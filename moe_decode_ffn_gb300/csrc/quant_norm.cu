@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *_
   grid_dep_launch();
   const int64_t groups = n / 8;
   const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kQuantThreads * kQuantUnroll;
+  const bool full = g0 + kQuantThreads * kQuantUnroll <= groups;
   float v[kQuantUnroll][8];
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
@@ -42,10 +43,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *_
   }
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
-    // a warp whose groups all lie past the end skips the encode (its lanes
-    // agree: the bound is the warp's first group), so a short vector costs
-    // one encode per thread, not kQuantUnroll
-    if (g0 + u * kQuantThreads + (threadIdx.x & ~31u) >= groups) break;
+    // in the last, partial chunk a warp whose groups all lie past the end
+    // skips the encode (its lanes agree: the bound is the warp's first
+    // group), so a short vector costs one encode per thread, not kQuantUnroll
+    if (!full && g0 + u * kQuantThreads + (threadIdx.x & ~31u) >= groups) break;
     uint32_t lo, hi;
     uint16_t d16, s16;
     q8_1_encode_4lanes(v[u], lo, hi, d16, s16);

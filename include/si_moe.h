@@ -352,14 +352,17 @@ si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n_layers, in
  *   SI_STACK_PERSISTENT  one cooperative kernel, one block per SM, for the
  *                        whole stack ("perf(qwen3.6): fuse decode kernel
  *                        launches", Summary: decode is launch bound); returns
- *                        SI_ERR_UNSUPPORTED unless every layer has Q4_K routed
- *                        experts, a Q4_K, Q8_0 or no shared expert (one format
- *                        for all layers) and a bf16 router,
- *                        all layers share one shape with H a multiple of 2048
- *                        (<= 4096), E even (<= 256), top_k <= 8, n_layers <= 128,
- *                        and one block per SM covers every gate/up unit of 32
- *                        rows. Its workspace also carries the epoch of its
- *                        exchange tags, which advances with every replay.
+ *                        SI_ERR_UNSUPPORTED unless every layer has a bf16
+ *                        router and either Q4_K routed experts (gate, up and
+ *                        down) with a Q4_K, Q8_0 or no shared expert, or bf16
+ *                        routed experts with a bf16 or no shared expert (one
+ *                        format for all layers); all layers share one shape
+ *                        with H a multiple of 2048 (<= 4096), E even (<= 256),
+ *                        top_k <= 8, n_layers <= 128; one block per SM covers
+ *                        every gate/up unit of 32 rows; and the block's shared
+ *                        memory fits (bf16 down rows: J x top_k x inter x 2 B).
+ *                        Its workspace also carries the epoch of its exchange
+ *                        tags, which advances with every replay.
  * Both paths give bit-identical results. si_graph_is_persistent returns 1 for
  * a graph holding the persistent kernel, 0 for the per-layer path, -1 for NULL.
  */

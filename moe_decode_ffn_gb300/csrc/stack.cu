@@ -12,8 +12,9 @@
 //                       grid completion handshake of "perf(qwen3.6): fused
 //                       router GEMV+top-k + folded residual-norm (decode)"
 //                       (PR #273, Summary item 1) becomes one gather;
-//   X2 h codes        - each gate/up unit writes its 32 Q8_1 codes + scales;
-//                       every block with down rows gathers all of them;
+//   X2 h              - each gate/up unit writes its 32 Q8_1 codes + scales
+//                       (quantised layers) or its 32 fp32 values (bf16
+//                       layers); every block with down rows gathers them all;
 //   X3 output rows    - each block writes bf16(routed + shared) of its rows;
 //                       every block gathers all rows and folds the residual +
 //                       RMSNorm of the next layer itself (Summary item 2 of
@@ -22,8 +23,9 @@
 // 64-bit accesses, so a reader that sees the tag of this iteration also sees
 // its payload: one load both proves readiness and delivers the data (no
 // counter, flag or fence round trip). Every writer owns whole 128-byte slots
-// and fills its slot with one coalesced store: slots shared by several
-// writers, polled by every block, made those writes wait behind the polls. Tags are epoch + iteration + 1, the
+// and fills its slot with one coalesced store (twice: each copy has half
+// the readers): slots shared by several writers, polled by every block, made
+// those writes wait behind the polls. Tags are epoch + iteration + 1, the
 // epoch advancing by the iteration count at the end of every launch, so lines
 // left by an earlier launch never match. Lines are double-buffered by
 // iteration parity: a block writes buffer (i & 1) at iteration i only after it
@@ -33,8 +35,12 @@
 // Weights that do not depend on the routing are requested ahead, by warps
 // that are idle at that moment: the next layer's router rows, shared-gate
 // vector and norm weights and this layer's shared down rows while the logits
-// are gathered; the next shared-expert gate/up unit as soon as this one is
-// consumed. Only the routed experts' bytes wait for the selection.
+// are gathered; the next shared-expert gate/up unit (Q4_K, Q8_0) as soon as
+// its buffer is free. Only the routed experts' bytes wait for the selection.
+// Three layer kinds, one body (template arguments: routed and shared
+// formats): Q4_K routed experts with a Q4_K, Q8_0 or no shared expert, whose
+// 64-row gate/up unit fits shared memory whole, and bf16 layers, whose unit
+// (256 KB) passes through a ring of bulk copies.
 //
 // Per-thread index arithmetic is hoisted out of the loop; the per-row
 // arithmetic is the multi-kernel path's, so both give identical bits.
@@ -377,11 +383,11 @@ template <int EFMT, int SFMT>
 __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr bool kShared = SFMT != 0;
-  // bf16 experts (and shared expert): the gate/up rows stream from global
-  // memory into registers, two rows per warp in flight (a unit of 64 rows of
-  // H bf16 is larger than shared memory); h travels as fp32 (two slots per
-  // unit); the down rows of every selected expert are requested at the
-  // selection.
+  // bf16 experts (and shared expert): a unit of 64 rows of H bf16 is larger
+  // than shared memory, so its rows pass through a ring of kBfRing slots of 8
+  // rows (bulk copies, refilled as the groups are consumed); h travels as
+  // fp32 (two slots per unit); a unit block's routed down rows go to L2 half
+  // way through its gate/up rows and into the ring's space after them.
   constexpr bool kBf = EFMT == SI_BF16;
   constexpr int kSu = kBf ? 2 : 1;           // X2 slots per gate/up unit
   constexpr int kGq = kBf ? 5 : 2;           // X2 pairs gathered per thread

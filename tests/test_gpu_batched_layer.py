@@ -42,7 +42,8 @@ def _oracle_check(spec, seed, layer, x, res, out, t, where):
         assert ok, f"{where} {key}: {rep}"
 
 
-@pytest.mark.parametrize("T", [1, 4, 16, 64])
+# 128 tokens x top-8 = 1024 (token, expert) pairs: the most the grouping takes
+@pytest.mark.parametrize("T", [1, 4, 16, 64, 128])
 def test_batched_layer_equals_single_token_layers_and_the_oracle(T):
     dev = device_layer(SPEC, 500, 0)
     x = gen.make_tokens(501 + T, T).cuda()
@@ -125,6 +126,16 @@ def test_batched_48_layer_stack_at_64_tokens():
     g.close()
     del layers, steps
     torch.cuda.empty_cache()
+
+
+def test_batched_layer_refuses_more_pairs_than_the_grouping_takes():
+    """129 tokens x top-8 = 1032 pairs, above the 1024 the grouping holds:
+    refused on the host, nothing enqueued."""
+    dev = device_layer(SPEC, 500, 0)
+    x = gen.make_tokens(540, 129).cuda()
+    with pytest.raises(m.SiError) as e:
+        m.si_moe_layer_decode_batched(dev, x, ws=m.workspace(1 << 20))
+    assert e.value.status == m.SI_ERR_UNSUPPORTED
 
 
 def test_batched_layer_rejects_a_shared_expert():

@@ -180,3 +180,31 @@ def test_persistent_kernel_shapes_equal_the_per_layer_path(name):
     assert torch.equal(gp.y, gl.y) and torch.equal(gp.sum, gl.sum)
     gp.close()
     gl.close()
+
+
+def test_persistent_stack_at_its_layer_limit():
+    """128 layers (the most one persistent launch takes; its layer table sits
+    in shared memory) of a small layer shape x 2 tokens: the persistent
+    kernel equals four kernels per layer bit for bit; 129 layers are refused
+    by the persistent path and run per layer."""
+    spec = gen.LayerSpec(n_experts=64, top_k=4, inter=256, shared_inter=256, shared_type="q4_k")
+    layers = [device_layer(spec, 950, l) for l in range(128)]
+    x = gen.make_tokens(951, 2).cuda()
+    gp = m.StackGraph(layers, x, mode=m.SI_STACK_PERSISTENT)
+    gl = m.StackGraph(layers, x, mode=m.SI_STACK_PER_LAYER)
+    gp.launch()
+    gl.launch()
+    torch.cuda.synchronize()
+    assert gp.persistent and not gl.persistent
+    assert m.si_workspace_status(gp.ws) == m.SI_OK and m.si_workspace_status(gl.ws) == m.SI_OK
+    assert torch.equal(gp.ids, gl.ids)
+    assert torch.equal(gp.y, gl.y) and torch.equal(gp.sum, gl.sum)
+    gp.close()
+    gl.close()
+    more = layers + [device_layer(spec, 950, 128)]
+    with pytest.raises(m.SiError) as e:
+        m.StackGraph(more, x, mode=m.SI_STACK_PERSISTENT)
+    assert e.value.status == m.SI_ERR_UNSUPPORTED
+    g = m.StackGraph(more, x)
+    assert not g.persistent
+    g.close()

@@ -617,6 +617,17 @@ def run_configs(args):
              note="bytes = distinct experts' Q4_K weights + bf16 router, per layer",
              device_status=m.status_string(st))
         g.close()
+    # decode of the same 48-layer stack one token at a time on the persistent
+    # kernel (16 sequential tokens in one launch)
+    xs = gen.make_tokens(SEED + 800, 16, device=dev)
+    g = m.StackGraph(layers, xs, mode=m.SI_STACK_PERSISTENT)
+    us = _time_replays(lambda: g.launch(stream), stream, warm=3, reps=10) / (NL5 * 16)
+    st = m.si_workspace_status(g.ws, stream)
+    emit("5: 48-layer stack, 128 experts, I=768, T=1 (sequential tokens)",
+         "persistent kernel, one token at a time (16 tokens per launch)", us, "us/layer/token",
+         round(8 * Q4K_EXPERT_128E + 128 * 2048 * 2), path="persistent kernel",
+         device_status=m.status_string(st))
+    g.close()
     return 0
 
 

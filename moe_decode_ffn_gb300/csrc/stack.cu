@@ -68,9 +68,16 @@ constexpr int kGuGroups = 4;
 constexpr int kGuRows = 32 / kGuGroups;
 // mbarriers of a stack block: 0, 1 the routing-independent prefetch (router
 // rows, shared-gate vector, norm weights) by iteration parity; then one per
-// gate/up group of the block's unit; then the routed down rows; then the
-// shared down rows.
-enum { kBarPre = 0, kBarGu = 2, kBarDn = 2 + kGuGroups, kBarSd = 3 + kGuGroups, kNumBars = 4 + kGuGroups };
+// gate/up group of the block's unit, and of its second unit (layers with
+// more units than SMs); then the routed down rows; then the shared down rows.
+enum {
+  kBarPre = 0,
+  kBarGu = 2,
+  kBarGu2 = 2 + kGuGroups,
+  kBarDn = 2 + 2 * kGuGroups,
+  kBarSd = 3 + 2 * kGuGroups,
+  kNumBars = 4 + 2 * kGuGroups
+};
 
 struct StackLayerPtrs {             // 80 bytes
   const __nv_bfloat16 *w_router, *w_sg, *w_norm;
@@ -404,8 +411,12 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   const int nsb_r = I / kQKK, nsb_s = Is / kQKK;
   // down pieces of a row: Q4_K halves of 128 weights, Q8_0 whole 256-weight
   // groups (a Q8_0 half would start off a 16-byte boundary)
-  const int P_r = 2 * nsb_r, P_s = kShared ? (kShQ80 ? nsb_s : 2 * nsb_s) : 1,
-            P_max = P_r > P_s ? P_r : P_s;
+  const int P_r = 2 * nsb_r, P_s = kShared ? (kShQ80 ? nsb_s : 2 * nsb_s) : 1;
+  // the pieces of a row take a power-of-two group of lanes (6 pieces: 8
+  // lanes, two of them idle), so a group never straddles two warps
+  const int P_rp = P_r <= 2 ? P_r : (P_r <= 4 ? 4 : (P_r <= 8 ? 8 : (P_r <= 16 ? 16 : 32)));
+  const int P_sp = P_s <= 2 ? P_s : (P_s <= 4 ? 4 : (P_s <= 8 ? 8 : (P_s <= 16 ? 16 : 32)));
+  const int P_max = P_rp > P_sp ? P_rp : P_sp;
   const int n_iters = p.n_tokens * p.n_layers;
   const int J = p.J;
   const int nvec = H / 2048;   // router: 16-byte vectors of a row per thread of the first 256
@@ -423,8 +434,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   float *s_wts = reinterpret_cast<float *>(smem + 320);    // [8]
   uint64_t *s_sel = reinterpret_cast<uint64_t *>(smem + 384);
   uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + 448);   // [64]
-  float *h_s = reinterpret_cast<float *>(smem + 960);      // [32]
-  float *s_gu = reinterpret_cast<float *>(smem + 1088);    // [64] bf16 gate/up row dots
+  float *h_s = reinterpret_cast<float *>(smem + 960);      // [2][32] h of the block's units
+  float *s_gu = reinterpret_cast<float *>(smem + 1216);    // [64] bf16 gate/up row dots
   StackLayerPtrs *s_layers = reinterpret_cast<StackLayerPtrs *>(smem + p.sm.layers);
   float *resid = reinterpret_cast<float *>(smem + p.sm.resid);
   float *y = reinterpret_cast<float *>(smem + p.sm.y);
@@ -445,7 +456,12 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   // ---- static assignment ----------------------------------------------------
   const int my_unit = c < units ? c : -1;
   const bool shared_unit = kShared && my_unit >= units_r;
-  const int dn_off = static_cast<int>((kShQ80 && shared_unit) ? p.sm.gu : p.sm.dn);
+  // more units than blocks (quantised layers without a shared expert only):
+  // block c also takes unit c + G; its routed down rows then arrive, after
+  // its gate/up dot products, in the space of its units' rows
+  const int my_unit2 = (!kShared && !kBf && c + G < units) ? c + G : -1;
+  const int dn_off = static_cast<int>(((kShQ80 && shared_unit) || my_unit2 >= 0) ? p.sm.gu : p.sm.dn);
+  uint8_t *gu_buf2 = gu_buf + 64 * p.rb;   // the second unit's gate [32] + up [32] rows
   uint8_t *dn_buf = smem + dn_off;    // [k][J] routed down rows
   const int rb_unit = shared_unit ? p.rbs : p.rb;   // row bytes of this block's gate/up unit
   const int j0 = c * J;
@@ -484,27 +500,27 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   // first of them (qq == 0) sums them in order
   int d_row[2], d_act[2], d_blk[2], d_h[2], d_dst[2], d_P[2];
   bool d_live[2], d_first[2], d_q80[2];
-  const int items_r = k * J * P_r;
-  const int items = items_r + (kShared ? J * P_s : 0);
+  const int items_r = k * J * P_rp;
+  const int items = items_r + (kShared ? J * P_sp : 0);
   if constexpr (!kBf) {
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int u = static_cast<int>(threadIdx.x) + s * kStkThreads;
       int r, jl, qq;
       if (u < items_r) {
-        r = u / (J * P_r);
-        const int rem = u - r * (J * P_r);
-        jl = rem / P_r;
-        qq = rem - jl * P_r;
+        r = u / (J * P_rp);
+        const int rem = u - r * (J * P_rp);
+        jl = rem / P_rp;
+        qq = rem - jl * P_rp;
       } else {
         r = k;
-        jl = (u - items_r) / P_s;
-        qq = (u - items_r) - jl * P_s;
+        jl = (u - items_r) / P_sp;
+        qq = (u - items_r) - jl * P_sp;
       }
       const bool sh = kShared && r == k;
       d_q80[s] = kShQ80 && sh;
       const int sb = d_q80[s] ? qq : qq >> 1;
-      d_live[s] = u < items && jl < nrows;
+      d_live[s] = u < items && jl < nrows && qq < (sh ? P_s : P_r);
       d_first[s] = qq == 0;
       d_P[s] = sh ? P_s : P_r;
       d_dst[s] = r * J + jl;
@@ -707,6 +723,9 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
           if (!kBf && my_unit >= 0 && !shared_unit)
 #pragma unroll 1
             for (int g = 0; g < kGuGroups; ++g) arm(bars, s_arm, kBarGu + g, 2 * cbytes);
+          if (my_unit2 >= 0)
+#pragma unroll 1
+            for (int g = 0; g < kGuGroups; ++g) arm(bars, s_arm, kBarGu2 + g, 2 * cbytes);
           if (nrows > 0) arm(bars, s_arm, kBarDn, static_cast<uint32_t>(k * nrows * p.rbd));
         }
         const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];
@@ -758,6 +777,16 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         const size_t row0 = static_cast<size_t>(e) * I + static_cast<size_t>(hb) * 32 + kGuRows * g;
         bulk_g2s_evict_first(gu_buf + ((up ? 32 : 0) + kGuRows * g) * p.rb, (up ? Lp.wu : Lp.wg) + row0 * p.rb,
                              cbytes, &bars[kBarGu + g], pol);
+      }
+      if (warp >= 8 && warp < 8 + 2 * kGuGroups && my_unit2 >= 0) {   // the second unit, warps 8..15
+        const int slot = my_unit2 / (I / 32), hb = my_unit2 - slot * (I / 32);
+        int e = key_index(s_sel[slot]);
+        if (e < 0 || e >= E) e = 0;
+        const int g = (warp - 8) % kGuGroups;
+        const bool up = warp - 8 >= kGuGroups;
+        const size_t row0 = static_cast<size_t>(e) * I + static_cast<size_t>(hb) * 32 + kGuRows * g;
+        bulk_g2s_evict_first(gu_buf2 + ((up ? 32 : 0) + kGuRows * g) * p.rb, (up ? Lp.wu : Lp.wg) + row0 * p.rb,
+                             cbytes, &bars[kBarGu2 + g], pol);
       }
       if (warp >= 8 && warp < 8 + k && nrows > 0 && (kBf || my_unit < 0)) {
         int e = key_index(s_sel[warp - 8]);
@@ -881,7 +910,24 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
       const float other = __shfl_xor_sync(0xffffffffu, acc, 8);
       if ((threadIdx.x & 15) == 0) h_s[pr] = __fdiv_rn(acc, 1.f + expf(-acc)) * other;
-      if (__syncthreads_or(!ok)) goto fail;
+      bool ok2 = true;
+      if (my_unit2 >= 0) {   // block-uniform: the second unit, the same rows of it
+        float acc2 = 0.f;
+        ok2 = mbar_wait_bounded(&bars[kBarGu2 + pr / kGuRows], par, p.status);
+        if (ok2) {
+          const uint8_t *row = gu_buf2 + (gm * 32 + pr) * p.rb;
+          for (int sb = lane8; sb < nsb; sb += 8)
+            acc2 += q4k_sb_dot(reinterpret_cast<const uint4 *>(row + sb * kQ4KBytes),
+                               reinterpret_cast<const uint4 *>(xt.qs + sb * kActSbStride), xt.d + 8 * sb,
+                               xt.s + 8 * sb);
+        }
+        acc2 += __shfl_xor_sync(0xffffffffu, acc2, 1);
+        acc2 += __shfl_xor_sync(0xffffffffu, acc2, 2);
+        acc2 += __shfl_xor_sync(0xffffffffu, acc2, 4);
+        const float other2 = __shfl_xor_sync(0xffffffffu, acc2, 8);
+        if ((threadIdx.x & 15) == 0) h_s[32 + pr] = __fdiv_rn(acc2, 1.f + expf(-acc2)) * other2;
+      }
+      if (__syncthreads_or(!(ok && ok2))) goto fail;
       STK_TRACE(7);
       // every wait on this iteration's gate/up phases is over
       if (lane == 0 && warp >= 8 && warp < 8 + k && nrows > 0) {
@@ -906,9 +952,10 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
         bulk_g2s_evict_first(gu_buf + (32 + kGuRows * g) * p.rbs, Ln.wsu + row0 * p.rbs, cbytes_s,
                              &bars[kBarGu + g], pol);
       }
-      if (warp == 0) {
+      if (warp == 0 || (warp == 1 && my_unit2 >= 0)) {   // warp u: unit u's h
+        const int un = warp == 0 ? my_unit : my_unit2;
         uint16_t d16, s16;
-        const uint32_t q = static_cast<uint32_t>(q8_1_encode_warp(h_s[lane], d16, s16)) & 0xFFu;
+        const uint32_t q = static_cast<uint32_t>(q8_1_encode_warp(h_s[32 * warp + lane], d16, s16)) & 0xFFu;
         const uint32_t w = q | (__shfl_down_sync(0xffffffffu, q, 1) << 8) |
                            (__shfl_down_sync(0xffffffffu, q, 2) << 16) |
                            (__shfl_down_sync(0xffffffffu, q, 3) << 24);   // lane 4j: code word j
@@ -919,7 +966,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
           const int i = i0 + lane, r = i / 5, j = i - 5 * r;
           const uint32_t wa = __shfl_sync(0xffffffffu, w, (8 * j) & 31);
           const uint32_t wb = __shfl_sync(0xffffffffu, w, (8 * j + 4) & 31);
-          uint64_t *line = p.hl + ((static_cast<size_t>(par) * kXRep + r) * units + my_unit) * kSlot;
+          uint64_t *line = p.hl + ((static_cast<size_t>(par) * kXRep + r) * units + un) * kSlot;
           if (i < 5 * kXRep) {
             if (j < 4)
               st_tag2(line + 2 * j, tagged(tag, wa), tagged(tag, wb));
@@ -1179,10 +1226,16 @@ static int shared_row_bytes(const si_moe_layer &L, int width) {
   return L.shared_type == SI_Q8_0 ? width / 32 * kQ80Bytes : width / 256 * kQ4KBytes;
 }
 
-// Pieces of one routed / shared down row (the down step's work items).
+// Pieces of one routed / shared down row (the down step's work items), and
+// the power-of-two lane groups they take.
 static int down_pieces_routed(const si_moe_layer &L) { return 2 * L.inter / 256; }
 static int down_pieces_shared(const si_moe_layer &L) {
   return L.shared_type == SI_Q8_0 ? L.shared_inter / 256 : 2 * L.shared_inter / 256;
+}
+static int lane_group(int pieces) {
+  int g = 1;
+  while (g < pieces) g *= 2;
+  return g;
 }
 
 // bf16 layers: no Q8_1 tiles; y as packed bf16 (in the place of the x
@@ -1228,10 +1281,12 @@ static StackSmem stack_smem(const si_moe_layer &L, int J, int n_layers) {
   const bool q80 = sh && L.shared_type == SI_Q8_0;
   const int H = L.hidden, k = L.top_k, nsb = H / 256;
   const int nq = k * L.inter + L.shared_inter, n_slots = k + (sh ? 1 : 0);
-  const int P_r = down_pieces_routed(L), P_s = sh ? down_pieces_shared(L) : 0;
+  const int P_r = lane_group(down_pieces_routed(L)), P_s = sh ? lane_group(down_pieces_shared(L)) : 0;
   const int P_max = P_r > P_s ? P_r : P_s;
   const int rb = H / 256 * kQ4KBytes, rbd = L.inter / 256 * kQ4KBytes,
             rbsd = sh ? shared_row_bytes(L, L.shared_inter) : 0;
+  const int sms = device_sms();
+  const bool two_units = !sh && sms > 0 && k * L.inter / 32 > sms;
   size_t off = kStkFixedBytes;
   auto take = [&](uint32_t &field, size_t bytes, size_t align) {
     off = round_up(off, align);
@@ -1257,6 +1312,13 @@ static StackSmem stack_smem(const si_moe_layer &L, int J, int n_layers) {
     const size_t routed = 64u * rb + static_cast<size_t>(J) * k * rbd;
     const size_t shared = 64u * static_cast<size_t>(shared_row_bytes(L, H));
     take(s.gu, routed > shared ? routed : shared, 128);
+    s.dn = s.gu + 64u * rb;
+  } else if (two_units) {
+    // one region: two units (a block with a second unit takes its routed
+    // down rows into this space after its dot products), or one unit and
+    // the routed down rows
+    const size_t one = 64u * rb + static_cast<size_t>(J) * k * rbd, two = 128u * rb;
+    take(s.gu, one > two ? one : two, 128);
     s.dn = s.gu + 64u * rb;
   } else {
     take(s.gu, 64u * rb, 128);
@@ -1317,14 +1379,16 @@ bool stack_supported(const si_moe_layer *layers, int n_layers) {
   if (sms <= 0) return false;
   const StackGeom g = stack_geom(L, n_layers, sms);
   const int n_slots = L.top_k + (L.shared_inter > 0 ? 1 : 0);
-  const int P_r = down_pieces_routed(L), P_s = L.shared_inter > 0 ? down_pieces_shared(L) : 0;
+  const int P_r = lane_group(down_pieces_routed(L));
+  const int P_s = L.shared_inter > 0 ? lane_group(down_pieces_shared(L)) : 0;
   const int P_max = P_r > P_s ? P_r : P_s;
-  if (sms < g.units || g.units * 5 > 2 * kStkThreads || g.J > 32 || sms * g.np3 > 2 * kStkThreads ||
+  // a second gate/up unit per block only without a shared expert
+  if ((L.shared_inter > 0 ? sms : 2 * sms) < g.units || g.units * 5 > 2 * kStkThreads || g.J > 32 || sms * g.np3 > 2 * kStkThreads ||
       n_slots * g.J * P_max > 2 * kStkThreads || n_slots * g.J > kStkThreads)
     return false;
-  // the pieces of a (slot, row) of the down step are summed across lanes of
-  // one warp: the piece counts must divide 32, and the shared slot's pieces
-  // must start on a multiple of their count
+  // the pieces of a (slot, row) of the down step are summed across a
+  // power-of-two group of lanes of one warp: the groups must divide 32, and
+  // the shared slot's groups must start on a multiple of their size
   if (32 % P_r || (L.shared_inter > 0 && (32 % P_s || (L.top_k * g.J * P_r) % P_s))) return false;
   if ((L.n_experts > 128 ? 2 * sms : sms) < L.n_experts) return false;
   if (sms > kStkThreads) return false;

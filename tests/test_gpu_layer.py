@@ -154,6 +154,8 @@ PERSISTENT_SHAPES = {
     "e128_shared_q8_0": gen.LayerSpec(n_experts=128, shared_type="q8_0"),
     "i256_shared_q8_0_is1024": gen.LayerSpec(inter=256, shared_inter=1024, shared_type="q8_0"),
     "bf16_no_shared": gen.LayerSpec(expert_type="bf16", shared_inter=0, shared_type="bf16"),
+    # 192 gate/up units on 152 SMs (40 blocks take two), 6 down pieces per row
+    "e128_i768_no_shared": gen.Q4K_LAYER_128E,
     "bf16_e128_top4_i768": gen.LayerSpec(expert_type="bf16", n_experts=128, top_k=4, inter=768,
                                          shared_type="bf16"),
     "bf16_e64_top2_i256": gen.LayerSpec(expert_type="bf16", n_experts=64, top_k=2, inter=256,

@@ -615,6 +615,8 @@ def run_configs(args):
              "batched layer stack (router + grouped experts + norm per layer), one graph", us,
              "us/layer", nbytes, distinct_experts=U, us_per_layer_token=round(us / T, 3),
              note="bytes = distinct experts' Q4_K weights + bf16 router, per layer",
+             path="persistent kernel" if g.persistent else "batched kernels (router, prep, gate/up, "
+                                                           "down, combine, norm)",
              device_status=m.status_string(st))
         g.close()
     # decode of the same 48-layer stack one token at a time on the persistent

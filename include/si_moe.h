@@ -407,6 +407,9 @@ si_status si_moe_layer_decode_batched(const si_moe_layer *L, int n_tokens, int m
  *   ids_out device int32 [n_layers][T][k] or NULL
  *   workspace si_moe_stack_batched_workspace_bytes(layers, n_layers, T) bytes, zeroed once
  * The graph captures the pointers; `stream` is used for capture only.
+ * With one token and mode SI_FFN_AUTO the graph holds the persistent stack
+ * kernel when it takes the layers (si_graph_is_persistent returns 1): the
+ * same bits, one launch for the whole stack.
  */
 size_t si_moe_stack_batched_workspace_bytes(const si_moe_layer *layers, int n_layers, int n_tokens);
 si_status si_moe_stack_graph_create_batched(const si_moe_layer *layers, int n_layers, int n_tokens,

@@ -490,6 +490,8 @@ class BatchedStackGraph:
             _cuda(self.sum, "sum"), _opt(self.ids, "ids"), _cuda(self.ws, "ws"), self.ws.numel(),
             _stream(cap), ctypes.byref(h)), "si_moe_stack_graph_create_batched")
         self.handle = h
+        # one token in the automatic mode: the persistent stack kernel when it takes the layers
+        self.persistent = bool(library().si_graph_is_persistent(h))
 
     def launch(self, stream=None):
         _check(library().si_graph_launch(self.handle, _stream(stream)), "si_graph_launch")

@@ -233,9 +233,14 @@ extern "C" si_status si_moe_stack_graph_create_mode(const si_moe_layer *layers, 
   if (!aligned16(x_in) || !aligned16(y_out) || (sum_out && !aligned16(sum_out)) ||
       (ids_out && (reinterpret_cast<uintptr_t>(ids_out) & 3u)))
     return SI_ERR_INVALID_ARG;
-  if (!workspace || !aligned256(workspace) ||
-      workspace_bytes < si_moe_stack_workspace_bytes(layers, n_layers))
-    return SI_ERR_WORKSPACE;
+  // The persistent kernel serves the layers stack_supported takes; the others
+  // run as four kernels per layer. A forced persistent graph needs only the
+  // persistent kernel's workspace.
+  const bool can_persist = stack_supported(layers, n_layers);
+  if (mode == SI_STACK_PERSISTENT && !can_persist) return SI_ERR_UNSUPPORTED;
+  const size_t need = mode == SI_STACK_PERSISTENT ? stack_workspace_bytes(layers, n_layers)
+                                                  : si_moe_stack_workspace_bytes(layers, n_layers);
+  if (!workspace || !aligned256(workspace) || workspace_bytes < need) return SI_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (preload_router() != cudaSuccess || preload_ffn() != cudaSuccess ||
       preload_norm() != cudaSuccess || preload_stack() != cudaSuccess)
@@ -243,10 +248,6 @@ extern "C" si_status si_moe_stack_graph_create_mode(const si_moe_layer *layers, 
   cudaStreamCaptureStatus cs;
   if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return SI_ERR_CUDA;
   if (cs != cudaStreamCaptureStatusNone) return SI_ERR_INVALID_ARG;
-  // The persistent kernel serves stacks of Q4_K layers; other layer types run
-  // as four kernels per layer.
-  const bool can_persist = stack_supported(layers, n_layers);
-  if (mode == SI_STACK_PERSISTENT && !can_persist) return SI_ERR_UNSUPPORTED;
   const bool persistent = can_persist && mode != SI_STACK_PER_LAYER;
   if (persistent) {
     const si_status sp = stack_prepare(layers, n_layers, workspace, s);
@@ -406,6 +407,10 @@ extern "C" size_t si_moe_stack_batched_workspace_bytes(const si_moe_layer *layer
     if (blayer_check(layers[l], n_tokens) != SI_OK) return 0;
     off += bstack_layer_bytes(layers[l], n_tokens);
   }
+  if (n_tokens == 1 && stack_supported(layers, n_layers)) {   // the automatic mode's persistent kernel
+    const size_t pk = stack_workspace_bytes(layers, n_layers);
+    if (pk > off) off = pk;
+  }
   return off;
 }
 
@@ -429,6 +434,12 @@ extern "C" si_status si_moe_stack_graph_create_batched(const si_moe_layer *layer
   if (!workspace || !aligned256(workspace) ||
       workspace_bytes < si_moe_stack_batched_workspace_bytes(layers, n_layers, n_tokens))
     return SI_ERR_WORKSPACE;
+  // one token: the same results (every path gives every token the bits of
+  // the single-token layer) from the persistent kernel when it takes the
+  // layers; the ids layout [n_layers][1][k] is the persistent one's [1][n_layers][k]
+  if (mode == SI_FFN_AUTO && n_tokens == 1 && stack_supported(layers, n_layers))
+    return si_moe_stack_graph_create_mode(layers, n_layers, 1, x_in, y_out, sum_out, ids_out, workspace,
+                                          workspace_bytes, SI_STACK_PERSISTENT, stream, graph_out);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (preload_router() != cudaSuccess || preload_batched() != cudaSuccess || preload_norm() != cudaSuccess)
     return SI_ERR_CUDA;

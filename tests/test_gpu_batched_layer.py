@@ -128,6 +128,26 @@ def test_batched_48_layer_stack_at_64_tokens():
     torch.cuda.empty_cache()
 
 
+def test_batched_stack_of_one_token_runs_on_the_persistent_kernel():
+    """One token, automatic mode: the graph holds the persistent stack kernel
+    (the layer has 192 gate/up units on 152 SMs) and gives the bits of the
+    batched integer path, layer ids included."""
+    layers = [device_layer(SPEC, 560, l) for l in range(6)]
+    x = gen.make_tokens(561, 1).cuda()
+    ga = m.BatchedStackGraph(layers, x)
+    gi = m.BatchedStackGraph(layers, x, mode=m.SI_FFN_INT8)
+    assert ga.persistent and not gi.persistent
+    for _ in range(2):
+        ga.launch()
+    gi.launch()
+    torch.cuda.synchronize()
+    assert m.si_workspace_status(ga.ws) == m.SI_OK and m.si_workspace_status(gi.ws) == m.SI_OK
+    assert torch.equal(ga.ids, gi.ids)
+    assert torch.equal(ga.y, gi.y) and torch.equal(ga.sum, gi.sum)
+    ga.close()
+    gi.close()
+
+
 def test_batched_layer_refuses_more_pairs_than_the_grouping_takes():
     """129 tokens x top-8 = 1032 pairs, above the 1024 the grouping holds:
     refused on the host, nothing enqueued."""

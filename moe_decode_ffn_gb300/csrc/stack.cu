@@ -872,6 +872,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
                                s_layers[l].wd + (static_cast<size_t>(e) * H + j0) * p.rbd,
                                static_cast<uint32_t>(nrows) * p.rbd, &bars[kBarDn], pol);
         }
+        // the next layer's shared unit into L2 while DRAM is quiet (it does
+        // not depend on the routing): lane 1 of warps 8..15, an eighth each
+        if (shared_unit && it + 1 < n_iters && lane == 1 && warp >= 8) {
+          const StackLayerPtrs &Ln = s_layers[l + 1 == p.n_layers ? 0 : l + 1];
+          const int q = warp - 8;   // 0..3 gate rows, 4..7 up rows, 8 rows each
+          const size_t row0 = static_cast<size_t>(my_unit - units_r) * 32 + 8 * (q & 3);
+          bulk_prefetch_l2((q < 4 ? Ln.wsg : Ln.wsu) + row0 * p.rb, 8u * p.rb);
+        }
         __syncwarp();
         STK_TRACE(7);
         if (warp == 0) {

@@ -459,7 +459,7 @@ SI_DEV void q4k_half_dot_rows_tokens(const uint8_t *const w[R], const uint8_t *h
 // row (so its lanes read the same activation codes) and lane l the rows l,
 // l + 32, ...; then each (pair, row) sums its pieces in order.
 template <int R>
-__global__ void __launch_bounds__(kDownBThreads) down_grouped_kernel(BatchedParams p) {
+__global__ void __launch_bounds__(kDownBThreads, 3) down_grouped_kernel(BatchedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int kRows = 32 * R;
   const int tiles = p.H / kRows;

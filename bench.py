@@ -511,7 +511,8 @@ def run_configs(args):
                                gen.NATIVE_LAYER_Q5K_DOWN, BYTES_NATIVE)):
         layers = [m.device_layer(spec, SEED + 100, l, device=dev) for l in range(NL)]
         modes = [m.SI_STACK_AUTO]
-        if spec in (gen.Q4K_LAYER_SHARED_Q4_K, gen.Q4K_LAYER_SHARED_Q8_0, gen.BF16_LAYER):
+        if spec in (gen.Q4K_LAYER_SHARED_Q4_K, gen.Q4K_LAYER_SHARED_Q8_0, gen.BF16_LAYER,
+                    gen.NATIVE_LAYER_Q5K_DOWN):
             modes = [m.SI_STACK_PERSISTENT, m.SI_STACK_PER_LAYER]
         for mode in modes:
             g = m.StackGraph(layers, x, mode=mode)

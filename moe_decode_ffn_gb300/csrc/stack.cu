@@ -386,7 +386,7 @@ static __device__ int g_stk_trace_phase;
   } while (0)
 #endif
 
-template <int EFMT, int SFMT>
+template <int EFMT, int SFMT, int DFMT = SI_Q4_K>
 __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr bool kShared = SFMT != 0;
@@ -404,6 +404,9 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   // the unit's dot products are done; the next unit is requested once the
   // down rows are consumed.
   constexpr bool kShQ80 = SFMT == SI_Q8_0;
+  // routed down rows in Q5_K (the shipped format: 176-byte super-blocks,
+  // the same half-super-block pieces)
+  constexpr bool kDnQ5 = DFMT == SI_Q5_K;
   const int G = gridDim.x, c = blockIdx.x;
   const int H = p.H, I = p.I, Is = kShared ? p.Is : 0, k = p.k, E = p.E;
   const int nsb = H / kQKK;
@@ -499,7 +502,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
   // the P pieces of a (slot, row) lie in consecutive lanes of one warp, the
   // first of them (qq == 0) sums them in order
   int d_row[2], d_act[2], d_blk[2], d_h[2], d_dst[2], d_P[2];
-  bool d_live[2], d_first[2], d_q80[2];
+  bool d_live[2], d_first[2], d_q80[2], d_q5[2];
   const int items_r = k * J * P_rp;
   const int items = items_r + (kShared ? J * P_sp : 0);
   if constexpr (!kBf) {
@@ -519,13 +522,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       }
       const bool sh = kShared && r == k;
       d_q80[s] = kShQ80 && sh;
+      d_q5[s] = kDnQ5 && !sh;
       const int sb = d_q80[s] ? qq : qq >> 1;
       d_live[s] = u < items && jl < nrows && qq < (sh ? P_s : P_r);
       d_first[s] = qq == 0;
       d_P[s] = sh ? P_s : P_r;
       d_dst[s] = r * J + jl;
       d_row[s] = (sh ? static_cast<int>(p.sm.sd) + jl * p.rbsd : dn_off + (r * J + jl) * p.rbd) +
-                 sb * (d_q80[s] ? 8 * kQ80Bytes : kQ4KBytes);
+                 sb * (d_q80[s] ? 8 * kQ80Bytes : (d_q5[s] ? kQ5KBytes : kQ4KBytes));
       d_act[s] = static_cast<int>(p.sm.ht_qs) + (r * nsb_r + sb) * kActSbStride;
       d_blk[s] = (r * I) / 32 + 8 * sb;
       d_h[s] = qq & 1;
@@ -1009,7 +1013,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
       if (kShared) okw &= mbar_wait_bounded(&bars[kBarSd], par, p.status);
       Q4KHalf wq;
       if constexpr (!kBf)
-        if (okw && d_live[0] && !d_q80[0])
+        if (okw && d_live[0] && !d_q80[0] && !d_q5[0])
           q4k_half_load(reinterpret_cast<const uint4 *>(smem + d_row[0]), d_h[0], wq);
 #pragma unroll
       for (int s = 0; s < kGq; ++s) {
@@ -1098,6 +1102,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) stack_kernel(StackParams p) {
             const uint4 *a = reinterpret_cast<const uint4 *>(smem + d_act[s]);
             if (kShQ80 && d_q80[s])
               v = q80_sb_dot(reinterpret_cast<const uint4 *>(smem + d_row[s]), a, ht.d + d_blk[s]);
+            else if (kDnQ5 && d_q5[s])
+              v = q5k_half_dot(smem + d_row[s], a, ht.d + d_blk[s], ht.s + d_blk[s], d_h[s]);
             else
               v = s == 0 ? q4k_half_dot_loaded(wq, a, ht.d + d_blk[s], ht.s + d_blk[s], d_h[s])
                          : q4k_half_dot(reinterpret_cast<const uint4 *>(smem + d_row[s]), a, ht.d + d_blk[s],
@@ -1291,7 +1297,7 @@ static StackSmem stack_smem(const si_moe_layer &L, int J, int n_layers) {
   const int nq = k * L.inter + L.shared_inter, n_slots = k + (sh ? 1 : 0);
   const int P_r = lane_group(down_pieces_routed(L)), P_s = sh ? lane_group(down_pieces_shared(L)) : 0;
   const int P_max = P_r > P_s ? P_r : P_s;
-  const int rb = H / 256 * kQ4KBytes, rbd = L.inter / 256 * kQ4KBytes,
+  const int rb = H / 256 * kQ4KBytes, rbd = L.inter / 256 * (down_type_of(L) == SI_Q5_K ? kQ5KBytes : kQ4KBytes),
             rbsd = sh ? shared_row_bytes(L, L.shared_inter) : 0;
   const int sms = device_sms();
   const bool two_units = !sh && sms > 0 && k * L.inter / 32 > sms;
@@ -1374,7 +1380,7 @@ bool stack_supported(const si_moe_layer *layers, int n_layers) {
     const si_moe_layer &M = layers[l];
     if (M.hidden != L.hidden || M.n_experts != L.n_experts || M.top_k != L.top_k ||
         M.inter != L.inter || M.shared_inter != L.shared_inter || M.expert_type != SI_Q4_K ||
-        down_type_of(M) != SI_Q4_K ||
+        (down_type_of(M) != SI_Q4_K && down_type_of(M) != SI_Q5_K) || down_type_of(M) != down_type_of(L) ||
         M.router_type != SI_BF16 ||
         (M.shared_inter > 0 && M.shared_type != SI_Q4_K && M.shared_type != SI_Q8_0) ||
         (M.shared_inter > 0 && M.shared_type != L.shared_type) || M.eps != L.eps)
@@ -1413,6 +1419,9 @@ cudaError_t preload_stack() {
   cudaError_t e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, 0>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, SI_Q4_K>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, SI_Q8_0>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, 0, SI_Q5_K>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, SI_Q4_K, SI_Q5_K>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_Q4_K, SI_Q8_0, SI_Q5_K>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_BF16, 0>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, stack_kernel<SI_BF16, SI_BF16>);
   return e;
@@ -1458,7 +1467,8 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   const bool bf = L.expert_type == SI_BF16;
   p.rb = bf ? L.hidden * 2 : L.hidden / 256 * kQ4KBytes;
   p.rbs = L.shared_inter > 0 && !bf ? shared_row_bytes(L, L.hidden) : p.rb;
-  p.rbd = bf ? L.inter * 2 : L.inter / 256 * kQ4KBytes;
+  const bool q5 = !bf && down_type_of(L) == SI_Q5_K;
+  p.rbd = bf ? L.inter * 2 : L.inter / 256 * (q5 ? kQ5KBytes : kQ4KBytes);
   p.rbsd = L.shared_inter > 0 ? (bf ? L.shared_inter * 2 : shared_row_bytes(L, L.shared_inter)) : 0;
   p.J = g.J;
   p.np3 = g.np3;
@@ -1476,6 +1486,9 @@ si_status stack_launch(const si_moe_layer *layers, int n_layers, int n_tokens, c
   const size_t smem = p.sm.bytes;
   if (smem > 227 * 1024) return SI_ERR_UNSUPPORTED;
   auto kern = bf ? (L.shared_inter == 0 ? stack_kernel<SI_BF16, 0> : stack_kernel<SI_BF16, SI_BF16>)
+              : q5 ? (L.shared_inter == 0      ? stack_kernel<SI_Q4_K, 0, SI_Q5_K>
+                      : L.shared_type == SI_Q8_0 ? stack_kernel<SI_Q4_K, SI_Q8_0, SI_Q5_K>
+                                                 : stack_kernel<SI_Q4_K, SI_Q4_K, SI_Q5_K>)
               : L.shared_inter == 0      ? stack_kernel<SI_Q4_K, 0>
               : L.shared_type == SI_Q8_0 ? stack_kernel<SI_Q4_K, SI_Q8_0>
                                          : stack_kernel<SI_Q4_K, SI_Q4_K>;

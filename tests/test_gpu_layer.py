@@ -124,7 +124,8 @@ def test_stack_graph_equals_eager_layers_and_replays_bit_exact(name):
 def test_stack_paths_agree_bit_exact_and_report_their_kind(name):
     """The same stack through the persistent kernel and through four kernels
     per layer: identical bits; a stack the persistent kernel does not serve
-    (Q5_K routed down rows) is refused when that path is forced."""
+    (H = 4096 on 152 SMs: 28 output rows per block) is refused when that
+    path is forced."""
     spec = SPECS[name]
     layers = _stack_layers(spec, 3, seed=310)
     x = gen.make_tokens(910, 2).cuda()
@@ -139,11 +140,14 @@ def test_stack_paths_agree_bit_exact_and_report_their_kind(name):
     for g in (gp, gl, ga):
         assert m.si_workspace_status(g.ws) == m.SI_OK
         g.close()
-    q5 = _stack_layers(gen.NATIVE_LAYER_Q5K_DOWN, 2, seed=311)
+    wide = _stack_layers(gen.LayerSpec(hidden=4096, n_experts=64, top_k=2, inter=256, shared_inter=256,
+                                       shared_type="q4_k"), 2, seed=311)
+    xw = gen.make_tokens(912, 2).cuda()
+    xw = torch.cat([xw, xw], dim=1).contiguous()   # bf16 [2, 4096]
     with pytest.raises(m.SiError) as e:
-        m.StackGraph(q5, x, mode=m.SI_STACK_PERSISTENT)
+        m.StackGraph(wide, xw, mode=m.SI_STACK_PERSISTENT)
     assert e.value.status == m.SI_ERR_UNSUPPORTED
-    assert not m.StackGraph(q5, x).persistent
+    assert not m.StackGraph(wide, xw).persistent
 
 
 PERSISTENT_SHAPES = {
@@ -156,6 +160,9 @@ PERSISTENT_SHAPES = {
     "bf16_no_shared": gen.LayerSpec(expert_type="bf16", shared_inter=0, shared_type="bf16"),
     # 192 gate/up units on 152 SMs (40 blocks take two), 6 down pieces per row
     "e128_i768_no_shared": gen.Q4K_LAYER_128E,
+    # the shipped formats: Q5_K routed down rows (Q8_0 or Q4_K shared expert)
+    "native_q5k_down_q8_0_shared": gen.NATIVE_LAYER_Q5K_DOWN,
+    "q5k_down_q4k_shared": gen.LayerSpec(down_type="q5_k", shared_type="q4_k"),
     "bf16_e128_top4_i768": gen.LayerSpec(expert_type="bf16", n_experts=128, top_k=4, inter=768,
                                          shared_type="bf16"),
     "bf16_e64_top2_i256": gen.LayerSpec(expert_type="bf16", n_experts=64, top_k=2, inter=256,

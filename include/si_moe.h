@@ -353,8 +353,9 @@ si_status si_moe_stack_graph_create(const si_moe_layer *layers, int n_layers, in
  *                        whole stack ("perf(qwen3.6): fuse decode kernel
  *                        launches", Summary: decode is launch bound); returns
  *                        SI_ERR_UNSUPPORTED unless every layer has a bf16
- *                        router and either Q4_K routed experts (gate, up and
- *                        down) with a Q4_K, Q8_0 or no shared expert, or bf16
+ *                        router and either Q4_K routed experts (gate and up;
+ *                        down Q4_K or Q5_K) with a Q4_K, Q8_0 or no shared
+ *                        expert, or bf16
  *                        routed experts with a bf16 or no shared expert (one
  *                        format for all layers); all layers share one shape
  *                        with H a multiple of 2048 (<= 4096), E even (<= 256),

@@ -12,27 +12,26 @@
 
 namespace si {
 
-// A block quantises a chunk of 256 Q8_1 blocks (8192 values): its loads are
-// 16-byte, coalesced, four per thread issued before the first encode; the
-// encoder takes 4 consecutive lanes per 32-value block (lane 4j + i holds
+// A block quantises a chunk of 64 U Q8_1 blocks (2048 U values): its loads
+// are 16-byte, coalesced, U per thread issued before the first encode (U = 4
+// for long vectors; 1 for short ones, where the chunk is the whole vector);
+// the encoder takes 4 consecutive lanes per 32-value block (lane 4j + i holds
 // values 8i .. 8i + 7 of one block); the 36-byte blocks are assembled in
 // shared memory and leave as consecutive 16-byte stores (4-byte stores when
 // y is not 16-byte aligned or for the last, partial chunk).
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;
-constexpr int kQuantChunkBlocks = kQuantThreads * kQuantUnroll / 4;   // 256 Q8_1 blocks
-template <typename T>
+template <typename T, int U>
 __global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *__restrict__ x, int64_t n,
                                                                      uint8_t *__restrict__ y, int y_vec16) {
-  __shared__ __align__(16) uint32_t s_out[kQuantChunkBlocks * kQ81Bytes / 4];
+  constexpr int kChunkBlocks = kQuantThreads * U / 4;
+  __shared__ __align__(16) uint32_t s_out[kChunkBlocks * kQ81Bytes / 4];
   grid_dep_wait();
   grid_dep_launch();
   const int64_t groups = n / 8;
-  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kQuantThreads * kQuantUnroll;
-  const bool full = g0 + kQuantThreads * kQuantUnroll <= groups;
-  float v[kQuantUnroll][8];
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kQuantThreads * U;
+  float v[U][8];
 #pragma unroll
-  for (int u = 0; u < kQuantUnroll; ++u) {
+  for (int u = 0; u < U; ++u) {
     const int64_t g = g0 + u * kQuantThreads + threadIdx.x;
     if (g < groups) {
       Load8<T>::run(x + 8 * g, v[u]);
@@ -42,11 +41,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *_
     }
   }
 #pragma unroll
-  for (int u = 0; u < kQuantUnroll; ++u) {
-    // in the last, partial chunk a warp whose groups all lie past the end
-    // skips the encode (its lanes agree: the bound is the warp's first
-    // group), so a short vector costs one encode per thread, not kQuantUnroll
-    if (!full && g0 + u * kQuantThreads + (threadIdx.x & ~31u) >= groups) break;
+  for (int u = 0; u < U; ++u) {
     uint32_t lo, hi;
     uint16_t d16, s16;
     q8_1_encode_4lanes(v[u], lo, hi, d16, s16);
@@ -59,13 +54,13 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *_
   }
   __syncthreads();
   const int64_t nblk_all = n / 32;
-  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kQuantChunkBlocks;
-  const int nblk = nblk_all - b0 < kQuantChunkBlocks ? static_cast<int>(nblk_all - b0) : kQuantChunkBlocks;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunkBlocks;
+  const int nblk = nblk_all - b0 < kChunkBlocks ? static_cast<int>(nblk_all - b0) : kChunkBlocks;
   uint8_t *dst = y + b0 * kQ81Bytes;
-  if (y_vec16 && nblk == kQuantChunkBlocks) {
+  if (y_vec16 && nblk == kChunkBlocks) {
     const uint4 *src = reinterpret_cast<const uint4 *>(s_out);
 #pragma unroll 1
-    for (int i = threadIdx.x; i < kQuantChunkBlocks * kQ81Bytes / 16; i += kQuantThreads)
+    for (int i = threadIdx.x; i < kChunkBlocks * kQ81Bytes / 16; i += kQuantThreads)
       reinterpret_cast<uint4 *>(dst)[i] = src[i];
   } else {
 #pragma unroll 1
@@ -180,8 +175,10 @@ cudaError_t preload_norm() {
   cudaFuncAttributes a;
   cudaError_t e = cudaFuncGetAttributes(&a, add_rmsnorm_kernel);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, residual_add_kernel);
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<float>);
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<__nv_bfloat16>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<float, 1>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<float, 4>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<__nv_bfloat16, 1>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, quantize_q8_1_kernel<__nv_bfloat16, 4>);
   return e;
 }
 
@@ -207,18 +204,29 @@ extern "C" si_status si_quantize_q8_1(const void *x, si_dtype x_type, int64_t n,
   if (!x || !y_q8_1 || n <= 0 || n % 32 != 0) return SI_ERR_INVALID_ARG;
   if (x_type != SI_F32 && x_type != SI_BF16) return SI_ERR_UNSUPPORTED;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y_q8_1) & 3u)) return SI_ERR_INVALID_ARG;
-  const int64_t chunks = (n / 32 + kQuantChunkBlocks - 1) / kQuantChunkBlocks;
+  // long vectors: four groups of 8 values per thread in flight; short ones
+  // (up to 64 K values): one, so that a 2048-value vector is one block
+  // without idle encodes
+  const int U = n > 65536 ? 4 : 1;
+  const int64_t chunk_blocks = kQuantThreads * U / 4;
+  const int64_t chunks = (n / 32 + chunk_blocks - 1) / chunk_blocks;
   if (chunks > 0x7FFFFFFF) return SI_ERR_INVALID_ARG;
   const dim3 grid(static_cast<unsigned>(chunks));
   const int vec16 = (reinterpret_cast<uintptr_t>(y_q8_1) & 15u) == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (x_type == SI_F32)
-    e = launch_pdl(quantize_q8_1_kernel<float>, grid, dim3(kQuantThreads), 0, s,
-                   static_cast<const float *>(x), n, static_cast<uint8_t *>(y_q8_1), vec16);
-  else
-    e = launch_pdl(quantize_q8_1_kernel<__nv_bfloat16>, grid, dim3(kQuantThreads), 0, s,
-                   static_cast<const __nv_bfloat16 *>(x), n, static_cast<uint8_t *>(y_q8_1), vec16);
+  uint8_t *yo = static_cast<uint8_t *>(y_q8_1);
+  if (x_type == SI_F32) {
+    const float *xf = static_cast<const float *>(x);
+    e = U == 4 ? launch_pdl(quantize_q8_1_kernel<float, 4>, grid, dim3(kQuantThreads), 0, s, xf, n, yo, vec16)
+               : launch_pdl(quantize_q8_1_kernel<float, 1>, grid, dim3(kQuantThreads), 0, s, xf, n, yo, vec16);
+  } else {
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    e = U == 4 ? launch_pdl(quantize_q8_1_kernel<__nv_bfloat16, 4>, grid, dim3(kQuantThreads), 0, s, xb, n, yo,
+                            vec16)
+               : launch_pdl(quantize_q8_1_kernel<__nv_bfloat16, 1>, grid, dim3(kQuantThreads), 0, s, xb, n, yo,
+                            vec16);
+  }
   return cuda_status(e);
 }
 

@@ -163,6 +163,8 @@ PERSISTENT_SHAPES = {
     # the shipped formats: Q5_K routed down rows (Q8_0 or Q4_K shared expert)
     "native_q5k_down_q8_0_shared": gen.NATIVE_LAYER_Q5K_DOWN,
     "q5k_down_q4k_shared": gen.LayerSpec(down_type="q5_k", shared_type="q4_k"),
+    "e128_i768_q5k_down": gen.LayerSpec(n_experts=128, inter=768, shared_inter=0, shared_type="q4_k",
+                                        down_type="q5_k"),
     "bf16_e128_top4_i768": gen.LayerSpec(expert_type="bf16", n_experts=128, top_k=4, inter=768,
                                          shared_type="bf16"),
     "bf16_e64_top2_i256": gen.LayerSpec(expert_type="bf16", n_experts=64, top_k=2, inter=256,

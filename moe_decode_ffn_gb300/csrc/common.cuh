@@ -380,6 +380,14 @@ SI_DEV void q4k_isums(const uint4 *w, const uint4 *a, int isum[8], uint32_t &dd,
   }
 }
 
+// Exact float of an integer |v| < 2^22 (the exponent-bias conversion): v is
+// added to the bit pattern of 1.5 * 2^23, whose unit in the last place is 1,
+// and the bias is taken off again by one exact fp32 subtraction. It serves
+// the scaled Q4_K sub-block sums (|sc * isum| <= 63 * 32 * 15 * 128 < 2^22)
+// and the Q8_0 block sums (<= 32 * 128 * 128); Q5_K's scaled sums can pass
+// 2^22 and keep the plain conversion.
+SI_DEV float isum_to_float(int v) { return __fsub_rn(__int_as_float(0x4B400000 + v), 12582912.f); }
+
 // Half h of a Q4_K super-block (sub-blocks 4h .. 4h + 3, 128 weights):
 // isum[i] = exact sum over sub-block 4h + i of q_w * q_a.
 SI_DEV void q4k_half_isums(const uint4 *w, const uint4 *a, int h, int isum[4]) {
@@ -425,8 +433,8 @@ static __device__ __noinline__ float q4k_dot_pairs(const uint8_t *w, const uint8
         mn[e] = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);
       }
     }
-    acc_d = fmaf(static_cast<float>(sc[0] * lo), da[2 * p], acc_d);
-    acc_d = fmaf(static_cast<float>(sc[1] * hi), da[2 * p + 1], acc_d);
+    acc_d = fmaf(isum_to_float(sc[0] * lo), da[2 * p], acc_d);
+    acc_d = fmaf(isum_to_float(sc[1] * hi), da[2 * p + 1], acc_d);
     acc_m = fmaf(static_cast<float>(mn[0]), sa[2 * p], acc_m);
     acc_m = fmaf(static_cast<float>(mn[1]), sa[2 * p + 1], acc_m);
   }
@@ -475,7 +483,7 @@ SI_DEV float q4k_half_dot_loaded(const Q4KHalf &q, const uint4 *a, const float *
   for (int i = 0; i < 4; ++i) {
     const int sc = static_cast<int>((q.scw >> (8 * i)) & 0xFFu);
     const int mn = static_cast<int>((q.mnw >> (8 * i)) & 0xFFu);
-    acc_d = fmaf(static_cast<float>(sc * isum[i]), da[4 * h + i], acc_d);
+    acc_d = fmaf(isum_to_float(sc * isum[i]), da[4 * h + i], acc_d);
     acc_m = fmaf(static_cast<float>(mn), sa[4 * h + i], acc_m);
   }
   return __fsub_rn(__fmul_rn(q.d, acc_d), __fmul_rn(q.dmin, acc_m));
@@ -500,7 +508,7 @@ SI_DEV float q4k_sb_dot(const uint4 *w, const uint4 *a, const float *da, const f
   for (int j = 0; j < 8; ++j) {
     const int sc = static_cast<int>(((j < 4 ? sc0 : sc1) >> (8 * (j & 3))) & 0xFFu);
     const int mn = static_cast<int>(((j < 4 ? mn0 : mn1) >> (8 * (j & 3))) & 0xFFu);
-    acc_d = fmaf(static_cast<float>(sc * isum[j]), da[j], acc_d);
+    acc_d = fmaf(isum_to_float(sc * isum[j]), da[j], acc_d);
     acc_m = fmaf(static_cast<float>(mn), sa[j], acc_m);
   }
   const float d = half_bits_to_float(static_cast<uint16_t>(dd & 0xFFFF));
@@ -595,7 +603,7 @@ SI_DEV float q80_sb_dot(const uint4 *w, const uint4 *a, const float *da) {
         q = ww[(cstart >> 2) + i];
       s = __dp4a(static_cast<int>(q), static_cast<int>(aw[i]), s);
     }
-    acc = fmaf(half_bits_to_float(dbits) * da[b], static_cast<float>(s), acc);
+    acc = fmaf(half_bits_to_float(dbits) * da[b], isum_to_float(s), acc);
   }
   return acc;
 }

@@ -13,8 +13,10 @@
 //
 // Kernels (integer mode, Q4_K experts, no shared expert):
 //  prep    block 0 groups the pairs by expert (counts, offsets, stable order
-//          by token, the list of active experts); the other blocks quantise
-//          every token's x once into a Q8_1 tile record.
+//          by token) and lists the active experts most tokens first, so the
+//          grouped kernels' longest blocks start first and the grid's tail
+//          holds the shortest; the other blocks quantise every token's x
+//          once into a Q8_1 tile record.
 //  gate/up one block per (active expert, 32-row unit of h), two per SM: 32
 //          gate + 32 up rows by TMA bulk copy, the expert's token tiles by
 //          bulk copy, each weight super-block unpacked once and dotted with
@@ -31,6 +33,7 @@ namespace si {
 
 constexpr int kBatchedMaxExperts = 256;
 constexpr int kPrepThreads = 512;
+static_assert(kBatchedMaxExperts <= kPrepThreads - 32, "prep: the last warp is free of expert rows");
 constexpr int kGuBThreads = 256;     // two gate/up blocks per SM: one's copies overlap the other's dots
 constexpr int kGuTok = 4;            // token tiles resident per gate/up block at once
 constexpr int kDownBThreads = 256;
@@ -54,7 +57,7 @@ struct BatchedParams {
   // workspace
   int *count;                // [E]
   int *offset;               // [E + 1]
-  int *active;               // [E] active expert ids, ascending
+  int *active;               // [E] active expert ids by token count, descending (ties: ascending id)
   int *n_active;             // [1]
   int *pair_token;           // [T*k] token of each grouped pair
   int *pair_of;              // [T*k] grouped position of pair (t, r)
@@ -108,11 +111,19 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
   __shared__ int s_e[1024];
   __shared__ unsigned char s_rank[1024];
   __shared__ unsigned short s_wc[32][kBatchedMaxExperts];   // [chunk][expert]
+  // the active list, most tokens first (longest processing time first): an
+  // active expert's bucket is b = min(count, 31); its place is the number of
+  // experts in higher buckets plus those of lower id in its own (the bit
+  // masks of the buckets' experts)
+  __shared__ int s_bn[32];
+  __shared__ uint32_t s_bmask[32][kBatchedMaxExperts / 32];
   const int P = p.T * p.k;   // <= 1024 (host check)
   const int nchunk = (P + 31) / 32;
   const int lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_cnt[e] = 0;
   for (int i = threadIdx.x; i < 32 * kBatchedMaxExperts; i += blockDim.x) (&s_wc[0][0])[i] = 0;
+  if (threadIdx.x < 32) s_bn[threadIdx.x] = 0;
+  if (threadIdx.x < 32 * kBatchedMaxExperts / 32) (&s_bmask[0][0])[threadIdx.x] = 0u;
   __syncthreads();
   for (int q = threadIdx.x; q < 32 * nchunk; q += blockDim.x) {   // whole warps
     int e = -1;
@@ -142,9 +153,14 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
       s_wc[c][e] = static_cast<unsigned short>(acc);
       acc += v;
     }
+    if (acc > 0) {
+      const int b = acc < 31 ? acc : 31;
+      atomicAdd(&s_bn[b], 1);
+      atomicOr(&s_bmask[b][e >> 5], 1u << (e & 31));
+    }
   } else if (threadIdx.x >= kPrepThreads - 32) {
-    // the last warp: expert offsets and the active list (ascending expert),
-    // lane L owning experts 8L .. 8L + 7
+    // the last warp: expert offsets (ascending expert), lane L owning
+    // experts 8L .. 8L + 7
     int cnt[8], sum = 0, nz = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -162,14 +178,13 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
         incl_nz += onz;
       }
     }
-    int acc = incl - sum, na = incl_nz - nz;
+    int acc = incl - sum;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = 8 * lane + i;
       if (e < p.E) {
         s_off[e] = acc;
         acc += cnt[i];
-        if (cnt[i] > 0) p.active[na++] = e;
       }
     }
     if (lane == 31) {
@@ -180,7 +195,21 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
   __syncthreads();
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) {
     p.offset[e] = s_off[e];
-    if (e < p.E) p.count[e] = s_cnt[e];
+    if (e < p.E) {
+      const int c = s_cnt[e];
+      p.count[e] = c;
+      if (c > 0) {
+        const int b = c < 31 ? c : 31;
+        int pos = 0;
+#pragma unroll
+        for (int v = 1; v < 32; ++v) pos += v > b ? s_bn[v] : 0;
+#pragma unroll
+        for (int w = 0; w < kBatchedMaxExperts / 32; ++w)
+          if (w <= (e >> 5))
+            pos += __popc(s_bmask[b][w] & (w < (e >> 5) ? 0xFFFFFFFFu : (1u << (e & 31)) - 1u));
+        p.active[pos] = e;
+      }
+    }
   }
   for (int q = threadIdx.x; q < P; q += blockDim.x) {
     const int e = s_e[q];

@@ -866,11 +866,23 @@ __global__ void __launch_bounds__(256) combine_kernel(BatchedParams p) {
   const int t = blockIdx.y;
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= p.T || j >= p.H) return;
+  // the token's pair positions and weights, then its k rows all in flight,
+  // then the fma chain in rank order
+  int q[8];
+  float w[8], yv[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    if (r < p.k) {
+      q[r] = __ldcg(p.pair_of + t * p.k + r);
+      w[r] = __ldcg(p.wts + t * p.k + r);
+    }
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    if (r < p.k) yv[r] = __ldcg(p.y + static_cast<size_t>(q[r]) * p.H + j);
   float acc = 0.f;
-  for (int r = 0; r < p.k; ++r) {
-    const int q = __ldcg(p.pair_of + t * p.k + r);
-    acc = fmaf(__ldcg(p.wts + t * p.k + r), __ldcg(p.y + static_cast<size_t>(q) * p.H + j), acc);
-  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    if (r < p.k) acc = fmaf(w[r], yv[r], acc);
   p.routed[static_cast<size_t>(t) * p.H + j] = __float2bfloat16_rn(acc);
 }
 

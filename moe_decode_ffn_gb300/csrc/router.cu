@@ -76,24 +76,34 @@ SI_DEV void unpack_w<float>(const uint4 &u, float *v) {
   v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
 }
 
-template <typename XT, int N>
-SI_DEV void load_x(const XT *p, float *v) {
-  if constexpr (sizeof(XT) == 2) {
-    if constexpr (N == 8) {
-      Load8<__nv_bfloat16>::run(p, v);
-    } else {  // 4 bf16 = 8 bytes
-      uint2 u = *reinterpret_cast<const uint2 *>(p);
-      v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-    }
-  } else {
-    if constexpr (N == 8) {
-      Load8<float>::run(p, v);
+// VEC activation values as loaded (raw words: the loads go out before any
+// of them is converted), then as fp32 exactly as load_x gives them.
+template <typename XT, int VEC>
+struct XRaw {
+  static constexpr int kWords = static_cast<int>(sizeof(XT)) * VEC / 4;   // 2, 4 or 8
+  uint32_t w[kWords];
+  SI_DEV void load(const XT *p) {
+    if constexpr (kWords == 2) {
+      const uint2 u = *reinterpret_cast<const uint2 *>(p);
+      w[0] = u.x; w[1] = u.y;
     } else {
-      float4 a = *reinterpret_cast<const float4 *>(p);
-      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+#pragma unroll
+      for (int i = 0; i < kWords / 4; ++i) {
+        const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+        w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+      }
     }
   }
-}
+  SI_DEV void to_float(float *v) const {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      if constexpr (sizeof(XT) == 2)
+        v[i] = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+      else
+        v[i] = __uint_as_float(w[i]);
+    }
+  }
+};
 
 template <typename XT, typename WT, int NCH>
 __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParams p) {
@@ -122,22 +132,39 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
   const int ntok = t1 - t0;
   const uint32_t epoch = __ldcg(&p.epochs[chunk]) + 1u;
   __shared__ float s_part[kMaxChunkTokens][kRouterWarps];
-  for (int t = t0; t < t1; ++t) {
-    float acc = 0.f;
-    if (row_live) {
-      const XT *xs = static_cast<const XT *>(p.x) + static_cast<size_t>(t) * p.H;
+  // TG tokens at a time: their activation vectors are all requested before
+  // the first product (at most 8 vectors per lane in flight; one token at a
+  // time for rows of 4 or more vectors per lane, which hold enough loads)
+  constexpr int TG = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
+  for (int tb = t0; tb < t1; tb += TG) {
+    XRaw<XT, VEC> xr[TG][NCH];
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float wv[VEC], xv[VEC];
-        unpack_w<WT>(wr[c], wv);
-        load_x<XT, VEC>(xs + ((c * p.W + wpart) * 32 + lane) * VEC, xv);
+    for (int u = 0; u < TG; ++u) {
+      if (row_live && tb + u < t1) {
+        const XT *xs = static_cast<const XT *>(p.x) + static_cast<size_t>(tb + u) * p.H;
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) acc = fmaf(wv[i], xv[i], acc);
+        for (int c = 0; c < NCH; ++c) xr[u][c].load(xs + ((c * p.W + wpart) * 32 + lane) * VEC);
       }
     }
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-    if (lane == 0) s_part[t - t0][warp] = acc;
+    for (int u = 0; u < TG; ++u) {
+      if (tb + u < t1) {   // uniform over the block
+        float acc = 0.f;
+        if (row_live) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            float wv[VEC], xv[VEC];
+            unpack_w<WT>(wr[c], wv);
+            xr[u][c].to_float(xv);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc = fmaf(wv[i], xv[i], acc);
+          }
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (lane == 0) s_part[tb + u - t0][warp] = acc;
+      }
+    }
   }
   __syncthreads();
   if (threadIdx.x < p.R * ntok) {

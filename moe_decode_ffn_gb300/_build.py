@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsi_moe.so")
 SOURCES = ["quant_norm.cu", "router.cu", "ffn.cu", "batched.cu", "stack.cu", "requant.cu", "api.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "host.hpp"),
-           os.path.join(CSRC, "topk.cuh"), os.path.join(CSRC, "tc.cuh"),
+           os.path.join(CSRC, "topk.cuh"), os.path.join(CSRC, "tc.cuh"), os.path.join(CSRC, "norm.cuh"),
            os.path.join(ROOT, "include", "si_moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

@@ -360,10 +360,8 @@ static si_status blayer_enqueue(const si_moe_layer &L, int T, int mode, const vo
   si_status st = router_launch(x, SI_BF16, L.w_router, L.router_type, L.hidden, L.n_experts,
                                L.top_k, T, ids, wts, nullptr, base + g.off_router, status, s);
   if (st != SI_OK) return st;
-  st = batched_launch(&L, T, mode, x, ids, wts, routed, base + g.off_ffn, status, s);
-  if (st != SI_OK) return st;
-  return norm_launch(routed, residual, nullptr, L.w_norm, L.hidden, T, L.eps, sum_out, norm_out,
-                     nullptr, s);
+  const BatchedNorm nm{residual, L.w_norm, L.eps, sum_out, norm_out};
+  return batched_launch(&L, T, mode, x, ids, wts, routed, base + g.off_ffn, status, s, &nm);
 }
 
 // Batched stack workspace: header, then per layer [layer workspace][sum bf16 T x H][norm bf16 T x H].

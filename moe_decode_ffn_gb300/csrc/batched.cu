@@ -24,9 +24,12 @@
 //  down    one block per (active expert, 32 output rows): the rows once, then
 //          y = D_e h for each of the expert's pairs (fp32 per pair), each
 //          weight piece unpacked once per chunk of pairs.
-//  combine routed[t][j] = sum_r w[t][r] * y[pair(t, r)][j] in rank order.
+//  combine routed[t][j] = sum_r w[t][r] * y[pair(t, r)][j] in rank order;
+//          in the batched layer one block per token also runs the residual
+//          norm on it (combine_norm_kernel).
 #include "common.cuh"
 #include "host.hpp"
+#include "norm.cuh"
 #include "tc.cuh"
 
 namespace si {
@@ -886,13 +889,67 @@ __global__ void __launch_bounds__(256) combine_kernel(BatchedParams p) {
   p.routed[static_cast<size_t>(t) * p.H + j] = __float2bfloat16_rn(acc);
 }
 
+// The batched layer's combine and residual norm in one pass: block t forms
+// routed[t] (the combine kernel's fma chain in rank order and its bf16
+// rounding; written out too) slice by slice as the norm row's input a, with
+// b = the residual: the bits of the combine kernel followed by the norm
+// kernel.
+__global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(BatchedParams p, BatchedNorm nm) {
+  extern __shared__ float s_sum[];   // [H]
+  __shared__ float s_red[kNormThreads / 32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int t = blockIdx.x;
+  int q[8];
+  float w[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    if (r < p.k) {
+      q[r] = __ldcg(p.pair_of + t * p.k + r);
+      w[r] = __ldcg(p.wts + t * p.k + r);
+    }
+  __nv_bfloat16 *routed = p.routed + static_cast<size_t>(t) * p.H;
+  auto load_routed = [&](int i0, float va[8]) {
+    float4 yv[8][2];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < p.k) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.y + static_cast<size_t>(q[r]) * p.H + i0);
+        yv[r][0] = __ldcg(src);
+        yv[r][1] = __ldcg(src + 1);
+      }
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < p.k) {
+        const float v[8] = {yv[r][0].x, yv[r][0].y, yv[r][0].z, yv[r][0].w,
+                            yv[r][1].x, yv[r][1].y, yv[r][1].z, yv[r][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[r], v[i], acc[i]);
+      }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) va[i] = bf16_round(acc[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = bf16_bits(va[2 * i]) | (static_cast<uint32_t>(bf16_bits(va[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4 *>(routed + i0) = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  add_rmsnorm_row(load_routed, static_cast<const __nv_bfloat16 *>(nm.residual), nullptr,
+                  static_cast<const __nv_bfloat16 *>(nm.w_norm), p.H, nm.eps, t,
+                  static_cast<__nv_bfloat16 *>(nm.sum_out), static_cast<__nv_bfloat16 *>(nm.norm_out), nullptr,
+                  s_sum, s_red);
+}
+
 // Test export: the exact integer block sums of the batched helpers for
 // n_vec activation vectors (the "tokens"), each super-block's code words
 // loaded once for all of them, as the grouped kernels do: whole super-blocks
 // (gate/up) or halves (down). out int32 [n_vec][rows][k / 32].
 __global__ void tokens_block_dots_kernel(const uint8_t *w, int rows, int k, const uint8_t *a,
                                          int n_vec, int halves, int32_t *out) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int nsb = k / kQKK, nb = k / 32, rec = tile_record_bytes(k);
   for (int t = 0; t < n_vec; ++t)
     tile_from_q8_1(a + static_cast<size_t>(t) * nb * kQ81Bytes, k, tile_at(smem + t * rec, k));
@@ -1011,7 +1068,8 @@ cudaError_t preload_batched() {
                       reinterpret_cast<const void *>(down_grouped_kernel<2>),
                       reinterpret_cast<const void *>(tc_gateup_kernel),
                       reinterpret_cast<const void *>(tc_down_kernel),
-                      reinterpret_cast<const void *>(combine_kernel)};
+                      reinterpret_cast<const void *>(combine_kernel),
+                      reinterpret_cast<const void *>(combine_norm_kernel)};
   for (const void *k : ks) {
     const cudaError_t e = cudaFuncGetAttributes(&a, k);
     if (e != cudaSuccess) return e;
@@ -1024,11 +1082,17 @@ size_t batched_workspace_bytes(const si_moe_layer &L, int n_tokens) {
 }
 si_status batched_validate(const si_moe_layer &L, int n_tokens) { return batched_check(L, n_tokens); }
 
+// The combine step: alone, or with the layer's residual norm.
+static cudaError_t launch_combine(const BatchedParams &p, const BatchedNorm *norm, cudaStream_t s) {
+  if (!norm) return launch_pdl(combine_kernel, dim3((p.H + 255) / 256, p.T), dim3(256), 0, s, p);
+  return launch_pdl(combine_norm_kernel, dim3(p.T), dim3(kNormThreads), sizeof(float) * p.H, s, p, *norm);
+}
+
 // Enqueue the batched routed FFN (arguments checked by the caller) into
 // workspace `workspace`, device errors reported to `status`.
 si_status batched_launch(const si_moe_layer *L, int n_tokens, int mode, const void *x,
                          const int32_t *topk_ids, const float *topk_w, void *routed_out,
-                         void *workspace, uint32_t *status, cudaStream_t s) {
+                         void *workspace, uint32_t *status, cudaStream_t s, const BatchedNorm *norm) {
   // AUTO takes the integer path: measured faster than the tensor-core path at
   // every supported batch (1..128 tokens over 128 experts leave at most ~8
   // tokens per selected expert, so dequantising the weights to fp16 costs more
@@ -1074,7 +1138,7 @@ si_status batched_launch(const si_moe_layer *L, int n_tokens, int mode, const vo
       e = launch_pdl(tc_down_kernel, dim3(max_active * (L->hidden / 128)), dim3(kTcThreads),
                      kTcSmem, s, p);
     if (e == cudaSuccess)
-      e = launch_pdl(combine_kernel, dim3((L->hidden + 255) / 256, n_tokens), dim3(256), 0, s, p);
+      e = launch_combine(p, norm, s);
     return cuda_status(e);
   }
   const int R = down_rows_per_lane(*L);
@@ -1094,7 +1158,7 @@ si_status batched_launch(const si_moe_layer *L, int n_tokens, int mode, const vo
   if (e == cudaSuccess)
     e = launch_pdl(down, dim3(max_active * tiles), dim3(down_threads), dsm, s, p);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel, dim3((L->hidden + 255) / 256, n_tokens), dim3(256), 0, s, p);
+    e = launch_combine(p, norm, s);
   return cuda_status(e);
 }
 

@@ -105,9 +105,17 @@ si_status ffn_launch(const si_moe_layer &L, const void *x, const void *x_q8_1, c
 // ---- batched routed FFN (batched.cu): shape check, workspace, enqueue
 si_status batched_validate(const si_moe_layer &L, int n_tokens);
 size_t batched_workspace_bytes(const si_moe_layer &L, int n_tokens);
+// The layer's residual norm taken into the combine step (batched layer):
+// sum = bf16(routed + residual), norm = RMSNorm(sum) * w_norm.
+struct BatchedNorm {
+  const void *residual, *w_norm;
+  float eps;
+  void *sum_out, *norm_out;
+};
 si_status batched_launch(const si_moe_layer *L, int n_tokens, int mode, const void *x,
                          const int32_t *topk_ids, const float *topk_w, void *routed_out,
-                         void *workspace, uint32_t *status, cudaStream_t s);
+                         void *workspace, uint32_t *status, cudaStream_t s,
+                         const BatchedNorm *norm = nullptr);
 cudaError_t preload_batched();
 
 // ---- test export of the batched helpers' integer block sums (batched.cu)

@@ -9,6 +9,7 @@
 // norm.
 #include "common.cuh"
 #include "host.hpp"
+#include "norm.cuh"
 
 namespace si {
 
@@ -70,19 +71,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_q8_1_kernel(const T *_
 }
 
 // ---------------------------------------------------------------------------
-// add_rmsnorm: one block per row, 256 threads, each owning 8 consecutive
-// values per 2048-value slice.
-//   t = bf16(a + b); s = c ? bf16(t + c) : t; r = rsqrt(mean(s^2) + eps);
-//   y = bf16((s * r) * w); optional Q8_1 of y.
-// With b == nullptr: s = bf16(a + c) (the 2-input norm of the unfused chain).
+// add_rmsnorm: one block per row (the row function of norm.cuh).
 // ---------------------------------------------------------------------------
 SI_TRACE_BUFFER
-
-constexpr int kNormThreads = 256;
-
-__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *p, float v[8]) {
-  Load8<__nv_bfloat16>::run(p, v);
-}
 
 __global__ void __launch_bounds__(kNormThreads)
     add_rmsnorm_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
@@ -92,63 +83,13 @@ __global__ void __launch_bounds__(kNormThreads)
   extern __shared__ float s_sum[];  // [n]
   __shared__ float s_red[kNormThreads / 32];
   const int row = blockIdx.x;
-  const size_t base = static_cast<size_t>(row) * n;
+  const __nv_bfloat16 *ar = a + static_cast<size_t>(row) * n;
   SI_TRACE_MARK(3, 0);
   grid_dep_wait();
   grid_dep_launch();
   SI_TRACE_MARK(3, 1);
-  float ss = 0.f;
-  for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * kNormThreads) {
-    float va[8], vb[8], vc[8], s[8];
-    load_bf16x8(a + base + i0, va);
-    if (b) load_bf16x8(b + base + i0, vb);
-    if (c) load_bf16x8(c + base + i0, vc);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float t = b ? bf16_round(va[i] + vb[i]) : va[i];
-      s[i] = c ? bf16_round(t + vc[i]) : t;
-      ss = fmaf(s[i], s[i], ss);
-      s_sum[i0 + i] = s[i];
-    }
-    uint4 o;
-    o.x = bf16_bits(s[0]) | (static_cast<uint32_t>(bf16_bits(s[1])) << 16);
-    o.y = bf16_bits(s[2]) | (static_cast<uint32_t>(bf16_bits(s[3])) << 16);
-    o.z = bf16_bits(s[4]) | (static_cast<uint32_t>(bf16_bits(s[5])) << 16);
-    o.w = bf16_bits(s[6]) | (static_cast<uint32_t>(bf16_bits(s[7])) << 16);
-    *reinterpret_cast<uint4 *>(sum_out + base + i0) = o;
-  }
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
-#pragma unroll
-  for (int i = 0; i < kNormThreads / 32; ++i) tot += s_red[i];
-  const float r = rsqrtf(__fdiv_rn(tot, static_cast<float>(n)) + eps);
-  SI_TRACE_MARK(3, 2);
-  for (int i0 = 8 * threadIdx.x; i0 < n; i0 += 8 * kNormThreads) {
-    float vw[8], y[8];
-    load_bf16x8(w + i0, vw);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = bf16_round(__fmul_rn(__fmul_rn(s_sum[i0 + i], r), vw[i]));
-    uint4 o;
-    o.x = bf16_bits(y[0]) | (static_cast<uint32_t>(bf16_bits(y[1])) << 16);
-    o.y = bf16_bits(y[2]) | (static_cast<uint32_t>(bf16_bits(y[3])) << 16);
-    o.z = bf16_bits(y[4]) | (static_cast<uint32_t>(bf16_bits(y[5])) << 16);
-    o.w = bf16_bits(y[6]) | (static_cast<uint32_t>(bf16_bits(y[7])) << 16);
-    *reinterpret_cast<uint4 *>(norm_out + base + i0) = o;
-    if (q8_out) {  // n % 256 == 0, so whole warps take this branch together
-      uint32_t lo, hi;
-      uint16_t d16, s16;
-      q8_1_encode_4lanes(y, lo, hi, d16, s16);
-      const int g = i0 / 8;
-      uint8_t *blk = q8_out + (static_cast<size_t>(row) * (n / 32) + (g >> 2)) * kQ81Bytes;
-      uint32_t *q = reinterpret_cast<uint32_t *>(blk + 4 + 8 * (g & 3));
-      q[0] = lo;
-      q[1] = hi;
-      if ((g & 3) == 0) *reinterpret_cast<uint32_t *>(blk) = d16 | (static_cast<uint32_t>(s16) << 16);
-    }
-  }
+  add_rmsnorm_row([&](int i0, float va[8]) { Load8<__nv_bfloat16>::run(ar + i0, va); }, b, c, w, n, eps, row,
+                  sum_out, norm_out, q8_out, s_sum, s_red);
   SI_TRACE_MARK(3, 3);
 }
 
@@ -161,8 +102,8 @@ __global__ void __launch_bounds__(256) residual_add_kernel(const __nv_bfloat16 *
   const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (8 * g >= n) return;
   float va[8], vb[8];
-  load_bf16x8(a + 8 * g, va);
-  load_bf16x8(b + 8 * g, vb);
+  Load8<__nv_bfloat16>::run(a + 8 * g, va);
+  Load8<__nv_bfloat16>::run(b + 8 * g, vb);
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)

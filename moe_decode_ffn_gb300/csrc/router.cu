@@ -105,81 +105,11 @@ struct XRaw {
   }
 };
 
-template <typename XT, typename WT, int NCH>
-__global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParams p) {
-  constexpr int VEC = Vec<WT>::n;
-  SI_TRACE_MARK(0, 0);
+// After a block has written its logits of chunk `chunk` (tokens t0 ..
+// t0 + ntok - 1): the chunk's completion count, and in the chunk's last
+// block the check of every logit's epoch, the top-k selection and softmax.
+SI_DEV void router_chunk_tail(const RouterParams &p, int chunk, int t0, int ntok, uint32_t epoch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = warp / p.W, wpart = warp % p.W;
-  const int e = blockIdx.x * p.R + r;
-  const int chunk = blockIdx.y;
-  const bool row_live = e < p.E;
-
-  // This warp's part of its row: 16-byte vectors (i * W + wpart) * 32 + lane.
-  uint4 wr[NCH];
-  if (row_live) {
-    const uint4 *wrow = reinterpret_cast<const uint4 *>(static_cast<const WT *>(p.w) +
-                                                        static_cast<size_t>(e) * p.H);
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) wr[c] = __ldg(wrow + (c * p.W + wpart) * 32 + lane);
-  }
-  grid_dep_wait();
-  grid_dep_launch();
-  SI_TRACE_MARK(0, 1);
-
-  const int t0 = chunk * p.tc;
-  const int t1 = min(p.T, t0 + p.tc);
-  const int ntok = t1 - t0;
-  const uint32_t epoch = __ldcg(&p.epochs[chunk]) + 1u;
-  __shared__ float s_part[kMaxChunkTokens][kRouterWarps];
-  // TG tokens at a time: their activation vectors are all requested before
-  // the first product (at most 8 vectors per lane in flight; one token at a
-  // time for rows of 4 or more vectors per lane, which hold enough loads)
-  constexpr int TG = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
-  for (int tb = t0; tb < t1; tb += TG) {
-    XRaw<XT, VEC> xr[TG][NCH];
-#pragma unroll
-    for (int u = 0; u < TG; ++u) {
-      if (row_live && tb + u < t1) {
-        const XT *xs = static_cast<const XT *>(p.x) + static_cast<size_t>(tb + u) * p.H;
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) xr[u][c].load(xs + ((c * p.W + wpart) * 32 + lane) * VEC);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < TG; ++u) {
-      if (tb + u < t1) {   // uniform over the block
-        float acc = 0.f;
-        if (row_live) {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            float wv[VEC], xv[VEC];
-            unpack_w<WT>(wr[c], wv);
-            xr[u][c].to_float(xv);
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) acc = fmaf(wv[i], xv[i], acc);
-          }
-        }
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (lane == 0) s_part[tb + u - t0][warp] = acc;
-      }
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < p.R * ntok) {
-    const int rr = threadIdx.x % p.R, tt = threadIdx.x / p.R;
-    const int ex = blockIdx.x * p.R + rr;
-    if (ex < p.E) {
-      float l = s_part[tt][rr * p.W];
-      for (int w = 1; w < p.W; ++w) l += s_part[tt][rr * p.W + w];
-      const size_t o = static_cast<size_t>(t0 + tt) * p.E + ex;
-      p.tagged[o] = make_uint2(__float_as_uint(l), epoch);
-      if (p.logits) p.logits[o] = l;
-    }
-  }
-  SI_TRACE_MARK(0, 2);
-
   // Completion count: release this block's logits, acquire everyone's.
   __shared__ int s_last;
   __syncthreads();
@@ -293,6 +223,181 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
   SI_TRACE_MARK(0, 6);
 }
 
+template <typename XT, typename WT, int NCH>
+__global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParams p) {
+  constexpr int VEC = Vec<WT>::n;
+  SI_TRACE_MARK(0, 0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = warp / p.W, wpart = warp % p.W;
+  const int e = blockIdx.x * p.R + r;
+  const int chunk = blockIdx.y;
+  const bool row_live = e < p.E;
+
+  // This warp's part of its row: 16-byte vectors (i * W + wpart) * 32 + lane.
+  uint4 wr[NCH];
+  if (row_live) {
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(static_cast<const WT *>(p.w) +
+                                                        static_cast<size_t>(e) * p.H);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) wr[c] = __ldg(wrow + (c * p.W + wpart) * 32 + lane);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  SI_TRACE_MARK(0, 1);
+
+  const int t0 = chunk * p.tc;
+  const int t1 = min(p.T, t0 + p.tc);
+  const int ntok = t1 - t0;
+  const uint32_t epoch = __ldcg(&p.epochs[chunk]) + 1u;
+  __shared__ float s_part[kMaxChunkTokens][kRouterWarps];
+  // TG tokens at a time: their activation vectors are all requested before
+  // the first product (at most 8 vectors per lane in flight; one token at a
+  // time for rows of 4 or more vectors per lane, which hold enough loads)
+  constexpr int TG = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
+  for (int tb = t0; tb < t1; tb += TG) {
+    XRaw<XT, VEC> xr[TG][NCH];
+#pragma unroll
+    for (int u = 0; u < TG; ++u) {
+      if (row_live && tb + u < t1) {
+        const XT *xs = static_cast<const XT *>(p.x) + static_cast<size_t>(tb + u) * p.H;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) xr[u][c].load(xs + ((c * p.W + wpart) * 32 + lane) * VEC);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < TG; ++u) {
+      if (tb + u < t1) {   // uniform over the block
+        float acc = 0.f;
+        if (row_live) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            float wv[VEC], xv[VEC];
+            unpack_w<WT>(wr[c], wv);
+            xr[u][c].to_float(xv);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc = fmaf(wv[i], xv[i], acc);
+          }
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (lane == 0) s_part[tb + u - t0][warp] = acc;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < p.R * ntok) {
+    const int rr = threadIdx.x % p.R, tt = threadIdx.x / p.R;
+    const int ex = blockIdx.x * p.R + rr;
+    if (ex < p.E) {
+      float l = s_part[tt][rr * p.W];
+      for (int w = 1; w < p.W; ++w) l += s_part[tt][rr * p.W + w];
+      const size_t o = static_cast<size_t>(t0 + tt) * p.E + ex;
+      p.tagged[o] = make_uint2(__float_as_uint(l), epoch);
+      if (p.logits) p.logits[o] = l;
+    }
+  }
+  SI_TRACE_MARK(0, 2);
+
+  router_chunk_tail(p, chunk, t0, ntok, epoch);
+}
+
+// Sums over the warp of N per-lane values (N a multiple of 32), each lane
+// keeping N / 32 of them: lane L ends with outputs L * N / 32 + j. At the
+// step of distance d (16, 8, 4, 2, 1) a lane keeps the half of its current
+// values that bit d of its index selects and adds its partner's copy of that
+// half to its own: every output is the value an xor butterfly over the same
+// distances gives it (own value plus partner's at each step), bit for bit,
+// with N - 1 shuffles per lane instead of 5 N.
+template <int N>
+SI_DEV void warp_sums_spread(float v[N], int lane) {
+#pragma unroll
+  for (int d = 16, m = N / 2; d > 0; d >>= 1, m >>= 1) {
+    const bool hi = (lane & d) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float keep = hi ? v[i + m] : v[i];
+      const float send = hi ? v[i] : v[i + m];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+    }
+  }
+}
+
+// Several tokens (a full chunk of up to kMaxChunkTokens) against RT router
+// rows per block: warp w, lane l take vectors (c * 8 + w) * 32 + l of every
+// row, as router_topk_kernel does with one row per block and 8 warps per
+// row, so every logit is the same fma chain, the same butterfly and the same
+// sum over the 8 warps: the same bits with RT + kMaxChunkTokens loads per
+// lane and chunk instead of one row load per kMaxChunkTokens x loads.
+template <typename XT, typename WT, int NCH, int RT>
+__global__ void __launch_bounds__(kRouterThreads) router_rows_kernel(RouterParams p) {
+  constexpr int VEC = Vec<WT>::n;
+  constexpr int C = kMaxChunkTokens;
+  constexpr int N = RT * C < 32 ? 32 : RT * C;
+  static_assert(kRouterWarps == 8, "8 warps split every row");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.x * RT;
+  const int chunk = blockIdx.y;
+  uint4 wr[RT][NCH];
+#pragma unroll
+  for (int r = 0; r < RT; ++r) {
+    const bool live = e0 + r < p.E;
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(static_cast<const WT *>(p.w) +
+                                                        static_cast<size_t>(live ? e0 + r : 0) * p.H);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+      wr[r][c] = live ? __ldg(wrow + (c * 8 + warp) * 32 + lane) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  const int t0 = chunk * p.tc;
+  const int ntok = min(p.T, t0 + p.tc) - t0;
+  const uint32_t epoch = __ldcg(&p.epochs[chunk]) + 1u;
+  float acc[N];
+#pragma unroll
+  for (int o = 0; o < N; ++o) acc[o] = 0.f;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    XRaw<XT, VEC> xr[C];
+#pragma unroll
+    for (int u = 0; u < C; ++u)
+      if (u < ntok)
+        xr[u].load(static_cast<const XT *>(p.x) + static_cast<size_t>(t0 + u) * p.H +
+                   ((c * 8 + warp) * 32 + lane) * VEC);
+#pragma unroll
+    for (int u = 0; u < C; ++u) {
+      if (u < ntok) {
+        float xv[VEC];
+        xr[u].to_float(xv);
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          float wv[VEC];
+          unpack_w<WT>(wr[r][c], wv);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) acc[r * C + u] = fmaf(wv[i], xv[i], acc[r * C + u]);
+        }
+      }
+    }
+  }
+  warp_sums_spread<N>(acc, lane);
+  __shared__ float s_part[N][kRouterWarps];
+#pragma unroll
+  for (int j = 0; j < N / 32; ++j) s_part[lane * (N / 32) + j][warp] = acc[j];
+  __syncthreads();
+  if (threadIdx.x < RT * C) {
+    const int r = threadIdx.x / C, u = threadIdx.x % C;
+    const int ex = e0 + r;
+    if (u < ntok && ex < p.E) {
+      float l = s_part[threadIdx.x][0];
+#pragma unroll
+      for (int w = 1; w < kRouterWarps; ++w) l += s_part[threadIdx.x][w];
+      const size_t o = static_cast<size_t>(t0 + u) * p.E + ex;
+      p.tagged[o] = make_uint2(__float_as_uint(l), epoch);
+      if (p.logits) p.logits[o] = l;
+    }
+  }
+  router_chunk_tail(p, chunk, t0, ntok, epoch);
+}
+
 // Rows per block R and warps per row W (R * W = 8): one row per block with
 // its 16-byte vectors dealt to the 256 lanes of all 8 warps (vector
 // c * 256 + 32 w + lane to lane `lane` of warp w), the order in which the
@@ -328,11 +433,29 @@ RouterGeom router_geom(int n_experts, int hidden, int n_tokens) {
   return g;
 }
 
+// Rows per block of the several-chunk kernel: enough rows that each block
+// reads fewer bytes than its tokens' activations, few enough that the grid
+// still covers the GPU (0: one row per block, router_topk_kernel).
+static int rows_per_block(int W, int nch, int tc, int n_chunks) {
+  if (W != 8 || nch > 2 || tc != kMaxChunkTokens) return 0;
+  return n_chunks >= 8 ? 8 : (n_chunks >= 4 ? 4 : (n_chunks >= 2 ? 2 : 0));
+}
+
 template <typename XT, typename WT>
 static cudaError_t launch_router_t(RouterParams p, int n_chunks, cudaStream_t s) {
   constexpr int VEC = Vec<WT>::n;
   int nch;
   router_shape(p.E, p.H, VEC, p.R, p.W, nch);
+  const int rt = rows_per_block(p.W, nch, p.tc, n_chunks);
+  if (rt > 0) {
+    p.cpc = (p.E + rt - 1) / rt;
+    const dim3 grid(p.cpc, n_chunks), block(kRouterThreads);
+    auto k = nch == 1 ? (rt == 8 ? router_rows_kernel<XT, WT, 1, 8>
+                                 : rt == 4 ? router_rows_kernel<XT, WT, 1, 4> : router_rows_kernel<XT, WT, 1, 2>)
+                      : (rt == 8 ? router_rows_kernel<XT, WT, 2, 8>
+                                 : rt == 4 ? router_rows_kernel<XT, WT, 2, 4> : router_rows_kernel<XT, WT, 2, 2>);
+    return launch_pdl(k, grid, block, 0, s, p);
+  }
   p.cpc = (p.E + p.R - 1) / p.R;
   const dim3 grid(p.cpc, n_chunks), block(kRouterThreads);
   switch (nch) {
@@ -353,6 +476,12 @@ static cudaError_t preload_router_t() {
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_topk_kernel<XT, WT, 4>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_topk_kernel<XT, WT, 8>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_topk_kernel<XT, WT, 16>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_rows_kernel<XT, WT, 1, 2>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_rows_kernel<XT, WT, 1, 4>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_rows_kernel<XT, WT, 1, 8>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_rows_kernel<XT, WT, 2, 2>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_rows_kernel<XT, WT, 2, 4>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, router_rows_kernel<XT, WT, 2, 8>);
   return e;
 }
 

@@ -102,3 +102,22 @@ def test_router_detects_unzeroed_workspace():
     ids, w, _ = m.si_moe_router_topk(X, W, 8, ws=ws)
     assert m.si_workspace_status(ws) == m.SI_OK
     assert torch.all(ids >= 0)
+
+
+@pytest.mark.parametrize("n_tokens", [16, 24, 32, 64, 100])
+@pytest.mark.parametrize("n_experts,w_fp32", [(128, False), (100, False), (256, True)])
+def test_router_chunks_equal_single_token_calls(n_tokens, n_experts, w_fp32):
+    """Several chunks of tokens (several router rows per block) give the bits
+    of one-token calls (one row per block): the same logits, ids and weights."""
+    W = gen.to_bf16(gen.normal([gen.stream_key(6, n_experts)], n_experts * 2048, 0.0, 0.02)[0]
+                    ).reshape(n_experts, 2048)
+    if w_fp32:
+        W = W.float()
+    X = gen.make_tokens(35, n_tokens).cuda()
+    W = W.cuda()
+    ids, w, logits = m.si_moe_router_topk(X, W, 8, want_logits=True)
+    for t in range(n_tokens):
+        i1, w1, l1 = m.si_moe_router_topk(X[t:t + 1], W, 8, want_logits=True)
+        assert torch.equal(logits[t:t + 1], l1), t
+        assert torch.equal(ids[t:t + 1], i1), t
+        assert torch.equal(w[t:t + 1], w1), t

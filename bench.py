@@ -758,6 +758,20 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         print(f"quantize n={n} launches={args.launches}")
         return 0
+    if args.batched and args.batched_stack:
+        T = args.batched
+        layers = [m.device_layer(gen.Q4K_LAYER_128E, args.seed, l) for l in range(args.layers)]
+        x = gen.make_tokens(args.seed + 1, T, device="cuda")
+        mode = m.SI_FFN_TENSOR if args.mode == "tensor" else m.SI_FFN_INT8
+        g = m.BatchedStackGraph(layers, x, mode=mode)
+        for _ in range(args.launches):
+            g.launch()
+        torch.cuda.synchronize()
+        st = m.si_workspace_status(g.ws)
+        print(f"batched stack layers={args.layers} T={T} mode={args.mode} launches={args.launches} "
+              f"persistent={g.persistent} status={m.status_string(st)}")
+        g.close()
+        return 0 if st == m.SI_OK else 1
     if args.batched:
         T = args.batched
         L = m.device_layer(gen.Q4K_LAYER_128E, args.seed, 0)
@@ -814,6 +828,9 @@ def main():
                     help="four kernels per layer instead of the persistent kernel")
     pc.add_argument("--spec", default="q4k", choices=["q4k", "q4k_q8_0", "bf16"])
     pc.add_argument("--batched", type=int, default=0, help="T: the batched FFN of T tokens instead")
+    pc.add_argument("--batched-stack", action="store_true",
+                    help="with --batched T: the batched layer stack (router, grouped experts, combine + "
+                         "norm) of --layers 128-expert layers")
     pc.add_argument("--mode", default="tensor", choices=["tensor", "int8"])
     pc.add_argument("--quant", type=int, default=0, help="n: the Q8_1 quantiser on n bf16 values instead")
     args = ap.parse_args()

@@ -105,15 +105,16 @@ def test_router_detects_unzeroed_workspace():
 
 
 @pytest.mark.parametrize("n_tokens", [16, 24, 32, 64, 100])
-@pytest.mark.parametrize("n_experts,w_fp32", [(128, False), (100, False), (256, True)])
-def test_router_chunks_equal_single_token_calls(n_tokens, n_experts, w_fp32):
+@pytest.mark.parametrize("n_experts,w_fp32,hidden", [(128, False, 2048), (100, False, 2048), (256, True, 2048),
+                                                     (128, False, 4096)])
+def test_router_chunks_equal_single_token_calls(n_tokens, n_experts, w_fp32, hidden):
     """Several chunks of tokens (several router rows per block) give the bits
     of one-token calls (one row per block): the same logits, ids and weights."""
-    W = gen.to_bf16(gen.normal([gen.stream_key(6, n_experts)], n_experts * 2048, 0.0, 0.02)[0]
-                    ).reshape(n_experts, 2048)
+    W = gen.to_bf16(gen.normal([gen.stream_key(6, n_experts, hidden)], n_experts * hidden, 0.0, 0.02)[0]
+                    ).reshape(n_experts, hidden)
     if w_fp32:
         W = W.float()
-    X = gen.make_tokens(35, n_tokens).cuda()
+    X = gen.make_tokens(35, n_tokens, hidden=hidden).cuda()
     W = W.cuda()
     ids, w, logits = m.si_moe_router_topk(X, W, 8, want_logits=True)
     for t in range(n_tokens):

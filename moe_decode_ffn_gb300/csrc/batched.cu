@@ -224,30 +224,39 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
 
 // ---------------------------------------------------------------------------
 // The code words of pair p (sub-blocks 2p, 2p + 1) of a Q4_K super-block,
-// split once into their low (sub-block 2p) and high (2p + 1) nibbles, and
-// the exact int32 sums of those nibbles with one token's 64 activation codes
-// of the pair (a4: sub-block 2p's 32 codes, then 2p + 1's): the integer sums
-// of q4k_pair_isums.
+// split once into their low nibbles (sub-block 2p) and their high nibbles
+// left in place (2p + 1, each byte 16 times its code: one mask, no shift),
+// and the exact int32 sums of those codes with one token's 64 activation
+// codes of the pair (a4: sub-block 2p's 32 codes, then 2p + 1's): the
+// integer sums of q4k_pair_isums (the high sum taken as unsigned x signed
+// bytes and divided by 16, which is exact).
 SI_DEV void q4k_pair_nibbles(const uint4 *wv, int p, uint32_t lo[8], uint32_t hi[8]) {
   uint32_t qw[8];
   q4k_pair_words(wv, p, qw);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     lo[i] = qw[i] & 0x0F0F0F0Fu;
-    hi[i] = (qw[i] >> 4) & 0x0F0F0F0Fu;
+    hi[i] = qw[i] & 0xF0F0F0F0u;   // the high nibbles, times 16
   }
+}
+// dp4a of unsigned bytes a with signed bytes b
+SI_DEV int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 SI_DEV void q4k_pair_nibble_isums(const uint32_t lo[8], const uint32_t hi[8], const uint4 a4[4], int &slo,
                                   int &shi) {
   const uint32_t al[8] = {a4[0].x, a4[0].y, a4[0].z, a4[0].w, a4[1].x, a4[1].y, a4[1].z, a4[1].w};
   const uint32_t ah[8] = {a4[2].x, a4[2].y, a4[2].z, a4[2].w, a4[3].x, a4[3].y, a4[3].z, a4[3].w};
   slo = 0;
-  shi = 0;
+  int shi16 = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     slo = __dp4a(static_cast<int>(lo[i]), static_cast<int>(al[i]), slo);
-    shi = __dp4a(static_cast<int>(hi[i]), static_cast<int>(ah[i]), shi);
+    shi16 = dp4a_us(hi[i], ah[i], shi16);
   }
+  shi = shi16 >> 4;   // exact: 16 times the sum of the high nibbles' products
 }
 
 // Two rows' Q4_K super-blocks w0, w1 (the same super-block sb, shared

@@ -511,8 +511,11 @@ __global__ void __launch_bounds__(kDownBThreads, 3) down_grouped_kernel(BatchedP
   float *part = reinterpret_cast<float *>(smem + 64);            // [kDnTok][P][kRows]
   uint8_t *ht = smem + 64 + kDnTok * kRows * P * 4;              // [kDnTok][hrb]
   uint8_t *wbuf = ht + kDnTok * hrb;                             // [kRows][rb_d]
-  grid_dep_wait();
-  grid_dep_launch();
+  // The grouping (counts, offsets, active list) comes from the grouping
+  // kernel two launches back, which has completed: this grid is launched
+  // only once every gate/up block has passed its own wait on it. So this
+  // block's weight rows are requested before the wait on the gate/up kernel,
+  // whose h tiles it reads after it.
   const int na = __ldcg(p.n_active);
   if (static_cast<int>(blockIdx.x) >= na * tiles) return;
   const int e = __ldcg(p.active + blockIdx.x / tiles);
@@ -531,6 +534,8 @@ __global__ void __launch_bounds__(kDownBThreads, 3) down_grouped_kernel(BatchedP
     bulk_g2s_evict_first(wbuf, p.wd + (static_cast<size_t>(e) * p.H + j0) * p.rb_d, bytes, &bars[0],
                          policy_evict_first());
   }
+  grid_dep_wait();
+  grid_dep_launch();
   uint32_t phase = 0;
   for (int c0 = 0; c0 < n_e; c0 += kDnTok) {
     const int nc = min(kDnTok, n_e - c0);

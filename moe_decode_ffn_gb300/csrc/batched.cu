@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
   const int nchunk = (P + 31) / 32;
   const int lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_cnt[e] = 0;
-  for (int i = threadIdx.x; i < 32 * kBatchedMaxExperts; i += blockDim.x) (&s_wc[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < nchunk * kBatchedMaxExperts / 2; i += blockDim.x)   // the chunks' rows
+    reinterpret_cast<uint32_t *>(&s_wc[0][0])[i] = 0u;
   if (threadIdx.x < 32) s_bn[threadIdx.x] = 0;
   if (threadIdx.x < 32 * kBatchedMaxExperts / 32) (&s_bmask[0][0])[threadIdx.x] = 0u;
   __syncthreads();

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kPrepThreads) batched_prep_kernel(BatchedParam
   __shared__ int s_off[kBatchedMaxExperts + 1];
   __shared__ int s_e[1024];
   __shared__ unsigned char s_rank[1024];
-  __shared__ unsigned short s_wc[32][kBatchedMaxExperts];   // [chunk][expert]
+  __shared__ __align__(16) unsigned short s_wc[32][kBatchedMaxExperts];   // [chunk][expert]
   // the active list, most tokens first (longest processing time first): an
   // active expert's bucket is b = min(count, 31); its place is the number of
   // experts in higher buckets plus those of lower id in its own (the bit

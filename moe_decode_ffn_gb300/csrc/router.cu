@@ -251,8 +251,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterParam
   const uint32_t epoch = __ldcg(&p.epochs[chunk]) + 1u;
   __shared__ float s_part[kMaxChunkTokens][kRouterWarps];
   // TG tokens at a time: their activation vectors are all requested before
-  // the first product (at most 8 vectors per lane in flight; one token at a
-  // time for rows of 4 or more vectors per lane, which hold enough loads)
+  // the first product (4 vectors per lane in flight, which keeps the kernel
+  // at the registers of one token at a time; rows of 4 or more vectors per
+  // lane already hold that many loads)
   constexpr int TG = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
   for (int tb = t0; tb < t1; tb += TG) {
     XRaw<XT, VEC> xr[TG][NCH];

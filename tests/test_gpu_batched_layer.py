@@ -60,6 +60,27 @@ def test_batched_layer_equals_single_token_layers_and_the_oracle(T):
         _oracle_check(SPEC, 500, 0, x[t], res[t], out, t, f"token {t}")
 
 
+# 256 experts (the most the grouping takes), I=512: the longest-first active
+# list over all 8 words of expert bits, several rows per router block
+SPEC_256 = gen.LayerSpec(n_experts=256, inter=512, shared_inter=0, shared_type="q4_k")
+
+
+@pytest.mark.parametrize("T", [16, 64])
+def test_batched_layer_256_experts_equals_single_token_layers(T):
+    dev = device_layer(SPEC_256, 520, 0)
+    x = gen.make_tokens(521 + T, T).cuda()
+    res = gen.make_tokens(621 + T, T).cuda()
+    out = m.si_moe_layer_decode_batched(dev, x, res, mode=m.SI_FFN_AUTO)
+    ws = m.workspace(m.layer_workspace_bytes(dev))
+    torch.cuda.synchronize()
+    for t in range(T):
+        one = m.si_moe_layer_decode(dev, x[t], res[t], ws=ws)
+        for key in ("ids", "w", "sum", "y", "routed"):
+            assert torch.equal(out[key][t], one[key]), (t, key)
+    assert m.si_workspace_status(ws) == m.SI_OK
+    _oracle_check(SPEC_256, 520, 0, x[T - 1], res[T - 1], out, T - 1, f"token {T - 1}")
+
+
 def test_batched_layer_auto_mode_is_the_integer_mode():
     dev = device_layer(SPEC, 500, 0)
     x = gen.make_tokens(505, 16).cuda()

@@ -122,3 +122,14 @@ def test_router_chunks_equal_single_token_calls(n_tokens, n_experts, w_fp32, hid
         assert torch.equal(logits[t:t + 1], l1), t
         assert torch.equal(ids[t:t + 1], i1), t
         assert torch.equal(w[t:t + 1], w1), t
+
+
+@pytest.mark.parametrize("top_k", [1, 5])
+def test_router_chunks_smaller_top_k_equal_single_token_calls(top_k):
+    W = gen.to_bf16(gen.normal([gen.stream_key(7, top_k)], 128 * 2048, 0.0, 0.02)[0]).reshape(128, 2048).cuda()
+    X = gen.make_tokens(36, 40).cuda()
+    ids, w, _ = m.si_moe_router_topk(X, W, top_k)
+    for t in range(40):
+        i1, w1, _ = m.si_moe_router_topk(X[t:t + 1], W, top_k)
+        assert torch.equal(ids[t:t + 1], i1), t
+        assert torch.equal(w[t:t + 1], w1), t

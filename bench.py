@@ -737,6 +737,74 @@ def run_kernels(args):
     return 0 if st == m.SI_OK else 1
 
 
+def run_phase_trace(args):
+    """Where the time of one persistent-kernel iteration goes, from the
+    profiling build (libsi_moe_trace.so, -DSI_TRACE): thread 0 of every block
+    stamps %globaltimer at the start of the last iteration of a launch and at
+    one selected phase. Every phase gets `launches` launches of the stack of
+    `layers` Q4_K layers x `tokens` tokens; the table gives, per phase, the
+    median over blocks of the time after the iteration start (mean over the
+    launches), less the stall of one stamp (phase 14 sits right after the
+    start stamp). Not a measurement of the product build."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import gen
+    import moe_decode_ffn_gb300 as m
+    from moe_decode_ffn_gb300 import _build
+
+    m.LIB = _build.build(trace=True)
+    lib = m.library()
+    lib.si_trace_dump_stack.argtypes = [ctypes.c_void_p]
+    lib.si_trace_stack_phase.argtypes = [ctypes.c_int]
+    layers = [m.device_layer(gen.Q4K_LAYER_SHARED_Q4_K, args.seed, l) for l in range(args.layers)]
+    x = gen.make_tokens(args.seed, args.tokens, device="cuda")
+    g = m.StackGraph(layers, x)
+    if not g.persistent:
+        print("the persistent kernel does not take these layers")
+        return 1
+    lib.si_trace_stack_phase(-1)
+    for _ in range(3):
+        g.launch()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        g.launch()
+    e1.record()
+    torch.cuda.synchronize()
+    lt = args.layers * args.tokens
+    print(f"profiling build without stamps: {e0.elapsed_time(e1) * 1e3 / 5 / lt:.3f} us per layer-token")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    names = {1: "fold done (X3 in)", 2: "logits written (X1 out)", 3: "Q8_1 of y done",
+             4: "logits in, sorted", 5: "ranked", 6: "copies issued, softmax", 7: "gate/up dots done",
+             8: "h written (X2 out)", 9: "h gathered (X2 in)", 10: "down rows ready", 11: "down dots",
+             12: "rows written (X3 out)", 13: "next fold done"}
+    res = {}
+    for ph in [14] + list(range(1, 14)):
+        lib.si_trace_stack_phase(ph)
+        rows = []
+        for _ in range(args.launches):
+            g.launch()
+            torch.cuda.synchronize()
+            buf = np.zeros(4 * 1024 * 16, dtype=np.uint64)
+            lib.si_trace_dump_stack(buf.ctypes.data)
+            t = buf.reshape(4, 1024, 16)[0, :sms, :].astype(np.float64)
+            ok = (t[:, ph] > 0) & (t[:, 0] > 0)
+            rows.append(np.where(ok, t[:, ph] - np.median(t[:, 0]), np.nan))
+        res[ph] = np.stack(rows)
+    st = m.si_workspace_status(g.ws)
+    g.close()
+    stall = np.nanmean(np.nanmedian(res[14], axis=1))
+    print(f"stamp stall {stall / 1e3:.3f} us (subtracted)")
+    for ph in range(1, 14):
+        v = res[ph] - stall
+        print(f"{ph:2d} {names[ph]:26s} {np.nanmean(np.nanmedian(v, 1)) / 1e3:7.3f} us")
+    print(f"status={m.status_string(st)}")
+    return 0 if st == m.SI_OK else 1
+
+
 def run_profile_case(args):
     """A bounded run for profilers (ncu), not a measurement: seeded layers,
     n_tokens tokens through n_layers layers captured as one CUDA graph and
@@ -820,6 +888,9 @@ def main():
                     help="instead of the headline line, one line per kernel of the four-kernel layer")
     pc = ap.add_argument_group("--profile-case", "a bounded run for profilers (not a measurement)")
     pc.add_argument("--profile-case", action="store_true")
+    pc.add_argument("--phase-trace", action="store_true",
+                    help="phase timings of the persistent kernel from the profiling build (uses --layers, "
+                         "--tokens, --launches, --seed)")
     pc.add_argument("--layers", type=int, default=4)
     pc.add_argument("--tokens", type=int, default=8)
     pc.add_argument("--launches", type=int, default=3)
@@ -836,6 +907,8 @@ def main():
     args = ap.parse_args()
     if args.profile_case:
         return run_profile_case(args)
+    if args.phase_trace:
+        return run_phase_trace(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
